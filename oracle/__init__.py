@@ -1,0 +1,186 @@
+"""CPU oracle for the Lightning Indexer — TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``indexer_oracle.c`` (plain C11, fp64); this module
+only compiles it with gcc and marshals numpy arrays through ctypes. Only the
+tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may
+import it. The CUDA library never imports it, and it imports nothing from the
+CUDA library.
+
+Method source: Hugging Face discussion "Notes from an NVFP4 port of Kimi K3.1
+Pro" — the indexer paragraph and item (4) of "Details that silently change the
+answer". All functions here are pinned by ``tests/test_oracle.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "indexer_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+HEADS = 32
+DIM = 128
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc, no GPU)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"],
+                       check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i64, i32 = ctypes.c_int64, ctypes.c_int32
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_key_layernorm.argtypes = [P, P, P, ctypes.c_double, i64, P, P]
+            lib.oracle_key_layernorm.restype = None
+            lib.oracle_scores.argtypes = [P, P, P, i64, P]
+            lib.oracle_scores.restype = None
+            lib.oracle_select.argtypes = [P, i64, i32, P]
+            lib.oracle_select.restype = i64
+            lib.oracle_score_topk.argtypes = [P, P, P, P, P, P, i32, i32, P, P, P, i64, i64, i64]
+            lib.oracle_score_topk.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of bf16 bit patterns, as float64 (bf16 = top half of fp32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """Round float64 values to bf16 (nearest, ties to even), one rounding step."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    flat_in, flat_out = x.reshape(-1), out.reshape(-1)
+    for i in range(flat_in.size):
+        flat_out[i] = lib.oracle_double_to_bf16(float(flat_in[i]))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the indexer
+# ---------------------------------------------------------------------------
+
+def key_layernorm(k_raw_bits, gamma, beta, eps: float):
+    """LayerNorm of each 128-wide key row -> (bf16 bits [n,128], fp64 [n,128]).
+
+    ``gamma``/``beta`` are given as exact float64 values of the parameters.
+    """
+    lib = _load()
+    k_raw = _c(k_raw_bits, np.uint16).reshape(-1, DIM)
+    g = _c(gamma, np.float64).reshape(DIM)
+    b = _c(beta, np.float64).reshape(DIM)
+    n = k_raw.shape[0]
+    out = np.empty((n, DIM), dtype=np.uint16)
+    y = np.empty((n, DIM), dtype=np.float64)
+    lib.oracle_key_layernorm(_ptr(k_raw), _ptr(g), _ptr(b), float(eps), n, _ptr(out), _ptr(y))
+    return out, y
+
+
+def scores(q_t_bits, k_seq_bits, w_t, n: int) -> np.ndarray:
+    """S[s] = sum_h w[h] relu(q_h . k_s) for s < n, in fp64 (one query)."""
+    lib = _load()
+    q = _c(q_t_bits, np.uint16).reshape(HEADS * DIM)
+    k = _c(k_seq_bits, np.uint16).reshape(-1, DIM)
+    w = _c(w_t, np.float32).reshape(HEADS)
+    assert k.shape[0] >= n
+    S = np.empty(max(n, 1), dtype=np.float64)
+    lib.oracle_scores(_ptr(q), _ptr(k), _ptr(w), n, _ptr(S))
+    return S[:n]
+
+
+def select(S, K: int) -> np.ndarray:
+    """Exact top-K of one score row under the tie/order rule -> int32 [K] (-1 padded)."""
+    lib = _load()
+    s = _c(S, np.float64).reshape(-1)
+    out = np.empty(K, dtype=np.int32)
+    r = lib.oracle_select(_ptr(s), s.size, int(K), _ptr(out))
+    if r < 0:
+        raise MemoryError("oracle_select")
+    return out
+
+
+def score_topk(q_bits, k_bits, w, q_pos, cu_q, cu_k, K: int = 2048, rows=None,
+               want_scores: bool = False, threads: int = 1):
+    """Indexer over a packed ragged batch.
+
+    Returns (idx [T,K] int32, cnt [T] int32, scores [T,ld] float64 or None).
+    ``rows`` restricts the work to an iterable of query rows (other rows of idx
+    stay -1 and cnt 0). ``threads`` > 1 runs disjoint row subsets in parallel
+    threads (each a separate call of the same C function).
+    """
+    lib = _load()
+    q = _c(q_bits, np.uint16).reshape(-1, HEADS, DIM)
+    k = _c(k_bits, np.uint16).reshape(-1, DIM)
+    w_ = _c(w, np.float32).reshape(-1, HEADS)
+    qp = _c(q_pos, np.int32).reshape(-1)
+    cq = _c(cu_q, np.int32).reshape(-1)
+    ck = _c(cu_k, np.int32).reshape(-1)
+    T, B = q.shape[0], cq.size - 1
+    idx = np.full((T, K), -1, dtype=np.int32)
+    cnt = np.zeros(T, dtype=np.int32)
+    ld = int(qp.max()) + 1 if (want_scores and T) else 0
+    sc = np.full((T, ld), np.nan, dtype=np.float64) if want_scores else None
+    row_list = list(range(T)) if rows is None else sorted(set(int(r) for r in rows))
+
+    def run(r0, r1):
+        rc = lib.oracle_score_topk(_ptr(q), _ptr(k), _ptr(w_), _ptr(qp), _ptr(cq), _ptr(ck),
+                                   B, int(K), _ptr(idx), _ptr(cnt), _ptr(sc), ld, r0, r1)
+        if rc != 0:
+            raise ValueError("oracle_score_topk: query position outside its sequence")
+
+    # contiguous runs of requested rows
+    runs = []
+    for r in row_list:
+        if runs and runs[-1][1] == r:
+            runs[-1][1] = r + 1
+        else:
+            runs.append([r, r + 1])
+    if threads <= 1 or len(row_list) <= 1:
+        for r0, r1 in runs:
+            run(r0, r1)
+    else:
+        # split into single rows, handed to a thread pool (ctypes drops the GIL)
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda r: run(r, r + 1), row_list))
+    return idx, cnt, sc

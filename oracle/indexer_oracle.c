@@ -1,0 +1,240 @@
+/*
+ * Lightning Indexer — CPU oracle (TEST INFRASTRUCTURE ONLY).
+ *
+ * This file is the plain, slow, obviously-correct definition of what the
+ * indexer computes. Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load it. The product path (the CUDA library under
+ * sparse_attention_key_gb300/) never calls, links or includes it, and it
+ * shares no code, header, table or helper with that path.
+ *
+ * Source of the method: the Hugging Face discussion "Notes from an NVFP4 port
+ * of Kimi K3.1 Pro" (moonshotai/Kimi-K3.1-Pro, discussion 7), its paragraph
+ * on the indexer ("The indexer is the entire delta ...") and item (4) of its
+ * list "Details that silently change the answer". Readings of that text that
+ * the page leaves open are stated at each function.
+ *
+ * Arithmetic: IEEE fp64 throughout, inputs converted exactly from bf16/fp32.
+ * Build: plain C11, no intrinsics, no OpenMP, no -ffast-math:
+ *     gcc -O2 -std=c11 -fPIC -shared indexer_oracle.c -o liboracle.so -lm
+ *
+ * Parity pins (tests/test_oracle.py, run without a GPU):
+ *   - oracle_select: hand-derived tie-rule cases (tests/golden/), brute force
+ *     over all subsets on tiny rows, keep-all for n <= K, all-equal rows,
+ *     distinct-score rows against an independent sort, +0/-0 equality.
+ *   - oracle_scores: a single nonzero head against a library GEMM (numpy
+ *     float64 matmul + relu), linearity in the head weights, causal length.
+ *   - oracle_key_layernorm: constant rows, +/-a rows (closed form), and the
+ *     fp64 result against torch.nn.functional.layer_norm in float64; the
+ *     bf16 rounding against the fp32 round-to-nearest-even bit rule.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define IDX_HEADS 32   /* "32 heads" */
+#define IDX_DIM 128    /* "of 128 dimensions"; also the LayerNorm width */
+
+/* ---------------------------------------------------------------------------
+ * Number formats
+ * ------------------------------------------------------------------------- */
+
+/* bf16 bit pattern -> exact double (bf16 is the top half of an IEEE fp32). */
+double oracle_bf16_to_double(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * double -> bf16, round to nearest, ties to even, in one rounding step.
+ * bf16 has 8 significant bits for normal numbers (exponent >= -126) and a
+ * fixed quantum of 2^-133 below that. The quantum q of x is a power of two,
+ * x/q is exact in double, rint() rounds it to an integer in the current
+ * (default: nearest-even) mode, and the product is the rounded value, which
+ * is exactly representable in fp32 and therefore in bf16.
+ */
+uint16_t oracle_double_to_bf16(double x) {
+    if (isnan(x)) return (uint16_t)0x7FC0;
+    if (x == 0.0) return signbit(x) ? (uint16_t)0x8000 : (uint16_t)0x0000;
+    if (isinf(x)) return signbit(x) ? (uint16_t)0xFF80 : (uint16_t)0x7F80;
+    int e;
+    (void)frexp(x, &e);        /* |x| = m * 2^e with m in [0.5, 1) */
+    int exp_unbiased = e - 1;  /* |x| in [2^exp_unbiased, 2^(exp_unbiased+1)) */
+    if (exp_unbiased < -126) exp_unbiased = -126;
+    double q = ldexp(1.0, exp_unbiased - 7);
+    double r = rint(x / q) * q;
+    if (fabs(r) >= ldexp(1.0, 128)) return signbit(x) ? (uint16_t)0xFF80 : (uint16_t)0x7F80;
+    float f = (float)r;        /* exact */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* ---------------------------------------------------------------------------
+ * Step 1 — key LayerNorm.
+ * The page: the key comes "from the attention input through a 128-wide
+ * LayerNorm that carries both a weight and a bias". Reading: the standard
+ * LayerNorm over the 128 features of one key, biased variance, eps inside
+ * the square root, y = (x - mean) / sqrt(var + eps) * gamma + beta; the
+ * result is stored in the 16-bit key cache (the page keeps the indexer in
+ * 16-bit), rounded to bf16 nearest-even.
+ *
+ * k_raw   [n_rows,128] bf16 bits (host)
+ * gamma   [128] double, beta [128] double (exact copies of the parameters)
+ * k_out   [n_rows,128] bf16 bits (host)
+ * y_exact [n_rows,128] double, or NULL: the unrounded fp64 result
+ * ------------------------------------------------------------------------- */
+void oracle_key_layernorm(const uint16_t* k_raw, const double* gamma, const double* beta,
+                          double eps, int64_t n_rows, uint16_t* k_out, double* y_exact) {
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const uint16_t* x = k_raw + r * IDX_DIM;
+        double mean = 0.0;
+        for (int d = 0; d < IDX_DIM; ++d) mean += oracle_bf16_to_double(x[d]);
+        mean /= IDX_DIM;
+        double var = 0.0;
+        for (int d = 0; d < IDX_DIM; ++d) {
+            double c = oracle_bf16_to_double(x[d]) - mean;
+            var += c * c;
+        }
+        var /= IDX_DIM;
+        double inv = 1.0 / sqrt(var + eps);
+        for (int d = 0; d < IDX_DIM; ++d) {
+            double y = (oracle_bf16_to_double(x[d]) - mean) * inv * gamma[d] + beta[d];
+            if (y_exact) y_exact[r * IDX_DIM + d] = y;
+            k_out[r * IDX_DIM + d] = oracle_double_to_bf16(y);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Steps 2-3 — head scores, relu, head-weighted sum, for one query.
+ * The page: "32 heads of 128 dimensions scoring relu(q.k) against the whole
+ * causal history", and "a per-head weight vector sums the heads before the
+ * select". Reading: S[s] = sum_h w[h] * max(q_h . k_s, 0) for every key s of
+ * the causal history 0..n-1 (n = query position + 1). There is no rotary
+ * (index_rope_dim is 0, item (3) of the page's list). No scale factor is
+ * printed; any scale is taken to be folded into w.
+ *
+ * q_t [32,128] bf16 bits, k_seq [n,128] bf16 bits (the sequence's post-LN
+ * keys), w_t [32] fp32, S_out [n] double.
+ * ------------------------------------------------------------------------- */
+void oracle_scores(const uint16_t* q_t, const uint16_t* k_seq, const float* w_t, int64_t n,
+                   double* S_out) {
+    double q[IDX_HEADS][IDX_DIM];
+    for (int h = 0; h < IDX_HEADS; ++h)
+        for (int d = 0; d < IDX_DIM; ++d) q[h][d] = oracle_bf16_to_double(q_t[h * IDX_DIM + d]);
+    double k[IDX_DIM];
+    for (int64_t s = 0; s < n; ++s) {
+        for (int d = 0; d < IDX_DIM; ++d) k[d] = oracle_bf16_to_double(k_seq[s * IDX_DIM + d]);
+        double S = 0.0;
+        for (int h = 0; h < IDX_HEADS; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < IDX_DIM; ++d) dot += q[h][d] * k[d];
+            double relu = dot > 0.0 ? dot : 0.0;
+            S += (double)w_t[h] * relu;
+        }
+        S_out[s] = S;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Steps 4-5 — exact top-K with the page's tie and order rule.
+ * The page keeps "the best 2048 positions exactly"; item (4): crossing the
+ * top-k boundary is a tie, and the output lists the positions strictly above
+ * the threshold in ascending order first, then the boundary group from the
+ * lowest position up — not a value-sorted list. When the history holds K or
+ * fewer keys every key is kept ("the selection is dormant"), in ascending
+ * order (the sparse path equals the dense one).
+ *
+ * Reading of the threshold: sort all n positions by (score descending,
+ * position ascending); tau is the score of the K-th entry. The first K
+ * entries are kept: those with score > tau (fewer than K) and the lowest
+ * positions of the group with score == tau. Scores compare numerically, so
+ * -0 equals +0.
+ *
+ * S [n] double; idx_out [K] int32, filled with the selection and then -1.
+ * Returns the number of positions emitted, min(n, K).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    double score;
+    int64_t pos;
+} oracle_entry;
+
+static int oracle_entry_order(const void* pa, const void* pb) {
+    const oracle_entry* a = (const oracle_entry*)pa;
+    const oracle_entry* b = (const oracle_entry*)pb;
+    if (a->score > b->score) return -1;  /* higher score first */
+    if (a->score < b->score) return 1;
+    if (a->pos < b->pos) return -1;      /* then lower position first */
+    if (a->pos > b->pos) return 1;
+    return 0;
+}
+
+static int oracle_pos_ascending(const void* pa, const void* pb) {
+    int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+    return (a > b) - (a < b);
+}
+
+int64_t oracle_select(const double* S, int64_t n, int32_t K, int32_t* idx_out) {
+    for (int32_t i = 0; i < K; ++i) idx_out[i] = -1;
+    if (n <= 0) return 0;
+    if (n <= K) {  /* dormant selection: every position, ascending */
+        for (int64_t s = 0; s < n; ++s) idx_out[s] = (int32_t)s;
+        return n;
+    }
+    oracle_entry* e = (oracle_entry*)malloc((size_t)n * sizeof *e);
+    if (!e) return -1;
+    for (int64_t s = 0; s < n; ++s) {
+        e[s].score = S[s];
+        e[s].pos = s;
+    }
+    qsort(e, (size_t)n, sizeof *e, oracle_entry_order);
+    double tau = e[K - 1].score;
+    int32_t out = 0;
+    for (int32_t i = 0; i < K; ++i)          /* strictly above the threshold */
+        if (e[i].score > tau) idx_out[out++] = (int32_t)e[i].pos;
+    int32_t n_above = out;
+    qsort(idx_out, (size_t)n_above, sizeof *idx_out, oracle_pos_ascending);
+    for (int32_t i = 0; i < K; ++i)          /* the boundary group's kept part */
+        if (e[i].score == tau) idx_out[out++] = (int32_t)e[i].pos;
+    qsort(idx_out + n_above, (size_t)(out - n_above), sizeof *idx_out, oracle_pos_ascending);
+    free(e);
+    return out;
+}
+
+/* ---------------------------------------------------------------------------
+ * The whole indexer over a packed ragged batch, for query rows
+ * [row_begin, row_end). Layout (the same one the CUDA library uses):
+ *   q [T,32,128] bf16, k [cu_k[B],128] bf16 (post-LN cache), w [T,32] fp32,
+ *   q_pos [T] int32 (position of the query within its sequence),
+ *   cu_q [B+1], cu_k [B+1] int32 (sequence b owns query rows cu_q[b]..cu_q[b+1]
+ *   and key rows cu_k[b]..cu_k[b+1]).
+ * Output: idx [T,K] int32 sequence-local positions padded with -1;
+ *   cnt [T] int32 (number emitted) or NULL; scores_out [T,ld] double or NULL
+ *   (the row's n scores; the rest untouched).
+ * Returns 0, or -1 on an argument error (position outside its sequence).
+ * ------------------------------------------------------------------------- */
+int oracle_score_topk(const uint16_t* q, const uint16_t* k, const float* w, const int32_t* q_pos,
+                      const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t K,
+                      int32_t* idx, int32_t* cnt, double* scores_out, int64_t ld,
+                      int64_t row_begin, int64_t row_end) {
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t len_k = (int64_t)cu_k[b + 1] - cu_k[b];
+        for (int64_t t = cu_q[b]; t < cu_q[b + 1]; ++t) {
+            if (t < row_begin || t >= row_end) continue;
+            int64_t n = (int64_t)q_pos[t] + 1;  /* causal: keys 0..q_pos inclusive */
+            if (q_pos[t] < 0 || n > len_k) return -1;
+            double* S = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof *S);
+            if (!S) return -1;
+            oracle_scores(q + t * IDX_HEADS * IDX_DIM, k + (int64_t)cu_k[b] * IDX_DIM,
+                          w + t * IDX_HEADS, n, S);
+            int64_t c = oracle_select(S, n, K, idx + t * K);
+            if (cnt) cnt[t] = (int32_t)c;
+            if (scores_out) memcpy(scores_out + t * ld, S, (size_t)n * sizeof *S);
+            free(S);
+        }
+    }
+    return 0;
+}

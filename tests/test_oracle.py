@@ -1,0 +1,343 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: values fixed
+by the page's rule (hand-derived golden cases), brute force over all subsets,
+closed forms, special cases that reduce to a library routine (numpy/torch
+float64), and invariants. Method source: "Notes from an NVFP4 port of Kimi
+K3.1 Pro" (indexer paragraph; item (4) of "Details that silently change the
+answer"; the closing paragraph on dormant selection).
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_key_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "tie_rule_cases.txt")
+
+
+def _golden_cases():
+    cases = []
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, s, e = (p.strip() for p in line.split("|"))
+            cases.append((int(k), [float(x) for x in s.split()], [int(x) for x in e.split()]))
+    return cases
+
+
+# ---------------------------------------------------------------------------
+# select: the tie / order rule
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K,scores,expected", _golden_cases())
+def test_select_golden_tie_rule(K, scores, expected):
+    got = oracle.select(np.array(scores), K)
+    assert got.tolist() == expected
+
+
+def _rule_order(S, sel):
+    """The page's output order for a selected set: above-threshold ascending, then the tie group."""
+    tau = min(S[a] for a in sel)
+    return sorted(a for a in sel if S[a] > tau) + sorted(a for a in sel if S[a] == tau)
+
+
+def test_select_brute_force_all_subsets():
+    rng = np.random.default_rng(11)
+    checked = 0
+    for n in range(2, 10):
+        for K in range(1, n):
+            for _ in range(6):
+                S = rng.integers(0, 4, size=n).astype(np.float64)  # heavy ties
+                valid = []
+                for sel in itertools.combinations(range(n), K):
+                    ss = set(sel)
+                    ok = all(S[a] > S[b] or (S[a] == S[b] and a < b)
+                             for a in ss for b in range(n) if b not in ss)
+                    if ok:
+                        valid.append(sel)
+                assert len(valid) == 1, "the defining property must give a unique set"
+                got = oracle.select(S, K)
+                assert sorted(got.tolist()) == list(valid[0])
+                assert got.tolist() == _rule_order(S, valid[0])
+                checked += 1
+    assert checked > 100
+
+
+def test_select_keep_all_when_history_fits():
+    rng = np.random.default_rng(12)
+    for n in (1, 5, 2047, 2048):
+        S = rng.standard_normal(n)
+        got = oracle.select(S, 2048)
+        assert got[:n].tolist() == list(range(n))
+        assert (got[n:] == -1).all()
+
+
+def test_select_empty_row():
+    got = oracle.select(np.zeros(0), 4)
+    assert got.tolist() == [-1, -1, -1, -1]
+
+
+def test_select_all_equal_keeps_lowest_positions():
+    for n in (2049, 5000):
+        got = oracle.select(np.full(n, 0.75), 2048)
+        assert got.tolist() == list(range(2048))
+
+
+def test_select_distinct_scores_against_library_sort():
+    rng = np.random.default_rng(13)
+    for n, K in ((3000, 2048), (10000, 2048), (50, 7)):
+        S = rng.permutation(n).astype(np.float64) * 0.5 - 100.0  # distinct
+        order = np.argsort(-S, kind="stable")
+        top = order[:K]
+        # distinct scores: all but the K-th are above tau (ascending), then the K-th
+        expected = sorted(top[:K - 1].tolist()) + [int(top[K - 1])]
+        assert oracle.select(S, K).tolist() == expected
+
+
+def test_select_signed_zero_compares_equal():
+    S = np.array([0.0, -0.0, -0.0, 0.0, 1.0])
+    assert oracle.select(S, 3).tolist() == [4, 0, 1]
+    S2 = np.array([-0.0, 0.0, 0.0])
+    assert oracle.select(S2, 2).tolist() == [0, 1]
+
+
+def test_select_invariants_random_rows():
+    rng = np.random.default_rng(14)
+    for trial in range(20):
+        n = int(rng.integers(2049, 9000))
+        kind = trial % 3
+        if kind == 0:
+            S = rng.integers(0, 8, size=n).astype(np.float64)
+        elif kind == 1:
+            S = rng.standard_normal(n)
+        else:
+            S = np.maximum(rng.standard_normal(n), 0.0)
+        got = oracle.select(S, 2048)
+        assert got.size == 2048 and (got >= 0).all() and (got < n).all()
+        assert len(set(got.tolist())) == 2048
+        tau = S[got].min()
+        above = [a for a in got.tolist() if S[a] > tau]
+        ties = [a for a in got.tolist() if S[a] == tau]
+        assert got.tolist() == above + ties
+        assert above == sorted(above) and ties == sorted(ties)
+        assert len(above) == int((S > tau).sum())       # every above-tau key kept
+        tie_all = np.flatnonzero(S == tau)
+        assert ties == tie_all[:len(ties)].tolist()     # lowest positions of the tie group
+
+
+# ---------------------------------------------------------------------------
+# scores: relu(q_h . k), head-weighted sum, causal history
+# ---------------------------------------------------------------------------
+
+def _rand_qk(rng, n):
+    k = wl.f32_to_bf16_bits(rng.standard_normal((n, 128), dtype=np.float32))
+    q = wl.f32_to_bf16_bits(rng.standard_normal((32, 128), dtype=np.float32))
+    return q, k
+
+
+def test_scores_single_head_is_relu_of_a_gemm():
+    rng = np.random.default_rng(21)
+    q, k = _rand_qk(rng, 300)
+    qf = oracle.bf16_bits_to_f64(q)
+    kf = oracle.bf16_bits_to_f64(k)
+    for h in (0, 7, 31):
+        w = np.zeros(32, np.float32)
+        w[h] = 1.0
+        got = oracle.scores(q, k, w, 300)
+        ref = np.maximum(kf @ qf[h], 0.0)            # library GEMV, float64
+        assert (ref == 0).sum() > 50                  # the relu is exercised
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_scores_linear_in_head_weights():
+    """S(w) = sum_h w_h S(e_h), for weights of either sign (relu before the weight)."""
+    rng = np.random.default_rng(22)
+    q, k = _rand_qk(rng, 200)
+    basis = []
+    for h in range(32):
+        e = np.zeros(32, np.float32)
+        e[h] = 1.0
+        basis.append(oracle.scores(q, k, e, 200))
+    basis = np.stack(basis)
+    w = rng.uniform(-1, 1, size=32).astype(np.float32)
+    got = oracle.scores(q, k, w, 200)
+    ref = w.astype(np.float64) @ basis
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_scores_integer_inputs_are_exact_integers():
+    rng = np.random.default_rng(23)
+    k = wl.f32_to_bf16_bits(rng.integers(-2, 3, (64, 128)).astype(np.float32))
+    q = wl.f32_to_bf16_bits(rng.integers(-2, 3, (32, 128)).astype(np.float32))
+    w = rng.integers(0, 2, 32).astype(np.float32)
+    got = oracle.scores(q, k, w, 64)
+    assert np.array_equal(got, np.round(got))
+    qi = oracle.bf16_bits_to_f64(q).astype(np.int64)
+    ki = oracle.bf16_bits_to_f64(k).astype(np.int64)
+    ref = (np.maximum(ki @ qi.T, 0) * w.astype(np.int64)).sum(axis=1)   # integer GEMM
+    assert np.array_equal(got, ref.astype(np.float64))
+
+
+def test_causal_history_is_inclusive_and_bounded():
+    """A query at position p scores keys 0..p and nothing after."""
+    rng = np.random.default_rng(24)
+    L = 40
+    k = wl.f32_to_bf16_bits(rng.integers(-1, 2, (L, 128)).astype(np.float32) * 0.0)
+    q = np.zeros((3, 32, 128), np.uint16)
+    one = wl.f32_to_bf16_bits(np.ones(1, np.float32))[0]
+    q[:, 0, 0] = one                                   # head 0 reads feature 0
+    k = k.copy()
+    for s in (9, 10, 30):                              # keys with a large feature 0
+        k[s, 0] = wl.f32_to_bf16_bits(np.array([5.0], np.float32))[0]
+    w = np.zeros((3, 32), np.float32)
+    w[:, 0] = 1.0
+    q_pos = np.array([9, 29, 39], np.int32)
+    idx, cnt, sc = oracle.score_topk(q, k, w, q_pos, [0, 3], [0, L], K=1, want_scores=True)
+    # query at 9 sees key 9 (inclusive) -> picks it; at 29 the earliest max is 9; at 39 too
+    assert idx[:, 0].tolist() == [9, 9, 9]
+    assert cnt.tolist() == [1, 1, 1]
+    assert np.isfinite(sc[0, :10]).all() and np.isnan(sc[0, 10:]).all()
+    assert np.isfinite(sc[1, :30]).all() and np.isnan(sc[1, 30:]).all()
+    # K=2: the query at 9 cannot see key 10 or 30 (future) -> tie group of zeros fills in at 0
+    idx2, _, _ = oracle.score_topk(q, k, w, q_pos, [0, 3], [0, L], K=2)
+    assert idx2[0].tolist() == [9, 0]
+    assert idx2[1].tolist() == [9, 10]
+    assert idx2[2].tolist() == [9, 10]
+
+
+def test_keep_all_boundary_2047_vs_2048():
+    """Positions 2047 and 2048 straddle the 2048-key budget (keep-all vs drop-one)."""
+    rng = np.random.default_rng(25)
+    L = 2100
+    k = wl.f32_to_bf16_bits(rng.integers(-2, 3, (L, 128)).astype(np.float32))
+    q = wl.f32_to_bf16_bits(rng.integers(-2, 3, (2, 32, 128)).astype(np.float32))
+    w = np.ones((2, 32), np.float32)
+    idx, cnt, sc = oracle.score_topk(q, k, w, np.array([2047, 2048], np.int32), [0, 2], [0, L],
+                                     want_scores=True)
+    assert idx[0].tolist() == list(range(2048)) and cnt[0] == 2048
+    S = sc[1, :2049]
+    assert cnt[1] == 2048
+    dropped = set(range(2049)) - set(idx[1].tolist())
+    assert len(dropped) == 1
+    d = dropped.pop()
+    # the dropped key is the lowest-scoring one, and the highest position among those lowest
+    assert S[d] == S.min() and d == int(np.flatnonzero(S == S.min()).max())
+
+
+def test_ragged_batch_against_independent_numpy_restatement():
+    """A small ragged batch against numpy float64 matmuls + a library lexsort selection.
+
+    Not a pin on its own (it restates the definition); it checks the packed-batch
+    indexing (cu_q / cu_k offsets, per-sequence local positions) end to end.
+    """
+    w_ = wl.custom(31, q_counts=[3, 0, 5, 2], k_lens=[40, 7, 90, 33], kind="int2",
+                   positions="random", topk=16)
+    idx, cnt, _ = oracle.score_topk(w_.q, w_.k, w_.w, w_.q_pos, w_.cu_q, w_.cu_k, K=16)
+    kf = oracle.bf16_bits_to_f64(w_.k)
+    qf = oracle.bf16_bits_to_f64(w_.q)
+    for b in range(w_.B):
+        for t in range(w_.cu_q[b], w_.cu_q[b + 1]):
+            n = int(w_.q_pos[t]) + 1
+            keys = kf[w_.cu_k[b]:w_.cu_k[b] + n]
+            S = (np.maximum(keys @ qf[t].T, 0.0) * w_.w[t].astype(np.float64)).sum(axis=1)
+            if n <= 16:
+                exp = list(range(n)) + [-1] * (16 - n)
+            else:
+                order = np.lexsort((np.arange(n), -S))[:16]
+                exp = _rule_order(S, set(order.tolist()))
+            assert idx[t].tolist() == exp
+            assert cnt[t] == min(n, 16)
+
+
+def test_out_of_range_position_is_rejected():
+    w_ = wl.custom(32, q_counts=[1], k_lens=[10], kind="int2")
+    bad = w_.q_pos.copy()
+    bad[0] = 10
+    with pytest.raises(ValueError):
+        oracle.score_topk(w_.q, w_.k, w_.w, bad, w_.cu_q, w_.cu_k, K=4)
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm and bf16 rounding
+# ---------------------------------------------------------------------------
+
+def _bf16(vals):
+    return wl.f32_to_bf16_bits(np.asarray(vals, np.float32))
+
+
+def test_bf16_rounding_matches_fp32_bit_rule():
+    rng = np.random.default_rng(41)
+    x = np.concatenate([rng.standard_normal(5000).astype(np.float32) * 10,
+                        rng.standard_normal(1000).astype(np.float32) * 1e-30])
+    assert np.array_equal(oracle.f64_to_bf16_bits(x.astype(np.float64)), wl.f32_to_bf16_bits(x))
+
+
+def test_bf16_rounding_special_cases():
+    cases = [
+        (1.0 + 2.0 ** -8, 0x3F80),                 # halfway, ties to even (down)
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),             # halfway, ties to even (up)
+        (1.0 + 2.0 ** -8 + 2.0 ** -30, 0x3F81),    # just above halfway: one rounding step
+        (-(1.0 + 2.0 ** -8 + 2.0 ** -30), 0xBF81),
+        (2.0 ** -130, 0x0008),                     # subnormal, exact
+        (3 * 2.0 ** -134, 0x0002),                 # subnormal halfway -> even
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (2.5, 0x4020),
+    ]
+    for x, bits in cases:
+        assert int(oracle.f64_to_bf16_bits([x])[0]) == bits, x
+
+
+def test_layernorm_constant_row_gives_bias():
+    g = oracle.bf16_bits_to_f64(_bf16(np.linspace(0.5, 1.5, 128)))
+    b = oracle.bf16_bits_to_f64(_bf16(np.linspace(-1, 1, 128)))
+    x = np.tile(_bf16([3.25]), (2, 128))
+    out, y = oracle.key_layernorm(x, g, b, 1e-6)
+    assert np.array_equal(out[0], _bf16(b.astype(np.float32)))
+    assert np.array_equal(y[1], b)
+
+
+@pytest.mark.parametrize("a,gamma,beta,eps", [(1.0, 1.0, 0.0, 1e-6), (1.0, 2.0, 0.5, 1e-6),
+                                              (2.0 ** -10, 1.0, 0.0, 1e-6), (3.0, 0.5, -1.0, 1e-5)])
+def test_layernorm_plus_minus_a_closed_form(a, gamma, beta, eps):
+    """Row of +a/-a: mean 0, biased variance a^2 -> y = +-a/sqrt(a^2+eps)*gamma+beta."""
+    row = np.array([a if d % 2 == 0 else -a for d in range(128)])
+    x = _bf16(row)[None, :]
+    out, y = oracle.key_layernorm(x, np.full(128, gamma), np.full(128, beta), eps)
+    yp = a / np.sqrt(a * a + eps) * gamma + beta
+    ym = -a / np.sqrt(a * a + eps) * gamma + beta
+    exp = np.array([yp if d % 2 == 0 else ym for d in range(128)])
+    np.testing.assert_allclose(y[0], exp, rtol=1e-14, atol=1e-15)
+    assert np.array_equal(out[0], oracle.f64_to_bf16_bits(exp))
+    if (a, gamma, beta) == (1.0, 1.0, 0.0):
+        assert out[0, 0] == 0x3F80 and out[0, 1] == 0xBF80
+    if (a, gamma, beta) == (1.0, 2.0, 0.5):
+        assert out[0, 0] == 0x4020 and out[0, 1] == 0xBFC0
+
+
+def test_layernorm_against_torch_float64():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(42)
+    x = _bf16(rng.standard_normal((64, 128)).astype(np.float32) * 3 + 0.7)
+    g = oracle.bf16_bits_to_f64(_bf16(1 + 0.1 * rng.standard_normal(128)))
+    b = oracle.bf16_bits_to_f64(_bf16(0.1 * rng.standard_normal(128)))
+    out, y = oracle.key_layernorm(x, g, b, 1e-6)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(oracle.bf16_bits_to_f64(x)), (128,),
+                                         torch.from_numpy(g), torch.from_numpy(b), eps=1e-6)
+    np.testing.assert_allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(out, oracle.f64_to_bf16_bits(ref.numpy()))
+
+
+def test_workloads_shapes_and_pairs():
+    w1 = wl.tiny_exact()
+    assert w1.pairs == 18913 and w1.T == 8 and w1.L == 3072 and w1.exact
+    w3 = wl.prefill_ties(L=512)
+    assert w3.pairs == 512 * 513 // 2
+    w2 = wl.decode_batch()
+    assert w2.pairs == 249856 and w2.k is None and w2.k_raw.shape == (249856, 128)
