@@ -1,0 +1,435 @@
+"""Benchmark of the GB300 Lightning Indexer: query-key pairs/s of score + exact top-2048.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+
+One step = one pass of the whole indexer over one batch of the named workload:
+key LayerNorm (when the workload chains it), head scores with the relu/head-
+weighted epilogue, and the exact top-2048 with the tie/order rule. Inputs are
+resident in HBM when the timed region starts; L2 is flushed (a 256 MB write)
+between timed steps. Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (the plain fp64 definition) on the host's
+cores on a bounded row sample of the same workload, as the reference arm.
+
+Multi-GPU (torchrun): each rank runs an independent replica of the workload
+(the indexer has no exchange step); value = all ranks' pairs / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_key_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "indexer query-key pairs/s (score+exact top-2048); % of HBM / tensor roofline"
+UNIT = "pairs/s"
+DEFAULT_WORKLOAD = 2   # the decode batch: 8 sequences, one query each, 8K-64K keys
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for (ts, s) in self.samples if t0 <= ts <= t1] or [s for _, s in self.samples]
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(mhz)) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per launch
+# ---------------------------------------------------------------------------
+
+def algorithmic(w: wl.Workload):
+    """Per-call algorithmic work: flops, HBM bytes for score (unique keys, q, w, out) and LN."""
+    unique_keys = 0
+    for b in range(w.B):
+        q0, q1 = int(w.cu_q[b]), int(w.cu_q[b + 1])
+        if q1 > q0:
+            unique_keys += int(w.q_pos[q0:q1].max()) + 1
+    score_bytes = unique_keys * 256 + w.T * (32 * 128 * 2 + 32 * 4)
+    topk_bytes = w.T * w.topk * 4 + w.T * 4
+    ln_bytes = (w.k_raw.shape[0] * 512 + 2 * 128 * 2) if (w.k is None and w.k_raw is not None) else 0
+    return {"flops": 8192.0 * w.pairs, "score_bytes": score_bytes, "topk_bytes": topk_bytes,
+            "ln_bytes": ln_bytes, "unique_keys": unique_keys}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from sparse_attention_key_gb300 import build as lib_build
+    if rank == 0:
+        lib_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from sparse_attention_key_gb300 import binding as B
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = wl.by_index(args.workload)
+    chained_ln = w.k is None
+
+    def up(a, dt=None):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(dt) if dt is not None else x).to(dev)
+
+    q, wt, q_pos = up(w.q, torch.int16), up(w.w), up(w.q_pos)
+    cu_q, cu_k = up(w.cu_q), up(w.cu_k)
+    if chained_ln:
+        k_raw, ln_w, ln_b = up(w.k_raw, torch.int16), up(w.ln_w, torch.int16), up(w.ln_b, torch.int16)
+        k = torch.empty_like(k_raw)
+    else:
+        k = up(w.k, torch.int16)
+    T, K, max_len = w.T, w.topk, w.max_len
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    cnt = torch.empty((T,), dtype=torch.int32, device=dev)
+    ws = B.workspace(B.score_topk_workspace_size(w.B, T, max_len, K), dev)
+    ld = (max_len + 3) // 4 * 4
+    scores = torch.empty((T, ld), dtype=torch.float32, device=dev)
+    ws_small = B.workspace(max(B.score_workspace_size(w.B, T, max_len),
+                               B.topk_workspace_size(T, max_len, K)), dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if chained_ln:
+            B.key_layernorm(k_raw, ln_w, ln_b, w.eps, out=k)
+        B.score_topk(q, k, wt, q_pos, cu_q, cu_k, max_len, K, idx=idx, cnt=cnt, ws=ws)
+
+    def step_split(ev):
+        ev[0].record(stream)
+        if chained_ln:
+            B.key_layernorm(k_raw, ln_w, ln_b, w.eps, out=k)
+        ev[1].record(stream)
+        B.score(q, k, wt, q_pos, cu_q, cu_k, max_len, ld=ld, out=scores, ws=ws_small)
+        ev[2].record(stream)
+        B.topk(scores, q_pos_plus1, max_len, K, idx=idx, cnt=cnt, ws=ws_small)
+        ev[3].record(stream)
+
+    q_pos_plus1 = q_pos + 1
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    code, detail = B.get_status(ws)
+    if code != 0:
+        raise RuntimeError(f"device status {code} (detail {detail}) after warm-up")
+
+    cvd = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x]
+    clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else str(local_rank))
+    clocks.start()
+    time.sleep(0.3)
+
+    # ---- timed region: K steps of the fused call (plus the chained LayerNorm)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = B.kernel_launches()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    launches = B.kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+
+    # ---- per-kernel durations: the same kernels through the split entry points
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        step_split(evs[i])
+    torch.cuda.synchronize()
+    t_wall2 = time.time()
+    clocks.stop()
+    ln_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    score_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    topk_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+
+    # ---- end to end through the public API with host buffers
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_in = {"q": pinned(w.q.view(np.int16)), "w": pinned(w.w), "q_pos": pinned(w.q_pos),
+            "cu_q": pinned(w.cu_q), "cu_k": pinned(w.cu_k)}
+    if chained_ln:
+        h_in["k_raw"] = pinned(w.k_raw.view(np.int16))
+    else:
+        h_in["k"] = pinned(w.k.view(np.int16))
+    d_in = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in h_in.items()}
+    h_idx = torch.empty((T, K), dtype=torch.int32).pin_memory()
+    h_cnt = torch.empty((T,), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = h_idx.numel() * 4 + h_cnt.numel() * 4
+
+    def e2e_step():
+        for n, t in h_in.items():
+            d_in[n].copy_(t, non_blocking=True)
+        kk = d_in.get("k")
+        if chained_ln:
+            kk = B.key_layernorm(d_in["k_raw"], ln_w, ln_b, w.eps, out=k)
+        B.score_topk(d_in["q"], kk, d_in["w"], d_in["q_pos"], d_in["cu_q"], d_in["cu_k"], max_len,
+                     K, idx=idx, cnt=cnt, ws=ws)
+        h_idx.copy_(idx, non_blocking=True)
+        h_cnt.copy_(cnt, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e_start[i].record(stream)
+        e2e_step()
+        e_end[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(sum(s.elapsed_time(e) for s, e in zip(e_start, e_end)))
+    ok = np.array_equal(h_idx.numpy(), idx.cpu().numpy())
+
+    # max over ranks
+    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return
+
+    pairs = w.pairs
+    value = pairs * world * args.steps / (total_ms / 1e3)
+    e2e_value = pairs * world * args.steps / (e2e_ms / 1e3)
+    pk = peaks()
+    alg = algorithmic(w)
+    kernels = {
+        "key_layernorm": {"ms": ln_ms, "bytes": alg["ln_bytes"]},
+        "score": {"ms": score_ms, "bytes": alg["score_bytes"], "flops": alg["flops"]},
+        "topk": {"ms": topk_ms, "bytes": alg["topk_bytes"]},
+    }
+    dominant = max((k_ for k_ in kernels if kernels[k_]["ms"] > 0), key=lambda k_: kernels[k_]["ms"])
+    tensor_bound = w.T > w.B * 4   # many queries per sequence: the contraction dominates
+    if dominant == "score" and tensor_bound:
+        ach = alg["flops"] / (score_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"]}
+    else:
+        by = kernels[dominant]["bytes"]
+        ach = by / (kernels[dominant]["ms"] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"]}
+    roof.update({"kernel": dominant, "traffic": None, "peak_source": pk["source"]})
+
+    ck = clocks.summary(t_wall0, t_wall2)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.NAMES[args.workload], "B": w.B, "T": T, "L": w.L,
+                   "pairs_per_step": pairs, "topk": K, "max_len": max_len,
+                   "layernorm_in_step": chained_ln, "l2": "flushed (256 MB write) between steps",
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "matches_device_result": bool(ok)},
+        "gpu_launches": int(launches),
+        "kernels_ms": {k_: v["ms"] for k_, v in kernels.items()},
+        "roofline": roof,
+        "clocks": ck,
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args)
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(w: wl.Workload, budget_pairs: int):
+    """Rows of the workload, spread over its queries, totalling about budget_pairs."""
+    n = w.q_pos.astype(np.int64) + 1
+    order = np.argsort(np.random.default_rng(0).random(w.T))
+    rows, tot = [], 0
+    for t in order:
+        if tot >= budget_pairs and rows:
+            break
+        rows.append(int(t))
+        tot += int(n[t])
+    return sorted(rows), tot
+
+
+def _oracle_inputs(w: wl.Workload):
+    import oracle
+    if w.k is None:  # the chained LayerNorm, computed by the oracle itself
+        k, _ = oracle.key_layernorm(w.k_raw, oracle.bf16_bits_to_f64(w.ln_w),
+                                    oracle.bf16_bits_to_f64(w.ln_b), float(np.float32(w.eps)))
+        return k
+    return w.k
+
+
+def cpu_baseline(w: wl.Workload, args):
+    import oracle
+    cores = os.cpu_count() or 1
+    k = _oracle_inputs(w)
+    # calibrate: ~0.2 s single-row probe, then size the sample to ~10-20 s of work
+    rows, tot = _oracle_sample(w, 20_000)
+    t0 = time.time()
+    oracle.score_topk(w.q, k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, rows=rows, threads=cores)
+    rate = tot / max(time.time() - t0, 1e-6)
+    rows, tot = _oracle_sample(w, int(rate * args.cpu_seconds))
+    t0 = time.time()
+    oracle.score_topk(w.q, k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, rows=rows, threads=cores)
+    dt = time.time() - t0
+    return {"value": tot / dt, "unit": UNIT, "cores": min(cores, len(rows)), "kind": "oracle",
+            "sample": f"{len(rows)} of {w.T} query rows ({tot} pairs) of {wl.NAMES[args.workload]}, "
+                      f"fp64 C oracle, one thread per row, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    w = wl.by_index(args.workload)
+    k = _oracle_inputs(w)
+    cores = os.cpu_count() or 1
+    rows, tot = _oracle_sample(w, 20_000)
+    t0 = time.time()
+    oracle.score_topk(w.q, k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, rows=rows, threads=cores)
+    rate = tot / max(time.time() - t0, 1e-6)
+    per_step = max(1.0, min(10.0, 120.0 / max(args.steps + args.warmup, 1)))
+    rows, tot = _oracle_sample(w, int(rate * per_step))
+    for _ in range(args.warmup):
+        oracle.score_topk(w.q, k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, rows=rows[:1], threads=1)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle.score_topk(w.q, k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, rows=rows, threads=cores)
+    dt = time.time() - t0
+    value = tot * args.steps / dt
+    used = min(cores, len(rows))
+    sample = (f"{len(rows)} of {w.T} query rows ({tot} pairs) per step of "
+              f"{wl.NAMES[args.workload]}; fp64 C oracle, one thread per row")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.NAMES[args.workload], "B": w.B, "T": w.T, "L": w.L,
+                       "pairs_per_step": w.pairs, "topk": w.topk},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

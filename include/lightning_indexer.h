@@ -1,0 +1,168 @@
+/*
+ * lightning_indexer.h — C ABI of the GB300 (sm_103a) Lightning Indexer library.
+ *
+ * The Lightning Indexer is described in the Hugging Face discussion "Notes from
+ * an NVFP4 port of Kimi K3.1 Pro" (moonshotai/Kimi-K3.1-Pro, discussion 7):
+ *   - the indexer paragraph: each query has 32 heads of width 128; every key of
+ *     its causal past gets relu(q_h . k) per head, the heads are combined with
+ *     a per-head weight vector, and the 2048 highest-scoring positions are kept
+ *     with no approximation; keys are normalised by a 128-wide LayerNorm that
+ *     has a weight and a bias;
+ *   - list "Details that silently change the answer", item (3): the indexer
+ *     uses no rotary embedding (index_rope_dim = 0); item (4): the output
+ *     order and the tie rule at the top-K boundary;
+ *   - the closing paragraph: when a query's history holds no more than 2048
+ *     keys, nothing is dropped and every position is kept.
+ *
+ * Conventions shared by every entry point
+ *   Memory     All data pointers are DEVICE pointers to caller-owned memory on the
+ *              current CUDA device. The library never allocates device memory,
+ *              never frees, and never synchronises: all work is enqueued on
+ *              `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *              stream) and completes asynchronously.
+ *   bf16       bfloat16 tensors are arrays of uint16_t bit patterns.
+ *   Layout     Row-major, contiguous, with 16-byte aligned base pointers.
+ *   Batches    A packed ragged batch of B sequences: sequence b owns query rows
+ *              cu_q[b] .. cu_q[b+1]-1 and key rows cu_k[b] .. cu_k[b+1]-1 (both
+ *              int32 [B+1], non-decreasing, cu_q[0] = cu_k[0] = 0, cu_q[B] = T).
+ *              q_pos[t] is query t's position inside its sequence; the query
+ *              sees keys 0 .. q_pos[t] (its causal length is n(t) = q_pos[t]+1,
+ *              which must not exceed the sequence's key count).
+ *              Output positions are sequence-local (0-based within the sequence).
+ *   Errors     Arguments are checked on the host before anything is enqueued; a
+ *              failed check returns a non-zero idx_status and enqueues nothing.
+ *              Values that live on the device (cu_q, cu_k, q_pos, n_valid) are
+ *              checked by the kernels, which skip the offending row and record
+ *              IDX_ERR_DEVICE_ARG in the workspace's status word; read it with
+ *              idx_get_status. A CUDA launch failure returns IDX_ERR_CUDA.
+ *              idx_last_error() gives a message for the calling thread's last
+ *              failure.
+ *   Workspace  ws / ws_bytes: caller-owned device scratch, at least the size the
+ *              matching *_workspace_size function returns, 256-byte aligned. It
+ *              holds the status word, the tile plan and staged scores. Calls that
+ *              may overlap on the GPU need separate workspaces.
+ */
+#ifndef LIGHTNING_INDEXER_H
+#define LIGHTNING_INDEXER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define IDX_API __attribute__((visibility("default")))
+#else
+#define IDX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    IDX_OK = 0,
+    IDX_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad alignment, topk out of range */
+    IDX_ERR_UNSUPPORTED = 2,  /* the current device is not an sm_103 (GB300) GPU */
+    IDX_ERR_WORKSPACE = 3,    /* ws_bytes below the required size, or ws misaligned */
+    IDX_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (text in idx_last_error) */
+    IDX_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (status word) */
+    IDX_ERR_DEVICE_ARG = 6    /* a device-resident argument was out of range (status word) */
+} idx_status;
+
+enum {
+    IDX_HEADS = 32,      /* indexer heads */
+    IDX_DIM = 128,       /* head dimension = key width = LayerNorm width */
+    IDX_TOPK_MAX = 2048  /* positions kept per query */
+};
+
+enum { IDX_PARAM_BF16 = 0, IDX_PARAM_F32 = 1 };
+
+/*
+ * Key LayerNorm (indexer paragraph: indexer keys pass a 128-wide LayerNorm
+ * with a weight and a bias). For every row x of k_raw:
+ *     y = (x - mean(x)) / sqrt(var(x) + eps) * ln_w + ln_b
+ * with the biased variance, computed in fp32 and rounded to bf16
+ * (nearest-even) into k_out. Runs once per key when the indexer's key cache is
+ * filled; the scoring entry points take its output.
+ *   k_raw   bf16 [n_rows,128]        k_out  bf16 [n_rows,128] (may equal k_raw)
+ *   ln_w, ln_b  [128], bf16 (ln_dtype = IDX_PARAM_BF16) or fp32 (IDX_PARAM_F32)
+ *   n_rows  >= 0 (0 enqueues nothing)
+ */
+IDX_API idx_status idx_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
+                             int ln_dtype, float eps, uint16_t* k_out, int64_t n_rows,
+                             void* stream);
+
+/*
+ * Head scores (indexer paragraph: per-head relu of q_h . k over the causal
+ * past, combined with a per-head weight; item (3): no rotary):
+ *     scores[t*ld + s] = sum_h w[t,h] * max(sum_d q[t,h,d] * k[cu_k[b]+s, d], 0)
+ * for every query t (of sequence b) and every s < n(t), bf16 products with
+ * fp32 accumulation. Entries s >= n(t) of a row are left untouched.
+ *   q      bf16 [T,32,128]     k  bf16 [cu_k[B],128] (post-LayerNorm key cache)
+ *   w      fp32 [T,32]         q_pos, cu_q, cu_k: int32 (see Batches)
+ *   max_len  an upper bound on n(t) over the batch (host value, >= 1)
+ *   scores fp32 [T,ld], ld >= max_len and a multiple of 4
+ */
+IDX_API idx_status idx_score(const uint16_t* q, const uint16_t* k, const float* w,
+                     const int32_t* q_pos, const int32_t* cu_q, const int32_t* cu_k,
+                     int32_t B, int32_t T, int64_t max_len, float* scores, int64_t ld,
+                     void* ws, size_t ws_bytes, void* stream);
+IDX_API size_t idx_score_workspace_size(int32_t B, int32_t T, int64_t max_len);
+
+/*
+ * Exact top-K of score rows under the order rule (indexer paragraph: the
+ * selection is exact; item (4): scores equal to the threshold at the K
+ * boundary form a tie group; the output first lists the kept positions whose
+ * score exceeds the threshold, by increasing position, then the kept members
+ * of the tie group, also by increasing position, the group being cut from its
+ * low-position end; it is not sorted by score; closing paragraph: a history of
+ * K or fewer keys keeps every position, in increasing order).
+ * Threshold: tau is the K-th score in (score descending, position ascending)
+ * order; -0.0 and +0.0 compare equal. Scores must be finite.
+ *   scores  fp32 [T,ld] (row t holds n_valid[t] scores)
+ *   n_valid int32 [T], 0 <= n_valid[t] <= min(ld, max_len)
+ *   topk    1 .. 2048
+ *   idx     int32 [T,topk]: the kept positions, then -1 padding
+ *   cnt     int32 [T] number kept (= min(n_valid, topk)), or NULL
+ */
+IDX_API idx_status idx_topk(const float* scores, int64_t ld, const int32_t* n_valid, int32_t T,
+                    int64_t max_len, int32_t topk, int32_t* idx, int32_t* cnt,
+                    void* ws, size_t ws_bytes, void* stream);
+IDX_API size_t idx_topk_workspace_size(int32_t T, int64_t max_len, int32_t topk);
+
+/*
+ * The whole indexer in one call: idx_score followed by idx_topk with
+ * n_valid[t] = q_pos[t] + 1, staging the fp32 scores inside the workspace.
+ * Arguments as for idx_score and idx_topk.
+ */
+IDX_API idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
+                          const int32_t* q_pos, const int32_t* cu_q, const int32_t* cu_k,
+                          int32_t B, int32_t T, int64_t max_len, int32_t topk, int32_t* idx,
+                          int32_t* cnt, void* ws, size_t ws_bytes, void* stream);
+IDX_API size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_len, int32_t topk);
+
+/*
+ * Device status word of a workspace, written by the kernels of the last call
+ * that used it: IDX_OK, IDX_ERR_DEVICE_ARG or IDX_ERR_TIMEOUT. Synchronises
+ * `stream` (a blocking read of 8 bytes). *detail (may be NULL) receives the
+ * first offending row or a wait-site code.
+ */
+IDX_API idx_status idx_get_status(const void* ws, void* stream, int32_t* detail);
+
+/* Message for the calling thread's last failed call ("" if none). */
+IDX_API const char* idx_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+IDX_API int32_t idx_version(void);
+
+/*
+ * Number of CUDA kernels this library has enqueued in this process (all
+ * devices, all threads), for launch accounting in benchmarks. Memsets are not
+ * counted.
+ */
+IDX_API uint64_t idx_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIGHTNING_INDEXER_H */

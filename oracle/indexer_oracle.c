@@ -8,9 +8,10 @@
  * shares no code, header, table or helper with that path.
  *
  * Source of the method: the Hugging Face discussion "Notes from an NVFP4 port
- * of Kimi K3.1 Pro" (moonshotai/Kimi-K3.1-Pro, discussion 7), its paragraph
- * on the indexer ("The indexer is the entire delta ...") and item (4) of its
- * list "Details that silently change the answer". Readings of that text that
+ * of Kimi K3.1 Pro" (moonshotai/Kimi-K3.1-Pro, discussion 7): the paragraph
+ * that describes the indexer, items (3) and (4) of the list "Details that
+ * silently change the answer", and the closing paragraph on why the port's own
+ * measurements leave selection unused. Readings of that text that
  * the page leaves open are stated at each function.
  *
  * Arithmetic: IEEE fp64 throughout, inputs converted exactly from bf16/fp32.
@@ -32,8 +33,8 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define IDX_HEADS 32   /* "32 heads" */
-#define IDX_DIM 128    /* "of 128 dimensions"; also the LayerNorm width */
+#define IDX_HEADS 32   /* indexer heads per query */
+#define IDX_DIM 128    /* width of each head, of a key and of the LayerNorm */
 
 /* ---------------------------------------------------------------------------
  * Number formats
@@ -74,8 +75,8 @@ uint16_t oracle_double_to_bf16(double x) {
 
 /* ---------------------------------------------------------------------------
  * Step 1 — key LayerNorm.
- * The page: the key comes "from the attention input through a 128-wide
- * LayerNorm that carries both a weight and a bias". Reading: the standard
+ * The page: indexer keys are taken from the attention input and normalised by
+ * a LayerNorm of width 128 that has a weight and a bias. Reading: the standard
  * LayerNorm over the 128 features of one key, biased variance, eps inside
  * the square root, y = (x - mean) / sqrt(var + eps) * gamma + beta; the
  * result is stored in the 16-bit key cache (the page keeps the indexer in
@@ -110,9 +111,9 @@ void oracle_key_layernorm(const uint16_t* k_raw, const double* gamma, const doub
 
 /* ---------------------------------------------------------------------------
  * Steps 2-3 — head scores, relu, head-weighted sum, for one query.
- * The page: "32 heads of 128 dimensions scoring relu(q.k) against the whole
- * causal history", and "a per-head weight vector sums the heads before the
- * select". Reading: S[s] = sum_h w[h] * max(q_h . k_s, 0) for every key s of
+ * The page: each of 32 heads (width 128) scores every key of the causal past
+ * with relu of its dot product with the key, and a vector of per-head weights
+ * combines the heads before selection. Reading: S[s] = sum_h w[h] * max(q_h . k_s, 0) for every key s of
  * the causal history 0..n-1 (n = query position + 1). There is no rotary
  * (index_rope_dim is 0, item (3) of the page's list). No scale factor is
  * printed; any scale is taken to be folded into w.
@@ -141,12 +142,13 @@ void oracle_scores(const uint16_t* q_t, const uint16_t* k_seq, const float* w_t,
 
 /* ---------------------------------------------------------------------------
  * Steps 4-5 — exact top-K with the page's tie and order rule.
- * The page keeps "the best 2048 positions exactly"; item (4): crossing the
- * top-k boundary is a tie, and the output lists the positions strictly above
- * the threshold in ascending order first, then the boundary group from the
- * lowest position up — not a value-sorted list. When the history holds K or
- * fewer keys every key is kept ("the selection is dormant"), in ascending
- * order (the sparse path equals the dense one).
+ * The page: the top 2048 positions are kept with no approximation (indexer
+ * paragraph). Item (4): scores equal to the threshold at the K boundary are a
+ * tie; the output first lists the kept positions that score above the
+ * threshold, by increasing position, then the kept part of the tie group, by
+ * increasing position starting from its lowest; it is not a list sorted by
+ * score. Closing paragraph: a history of at most K keys loses nothing, so
+ * every position is kept, in increasing order (sparse equals dense there).
  *
  * Reading of the threshold: sort all n positions by (score descending,
  * position ascending); tau is the score of the K-th entry. The first K

@@ -1,0 +1,248 @@
+"""Python binding of the Lightning Indexer C ABI (``include/lightning_indexer.h``).
+
+Argument marshalling only: every step of the indexer runs in the CUDA library
+``_lib/liblightning_indexer.so``. Tensors must live on the current CUDA device,
+be contiguous and have the documented dtypes; bf16 tensors may be
+``torch.bfloat16`` or ``torch.uint16``/``torch.int16`` bit patterns. Work is
+enqueued on the current torch stream. If the library has not been built the
+first call raises ``RuntimeError`` — there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HEADS = 32
+DIM = 128
+TOPK_MAX = 2048
+
+IDX_OK = 0
+STATUS_NAMES = {0: "IDX_OK", 1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED",
+                3: "IDX_ERR_WORKSPACE", 4: "IDX_ERR_CUDA", 5: "IDX_ERR_TIMEOUT",
+                6: "IDX_ERR_DEVICE_ARG"}
+PARAM_BF16, PARAM_F32 = 0, 1
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib",
+                         "liblightning_indexer.so")
+_lib = None
+_lock = threading.Lock()
+
+EXPORTS = ("idx_key_layernorm", "idx_score", "idx_score_workspace_size", "idx_topk",
+           "idx_topk_workspace_size", "idx_score_topk", "idx_score_topk_workspace_size",
+           "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches")
+
+
+class IndexerError(RuntimeError):
+    def __init__(self, code: int, where: str, message: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}: {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load the CUDA library (raises RuntimeError if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"Lightning Indexer CUDA library not built ({_LIB_PATH} missing); run "
+                    "`python -m sparse_attention_key_gb300.build`")
+            L = ctypes.CDLL(_LIB_PATH)
+            P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            L.idx_key_layernorm.argtypes = [P, P, P, ctypes.c_int, ctypes.c_float, P, i64, P]
+            L.idx_score.argtypes = [P, P, P, P, P, P, i32, i32, i64, P, i64, P, sz, P]
+            L.idx_score_workspace_size.argtypes = [i32, i32, i64]
+            L.idx_score_workspace_size.restype = sz
+            L.idx_topk.argtypes = [P, i64, P, i32, i64, i32, P, P, P, sz, P]
+            L.idx_topk_workspace_size.argtypes = [i32, i64, i32]
+            L.idx_topk_workspace_size.restype = sz
+            L.idx_score_topk.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, P, P, P, sz, P]
+            L.idx_score_topk_workspace_size.argtypes = [i32, i32, i64, i32]
+            L.idx_score_topk_workspace_size.restype = sz
+            L.idx_get_status.argtypes = [P, P, ctypes.POINTER(i32)]
+            L.idx_last_error.argtypes = []
+            L.idx_last_error.restype = ctypes.c_char_p
+            L.idx_version.argtypes = []
+            L.idx_version.restype = i32
+            L.idx_kernel_launches.argtypes = []
+            L.idx_kernel_launches.restype = ctypes.c_uint64
+            for name in ("idx_key_layernorm", "idx_score", "idx_topk", "idx_score_topk",
+                         "idx_get_status"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(code: int, where: str):
+    if code != IDX_OK:
+        msg = lib().idx_last_error().decode(errors="replace")
+        raise IndexerError(code, where, msg)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtypes, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    return t
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A 256-byte aligned device buffer of at least ``nbytes`` (torch allocation)."""
+    buf = torch.empty(max(int(nbytes), 256) + 256, dtype=torch.uint8,
+                      device=device if device is not None else torch.cuda.current_device())
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + max(int(nbytes), 256)]
+
+
+# ---------------------------------------------------------------------------
+# entry points (same names as the C ABI, without the idx_ prefix)
+# ---------------------------------------------------------------------------
+
+def key_layernorm(k_raw: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Tensor, eps: float,
+                  out: torch.Tensor | None = None) -> torch.Tensor:
+    _dev(k_raw, "k_raw", _BF16)
+    if k_raw.dim() != 2 or k_raw.shape[1] != DIM:
+        raise ValueError("k_raw must be [n,128]")
+    if ln_w.dtype != ln_b.dtype:
+        raise TypeError("ln_w and ln_b must share a dtype")
+    _dev(ln_w, "ln_w", _BF16 + _F32, (DIM,))
+    _dev(ln_b, "ln_b", _BF16 + _F32, (DIM,))
+    pdt = PARAM_F32 if ln_w.dtype == torch.float32 else PARAM_BF16
+    if out is None:
+        out = torch.empty_like(k_raw)
+    _dev(out, "out", _BF16, tuple(k_raw.shape))
+    _check(lib().idx_key_layernorm(_ptr(k_raw), _ptr(ln_w), _ptr(ln_b), pdt, float(eps),
+                                   _ptr(out), k_raw.shape[0], _stream()), "idx_key_layernorm")
+    return out
+
+
+def _batch(q, k, w, q_pos, cu_q, cu_k):
+    _dev(q, "q", _BF16)
+    if q.dim() != 3 or q.shape[1:] != (HEADS, DIM):
+        raise ValueError("q must be [T,32,128]")
+    T = q.shape[0]
+    _dev(k, "k", _BF16)
+    if k.dim() != 2 or k.shape[1] != DIM:
+        raise ValueError("k must be [L,128]")
+    _dev(w, "w", _F32, (T, HEADS))
+    _dev(q_pos, "q_pos", _I32, (T,))
+    _dev(cu_q, "cu_q", _I32)
+    _dev(cu_k, "cu_k", _I32)
+    if cu_q.dim() != 1 or cu_q.shape != cu_k.shape or cu_q.numel() < 2:
+        raise ValueError("cu_q and cu_k must be [B+1] with B >= 1")
+    return T, cu_q.numel() - 1
+
+
+def score_workspace_size(B: int, T: int, max_len: int) -> int:
+    return int(lib().idx_score_workspace_size(B, T, max_len))
+
+
+def topk_workspace_size(T: int, max_len: int, topk: int) -> int:
+    return int(lib().idx_topk_workspace_size(T, max_len, topk))
+
+
+def score_topk_workspace_size(B: int, T: int, max_len: int, topk: int = TOPK_MAX) -> int:
+    return int(lib().idx_score_topk_workspace_size(B, T, max_len, topk))
+
+
+def score(q, k, w, q_pos, cu_q, cu_k, max_len: int, ld: int | None = None,
+          out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """fp32 scores [T, ld]; row t holds n(t) = q_pos[t]+1 valid entries."""
+    T, B = _batch(q, k, w, q_pos, cu_q, cu_k)
+    if ld is None:
+        ld = (max_len + 3) // 4 * 4
+    if out is None:
+        out = torch.full((T, ld), float("nan"), dtype=torch.float32, device=q.device)
+    _dev(out, "out", _F32, (T, ld))
+    need = score_workspace_size(B, T, max_len)
+    if ws is None:
+        ws = workspace(need, q.device)
+    _check(lib().idx_score(_ptr(q), _ptr(k), _ptr(w), _ptr(q_pos), _ptr(cu_q), _ptr(cu_k), B, T,
+                           max_len, _ptr(out), ld, _ptr(ws), ws.numel(), _stream()), "idx_score")
+    return out
+
+
+def topk(scores: torch.Tensor, n_valid: torch.Tensor, max_len: int, k: int = TOPK_MAX,
+         idx: torch.Tensor | None = None, cnt: torch.Tensor | None = None,
+         ws: torch.Tensor | None = None):
+    """Exact top-k of each row -> (idx [T,k] int32, cnt [T] int32)."""
+    _dev(scores, "scores", _F32)
+    if scores.dim() != 2:
+        raise ValueError("scores must be [T, ld]")
+    T, ld = scores.shape
+    _dev(n_valid, "n_valid", _I32, (T,))
+    if idx is None:
+        idx = torch.empty((T, k), dtype=torch.int32, device=scores.device)
+    if cnt is None:
+        cnt = torch.empty((T,), dtype=torch.int32, device=scores.device)
+    _dev(idx, "idx", _I32, (T, k))
+    _dev(cnt, "cnt", _I32, (T,))
+    need = topk_workspace_size(T, max_len, k)
+    if ws is None:
+        ws = workspace(need, scores.device)
+    _check(lib().idx_topk(_ptr(scores), ld, _ptr(n_valid), T, max_len, k, _ptr(idx), _ptr(cnt),
+                          _ptr(ws), ws.numel(), _stream()), "idx_topk")
+    return idx, cnt
+
+
+def score_topk(q, k, w, q_pos, cu_q, cu_k, max_len: int, topk: int = TOPK_MAX,
+               idx: torch.Tensor | None = None, cnt: torch.Tensor | None = None,
+               ws: torch.Tensor | None = None):
+    """The whole indexer -> (idx [T,topk] int32, cnt [T] int32)."""
+    T, B = _batch(q, k, w, q_pos, cu_q, cu_k)
+    if idx is None:
+        idx = torch.empty((T, topk), dtype=torch.int32, device=q.device)
+    if cnt is None:
+        cnt = torch.empty((T,), dtype=torch.int32, device=q.device)
+    _dev(idx, "idx", _I32, (T, topk))
+    _dev(cnt, "cnt", _I32, (T,))
+    need = score_topk_workspace_size(B, T, max_len, topk)
+    if ws is None:
+        ws = workspace(need, q.device)
+    _check(lib().idx_score_topk(_ptr(q), _ptr(k), _ptr(w), _ptr(q_pos), _ptr(cu_q), _ptr(cu_k), B,
+                                T, max_len, topk, _ptr(idx), _ptr(cnt), _ptr(ws), ws.numel(),
+                                _stream()), "idx_score_topk")
+    return idx, cnt
+
+
+def get_status(ws: torch.Tensor) -> tuple[int, int]:
+    """(status code, detail) of the last call that used workspace ``ws`` (synchronises)."""
+    detail = ctypes.c_int32(0)
+    code = lib().idx_get_status(_ptr(ws), _stream(), ctypes.byref(detail))
+    return int(code), int(detail.value)
+
+
+def version() -> int:
+    return int(lib().idx_version())
+
+
+def kernel_launches() -> int:
+    """Kernels this library has enqueued in this process."""
+    return int(lib().idx_kernel_launches())

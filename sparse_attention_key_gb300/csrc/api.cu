@@ -1,0 +1,257 @@
+// C ABI of the Lightning Indexer library: argument checks, workspace layout and
+// kernel dispatch. Declarations and the contract of each call are in
+// include/lightning_indexer.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace lidx {
+
+static thread_local char g_last_error[512] = "";
+
+static idx_status fail(idx_status code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+static idx_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(IDX_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static constexpr int kMaxDevices = 64;
+
+const DeviceInfo& device_info() {
+    static DeviceInfo infos[kMaxDevices];
+    static std::once_flag flags[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        static DeviceInfo none;
+        return none;
+    }
+    std::call_once(flags[dev], [dev]() {
+        DeviceInfo d;
+        d.device = dev;
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        int l2 = 0;
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+        d.l2_bytes = (size_t)l2;
+        infos[dev] = d;
+    });
+    return infos[dev];
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+cudaError_t ensure_smem_optin(const void* kernel, int64_t bytes) {
+    static std::mutex mu;
+    static const void* done_kernel[256];
+    static int done_dev[256];
+    static int n_done = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done_kernel[i] == kernel && done_dev[i] == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    if (n_done < 256) {
+        done_kernel[n_done] = kernel;
+        done_dev[n_done] = dev;
+        ++n_done;
+    }
+    return cudaSuccess;
+}
+
+static idx_status check_device() {
+    const DeviceInfo& d = device_info();
+    if (d.device < 0) return fail(IDX_ERR_CUDA, "no current CUDA device");
+    if (!(d.cc_major == 10 && d.cc_minor == 3))
+        return fail(IDX_ERR_UNSUPPORTED, "device compute capability %d.%d: this library is built "
+                    "for sm_103a (GB300) only", d.cc_major, d.cc_minor);
+    return IDX_OK;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Staged-score row stride used inside a fused call's workspace.
+static int64_t staged_ld(int64_t max_len) { return (int64_t)align_up((size_t)max_len, 4); }
+
+static size_t score_plan_bytes(int32_t /*B*/, int32_t /*T*/) { return 0; }
+
+static idx_status check_batch(const void* q, const void* k, const void* w, const void* q_pos,
+                              const void* cu_q, const void* cu_k, int32_t B, int32_t T,
+                              int64_t max_len) {
+    if (B < 1) return fail(IDX_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
+    if (T < 0) return fail(IDX_ERR_INVALID_ARG, "T must be >= 0 (got %d)", T);
+    if (max_len < 1 || max_len > 0x7fffffffLL)
+        return fail(IDX_ERR_INVALID_ARG, "max_len must be in [1, 2^31-1] (got %lld)",
+                    (long long)max_len);
+    if (!cu_q || !cu_k) return fail(IDX_ERR_INVALID_ARG, "cu_q / cu_k must not be NULL");
+    if (T > 0 && (!q || !k || !w || !q_pos))
+        return fail(IDX_ERR_INVALID_ARG, "q, k, w and q_pos must not be NULL");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 16) || !aligned(q_pos, 4) ||
+        !aligned(cu_q, 4) || !aligned(cu_k, 4))
+        return fail(IDX_ERR_INVALID_ARG, "q, k, w must be 16-byte aligned; int32 arrays 4-byte");
+    return IDX_OK;
+}
+
+static idx_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
+    if (!ws) return fail(IDX_ERR_WORKSPACE, "workspace must not be NULL");
+    if (!aligned(ws, 256)) return fail(IDX_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < need)
+        return fail(IDX_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", ws_bytes,
+                    need);
+    return IDX_OK;
+}
+
+static idx_status clear_status(void* ws, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), s);
+    return e == cudaSuccess ? IDX_OK : cuda_fail(e, "cudaMemsetAsync(status)");
+}
+
+}  // namespace lidx
+
+using namespace lidx;
+
+extern "C" {
+
+int32_t idx_version(void) { return 100; }
+
+const char* idx_last_error(void) { return g_last_error; }
+
+uint64_t idx_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+idx_status idx_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
+                             int ln_dtype, float eps, uint16_t* k_out, int64_t n_rows,
+                             void* stream) {
+    g_last_error[0] = 0;
+    if (n_rows < 0) return fail(IDX_ERR_INVALID_ARG, "n_rows must be >= 0");
+    if (ln_dtype != IDX_PARAM_BF16 && ln_dtype != IDX_PARAM_F32)
+        return fail(IDX_ERR_INVALID_ARG, "ln_dtype must be IDX_PARAM_BF16 or IDX_PARAM_F32");
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(IDX_ERR_INVALID_ARG, "eps must be finite, >= 0");
+    if (n_rows == 0) return IDX_OK;
+    if (!k_raw || !ln_w || !ln_b || !k_out)
+        return fail(IDX_ERR_INVALID_ARG, "k_raw, ln_w, ln_b, k_out must not be NULL");
+    if (!aligned(k_raw, 16) || !aligned(k_out, 16) || !aligned(ln_w, 4) || !aligned(ln_b, 4))
+        return fail(IDX_ERR_INVALID_ARG, "k_raw/k_out must be 16-byte aligned");
+    if (idx_status st = check_device()) return st;
+    cudaError_t e = launch_key_layernorm(k_raw, ln_w, ln_b, ln_dtype == IDX_PARAM_F32, eps, k_out,
+                                         n_rows, (cudaStream_t)stream);
+    return e == cudaSuccess ? IDX_OK : cuda_fail(e, "key_layernorm launch");
+}
+
+size_t idx_score_workspace_size(int32_t B, int32_t T, int64_t /*max_len*/) {
+    return kWsHeader + align_up(score_plan_bytes(B, T), 256);
+}
+
+idx_status idx_score(const uint16_t* q, const uint16_t* k, const float* w, const int32_t* q_pos,
+                     const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t T,
+                     int64_t max_len, float* scores, int64_t ld, void* ws, size_t ws_bytes,
+                     void* stream) {
+    g_last_error[0] = 0;
+    if (idx_status st = check_batch(q, k, w, q_pos, cu_q, cu_k, B, T, max_len)) return st;
+    if (ld < max_len || ld % 4 != 0)
+        return fail(IDX_ERR_INVALID_ARG, "ld must be >= max_len and a multiple of 4");
+    if (T > 0 && (!scores || !aligned(scores, 16)))
+        return fail(IDX_ERR_INVALID_ARG, "scores must be non-NULL and 16-byte aligned");
+    if (idx_status st = check_ws(ws, ws_bytes, idx_score_workspace_size(B, T, max_len))) return st;
+    if (idx_status st = check_device()) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (idx_status st = clear_status(ws, s)) return st;
+    if (T == 0) return IDX_OK;
+    ScoreArgs a{q, k, w, q_pos, cu_q, cu_k, B, T, max_len, scores, ld, (DeviceStatus*)ws};
+    cudaError_t e = launch_score_simt(a, s);
+    return e == cudaSuccess ? IDX_OK : cuda_fail(e, "score launch");
+}
+
+size_t idx_topk_workspace_size(int32_t /*T*/, int64_t /*max_len*/, int32_t /*topk*/) {
+    return kWsHeader;
+}
+
+idx_status idx_topk(const float* scores, int64_t ld, const int32_t* n_valid, int32_t T,
+                    int64_t max_len, int32_t topk, int32_t* idx, int32_t* cnt, void* ws,
+                    size_t ws_bytes, void* stream) {
+    g_last_error[0] = 0;
+    if (T < 0) return fail(IDX_ERR_INVALID_ARG, "T must be >= 0");
+    if (topk < 1 || topk > IDX_TOPK_MAX)
+        return fail(IDX_ERR_INVALID_ARG, "topk must be in [1, %d] (got %d)", IDX_TOPK_MAX, topk);
+    if (max_len < 1 || max_len > 0x7fffffffLL)
+        return fail(IDX_ERR_INVALID_ARG, "max_len must be in [1, 2^31-1]");
+    if (ld < 1 || ld % 4 != 0) return fail(IDX_ERR_INVALID_ARG, "ld must be a positive multiple of 4");
+    if (T > 0 && (!scores || !n_valid || !idx))
+        return fail(IDX_ERR_INVALID_ARG, "scores, n_valid and idx must not be NULL");
+    if (!aligned(scores, 16) || !aligned(n_valid, 4) || !aligned(idx, 4) || !aligned(cnt, 4))
+        return fail(IDX_ERR_INVALID_ARG, "scores must be 16-byte aligned, int32 arrays 4-byte");
+    if (idx_status st = check_ws(ws, ws_bytes, idx_topk_workspace_size(T, max_len, topk))) return st;
+    if (idx_status st = check_device()) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (idx_status st = clear_status(ws, s)) return st;
+    if (T == 0) return IDX_OK;
+    TopkArgs a{scores, ld, n_valid, false, T, max_len, topk, idx, cnt, (DeviceStatus*)ws};
+    cudaError_t e = launch_topk(a, s);
+    return e == cudaSuccess ? IDX_OK : cuda_fail(e, "topk launch");
+}
+
+size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_len, int32_t /*topk*/) {
+    if (T < 0 || max_len < 1) return kWsHeader;
+    return kWsHeader + align_up(score_plan_bytes(B, T), 256) +
+           align_up((size_t)T * (size_t)staged_ld(max_len) * sizeof(float), 256);
+}
+
+idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
+                          const int32_t* q_pos, const int32_t* cu_q, const int32_t* cu_k,
+                          int32_t B, int32_t T, int64_t max_len, int32_t topk, int32_t* idx,
+                          int32_t* cnt, void* ws, size_t ws_bytes, void* stream) {
+    g_last_error[0] = 0;
+    if (idx_status st = check_batch(q, k, w, q_pos, cu_q, cu_k, B, T, max_len)) return st;
+    if (topk < 1 || topk > IDX_TOPK_MAX)
+        return fail(IDX_ERR_INVALID_ARG, "topk must be in [1, %d] (got %d)", IDX_TOPK_MAX, topk);
+    if (T > 0 && !idx) return fail(IDX_ERR_INVALID_ARG, "idx must not be NULL");
+    if (!aligned(idx, 4) || !aligned(cnt, 4))
+        return fail(IDX_ERR_INVALID_ARG, "idx/cnt must be 4-byte aligned");
+    if (idx_status st = check_ws(ws, ws_bytes, idx_score_topk_workspace_size(B, T, max_len, topk)))
+        return st;
+    if (idx_status st = check_device()) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (idx_status st = clear_status(ws, s)) return st;
+    if (T == 0) return IDX_OK;
+    const int64_t ld = staged_ld(max_len);
+    char* base = (char*)ws + kWsHeader + align_up(score_plan_bytes(B, T), 256);
+    float* scores = (float*)base;
+    DeviceStatus* status = (DeviceStatus*)ws;
+    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, max_len, scores, ld, status};
+    cudaError_t e = launch_score_simt(sa, s);
+    if (e != cudaSuccess) return cuda_fail(e, "score launch");
+    TopkArgs ta{scores, ld, q_pos, true, T, max_len, topk, idx, cnt, status, cu_q, cu_k, B};
+    e = launch_topk(ta, s);
+    return e == cudaSuccess ? IDX_OK : cuda_fail(e, "topk launch");
+}
+
+idx_status idx_get_status(const void* ws, void* stream, int32_t* detail) {
+    if (!ws) return fail(IDX_ERR_INVALID_ARG, "workspace must not be NULL");
+    DeviceStatus h{0, 0};
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(&h, ws, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    if (detail) *detail = h.detail;
+    return (idx_status)h.code;
+}
+
+}  // extern "C"

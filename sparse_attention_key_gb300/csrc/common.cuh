@@ -1,0 +1,55 @@
+// Shared device/host helpers of the Lightning Indexer CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lightning_indexer.h"
+
+namespace lidx {
+
+constexpr int kHeads = IDX_HEADS;   // 32 indexer heads
+constexpr int kDim = IDX_DIM;       // 128 dims per head and per key
+constexpr int kTopkMax = IDX_TOPK_MAX;
+
+// ---------------------------------------------------------------------------
+// Workspace layout. Every entry point's workspace starts with a 256-byte
+// header holding the device status word; regions after it are 256-byte
+// aligned.
+// ---------------------------------------------------------------------------
+constexpr size_t kWsHeader = 256;
+
+struct DeviceStatus {
+    int32_t code;    // idx_status value: IDX_OK, IDX_ERR_DEVICE_ARG or IDX_ERR_TIMEOUT
+    int32_t detail;  // first offending row, or a wait-site code
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Record the first error of a call; later errors keep the first one.
+__device__ inline void report_error(DeviceStatus* st, int32_t code, int32_t detail) {
+    if (atomicCAS(&st->code, 0, code) == 0) atomicExch(&st->detail, detail);
+}
+
+// ---------------------------------------------------------------------------
+// Number formats
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+    uint32_t u = __float_as_uint(x);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+// Order-preserving map of an fp32 score to uint32: a > b (numerically) iff
+// key(a) > key(b). -0.0 maps to the key of +0.0 so that the two compare equal.
+__device__ __forceinline__ uint32_t score_key(float x) {
+    uint32_t u = __float_as_uint(x);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace lidx

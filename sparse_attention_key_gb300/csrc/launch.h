@@ -1,0 +1,71 @@
+// Host-side launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace lidx {
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int max_smem_optin = 0;   // bytes of shared memory a block may opt in to
+    size_t l2_bytes = 0;
+};
+
+// Count one kernel launch (reported by idx_kernel_launches).
+void count_launch(int n = 1);
+
+// Properties of the current device (cached per device).
+const DeviceInfo& device_info();
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` once per device.
+cudaError_t ensure_smem_optin(const void* kernel, int64_t bytes);
+
+cudaError_t launch_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
+                                 bool f32_params, float eps, uint16_t* k_out, int64_t n_rows,
+                                 cudaStream_t stream);
+
+// Arguments of one scoring call (device pointers, host sizes).
+struct ScoreArgs {
+    const uint16_t* q;
+    const uint16_t* k;
+    const float* w;
+    const int32_t* q_pos;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int32_t B, T;
+    int64_t max_len;
+    float* scores;
+    int64_t ld;
+    DeviceStatus* status;
+};
+
+// CUDA-core scorer: one thread per key, streams K with 16-byte loads.
+cudaError_t launch_score_simt(const ScoreArgs& a, cudaStream_t stream);
+
+// Arguments of one top-K call.
+struct TopkArgs {
+    const float* scores;
+    int64_t ld;
+    const int32_t* n_valid;   // per-row count, or q_pos when n_from_pos
+    bool n_from_pos;          // n(t) = n_valid[t] + 1
+    int32_t T;
+    int64_t max_len;
+    int32_t topk;
+    int32_t* idx;
+    int32_t* cnt;
+    DeviceStatus* status;
+    // Optional (fused call): the batch layout, used to skip rows whose query
+    // position lies outside its sequence. NULL when the caller gives n_valid.
+    const int32_t* cu_q = nullptr;
+    const int32_t* cu_k = nullptr;
+    int32_t B = 0;
+};
+
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
+
+}  // namespace lidx

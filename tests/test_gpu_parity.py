@@ -1,0 +1,320 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Bars (from the indexer's statement of the problem):
+  - integer-valued inputs (exact in fp32 in any summation order): indices and
+    counts bit-exact, scores exactly equal;
+  - real-valued inputs: every score within 1e-3 relative (+1e-6 x row max), and
+    the GPU's and the oracle's index sets may differ only at positions whose
+    oracle score is within 1e-3 of the oracle threshold; the GPU output must be
+    the exact rule-ordered top-K of the GPU's own fp32 scores;
+  - the stand-alone top-K on given fp32 rows: bit-exact (both sides decide on the
+    same fp32 values);
+  - LayerNorm: within 1 bf16 ulp of the fp64 oracle rounded once to bf16.
+Full-size workloads are checked on sampled rows the oracle computes one by one.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_key_gb300 import workloads as wl
+from tests._util import (bf16_ulp_distance, bits_of, rule_order_ok, scores_close,
+                         to_device, tolerance_set_check)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ORACLE_THREADS = 8
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_attention_key_gb300 import build
+    build.build()
+    from sparse_attention_key_gb300 import binding
+    return binding
+
+
+_cache = {}
+
+
+def workload(i):
+    if i not in _cache:
+        _cache[i] = wl.by_index(i)
+    return _cache[i]
+
+
+def gpu_scores(B, d, max_len):
+    return B.score(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], max_len)
+
+
+def oracle_rows(w, rows, want_scores=True, K=2048, k_bits=None):
+    return oracle.score_topk(w.q, w.k if k_bits is None else k_bits, w.w, w.q_pos, w.cu_q, w.cu_k,
+                             K=K, rows=rows, want_scores=want_scores, threads=ORACLE_THREADS)
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm
+# ---------------------------------------------------------------------------
+
+def _ln_check(B, k_raw_bits, ln_w_bits, ln_b_bits, eps, f32_params=False):
+    dev = torch.from_numpy(k_raw_bits.view(np.int16)).cuda()
+    if f32_params:
+        gw = torch.from_numpy(wl.bf16_bits_to_f32(ln_w_bits)).cuda()
+        gb = torch.from_numpy(wl.bf16_bits_to_f32(ln_b_bits)).cuda()
+    else:
+        gw = torch.from_numpy(ln_w_bits.view(np.int16)).cuda()
+        gb = torch.from_numpy(ln_b_bits.view(np.int16)).cuda()
+    out = bits_of(B.key_layernorm(dev, gw, gb, eps))
+    ref, _ = oracle.key_layernorm(k_raw_bits, oracle.bf16_bits_to_f64(ln_w_bits),
+                                  oracle.bf16_bits_to_f64(ln_b_bits), float(np.float32(eps)))
+    dist = bf16_ulp_distance(out, ref)
+    assert dist.max() <= 1, f"max ulp distance {dist.max()}"
+    assert (dist == 0).mean() > 0.99
+    return out
+
+
+def test_layernorm_tiny_exact_params(B):
+    w = workload(1)
+    _ln_check(B, w.k_raw, w.ln_w, w.ln_b, w.eps)
+
+
+def test_layernorm_decode_batch_params(B):
+    w = workload(2)
+    _ln_check(B, w.k_raw, w.ln_w, w.ln_b, w.eps)
+
+
+def test_layernorm_fp32_params_and_ragged_rows(B):
+    rng = np.random.default_rng(7)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((1237, 128)).astype(np.float32) * 2 + 0.3)
+    g = wl.f32_to_bf16_bits((1 + 0.1 * rng.standard_normal(128)).astype(np.float32))
+    b = wl.f32_to_bf16_bits((0.1 * rng.standard_normal(128)).astype(np.float32))
+    _ln_check(B, x, g, b, 1e-5, f32_params=True)
+
+
+def test_layernorm_in_place(B):
+    rng = np.random.default_rng(8)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((300, 128)).astype(np.float32))
+    g = wl.f32_to_bf16_bits(np.ones(128, np.float32))
+    b = wl.f32_to_bf16_bits(np.zeros(128, np.float32))
+    d = torch.from_numpy(x.view(np.int16)).cuda()
+    gw, gb = torch.from_numpy(g.view(np.int16)).cuda(), torch.from_numpy(b.view(np.int16)).cuda()
+    expect = bits_of(B.key_layernorm(d.clone(), gw, gb, 1e-6))
+    B.key_layernorm(d, gw, gb, 1e-6, out=d)
+    assert np.array_equal(bits_of(d), expect)
+
+
+# ---------------------------------------------------------------------------
+# scores
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["int2", "int4s3"])
+def test_scores_exact_on_integer_inputs(B, kind):
+    w = wl.custom(101, q_counts=[3, 130, 1, 0, 17], k_lens=[300, 700, 5000, 9, 129], kind=kind)
+    d = to_device(w)
+    S = gpu_scores(B, d, w.max_len).cpu().numpy()
+    _, _, ref = oracle_rows(w, range(w.T))
+    for t in range(w.T):
+        n = int(w.q_pos[t]) + 1
+        assert np.array_equal(S[t, :n].astype(np.float64), ref[t, :n]), t
+        assert np.isnan(S[t, n:]).all(), "entries past the causal length must stay untouched"
+
+
+def test_scores_real_inputs_within_tolerance(B):
+    w = wl.custom(102, q_counts=[5, 64, 1], k_lens=[1000, 2300, 4097], kind="normal",
+                  positions="random")
+    d = to_device(w)
+    S = gpu_scores(B, d, w.max_len).cpu().numpy()
+    _, _, ref = oracle_rows(w, range(w.T))
+    for t in range(w.T):
+        n = int(w.q_pos[t]) + 1
+        msg = scores_close(S[t, :n], ref[t, :n])
+        assert msg is None, f"row {t}: {msg}"
+
+
+# ---------------------------------------------------------------------------
+# stand-alone top-K on given fp32 rows: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["ties", "normal", "mixed", "const"])
+@pytest.mark.parametrize("K", [1, 7, 2048])
+@pytest.mark.parametrize("lens", ["short", "long"])
+def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
+    rng = np.random.default_rng(zlib.crc32(f"{kind}/{K}/{lens}".encode()))
+    if lens == "short":
+        n_valid = np.concatenate([[0, 1, K - 1 if K > 1 else 0, K, K + 1, 2047, 2048, 2049, 4096],
+                                  rng.integers(1, 20000, size=20), [50_000]]).astype(np.int32)
+    else:   # beyond the shared-memory row cap: the multi-pass global path
+        n_valid = np.array([70_000, 131_072, 65_537, K + 3, 100_001], np.int32)
+    max_len = int(n_valid.max())
+    ld = (max_len + 3) // 4 * 4
+    S = wl.score_rows(int(rng.integers(1 << 30)), n_valid.size, n_valid, ld, kind=kind)
+    dS = torch.from_numpy(S).cuda()
+    idx, cnt = B.topk(dS, torch.from_numpy(n_valid).cuda(), max_len, K)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for t, n in enumerate(n_valid):
+        ref = oracle.select(S[t, :n].astype(np.float64), K)
+        assert np.array_equal(idx[t], ref), f"row {t} (n={n})"
+        assert cnt[t] == min(n, K)
+
+
+# ---------------------------------------------------------------------------
+# the whole indexer
+# ---------------------------------------------------------------------------
+
+def _check_exact(B, w, rows=None, K=2048):
+    d = to_device(w)
+    idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len, K)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    rows = list(range(w.T)) if rows is None else rows
+    ridx, rcnt, _ = oracle_rows(w, rows, want_scores=False, K=K)
+    for t in rows:
+        assert np.array_equal(idx[t], ridx[t]), f"row {t}"
+        assert cnt[t] == rcnt[t]
+    return idx, cnt
+
+
+def test_indexer_tiny_exact_all_rows(B):
+    w = workload(1)
+    idx, cnt = _check_exact(B, w)
+    assert cnt.tolist() == [101, 2048, 2048, 2048, 2048, 2048, 2048, 2048]
+
+
+def test_indexer_small_ragged_prefill_ties_all_rows(B):
+    w = wl.custom(103, q_counts=[300, 45, 1], k_lens=[3000, 2049, 2050], kind="int2")
+    _check_exact(B, w)
+
+
+@pytest.mark.parametrize("K", [1, 16, 333])
+def test_indexer_small_topk_values(B, K):
+    w = wl.custom(104, q_counts=[40, 7], k_lens=[500, 390], kind="int4s3", positions="random",
+                  topk=K)
+    _check_exact(B, w, K=K)
+
+
+def test_indexer_prefill_ties_full_size_sampled(B):
+    w = workload(3)
+    rows = [0, 1, 127, 128, 2046, 2047, 2048, 2049, 4095, 5000, 6143, 8190, 8191]
+    _check_exact(B, w, rows=rows)
+
+
+def _check_tolerance(B, w, rows, d=None, k_oracle=None):
+    d = to_device(w) if d is None else d
+    idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len)
+    S = gpu_scores(B, d, w.max_len)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    ridx, rcnt, rS = oracle_rows(w, rows, k_bits=k_oracle)
+    for t in rows:
+        n = int(w.q_pos[t]) + 1
+        S_gpu = S[t, :n].cpu().numpy()
+        assert cnt[t] == rcnt[t] == min(n, 2048)
+        msg = scores_close(S_gpu, rS[t, :n])
+        assert msg is None, f"row {t}: {msg}"
+        msg = tolerance_set_check(rS[t, :n], idx[t], ridx[t], 2048)
+        assert msg is None, f"row {t}: {msg}"
+        msg = rule_order_ok(S_gpu, idx[t], 2048)
+        assert msg is None, f"row {t}: {msg}"
+
+
+def test_indexer_decode_batch_layernorm_chained(B):
+    w = workload(2)
+    d = to_device(w)
+    d["k"] = B.key_layernorm(d["k_raw"], d["ln_w"], d["ln_b"], w.eps)
+    k_ref, _ = oracle.key_layernorm(w.k_raw, oracle.bf16_bits_to_f64(w.ln_w),
+                                    oracle.bf16_bits_to_f64(w.ln_b), float(np.float32(w.eps)))
+    _check_tolerance(B, w, rows=list(range(w.T)), d=d, k_oracle=k_ref)
+
+
+def test_indexer_agentic_chunk_sampled(B):
+    w = workload(4)
+    rows = [0, 1, 399, 799, 800, 1600, 2401, 3199]
+    _check_tolerance(B, w, rows)
+
+
+def test_indexer_long_decode_sampled(B):
+    w = workload(5)
+    rows = [0, 7, 31, 32, 50, 63]
+    _check_tolerance(B, w, rows)
+    # every row: the GPU output is the rule-ordered top-K of the GPU's own scores
+    d = to_device(w)
+    idx, _ = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len)
+    S = gpu_scores(B, d, w.max_len).cpu().numpy()
+    idx = idx.cpu().numpy()
+    for t in range(w.T):
+        n = int(w.q_pos[t]) + 1
+        assert rule_order_ok(S[t, :n], idx[t], 2048) is None, t
+
+
+# ---------------------------------------------------------------------------
+# edge cases and errors
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 2047, 2048, 2049, 2050])
+def test_indexer_history_lengths_around_tiles_and_budget(B, L):
+    w = wl.custom(200 + L, q_counts=[min(L, 3)], k_lens=[L], kind="int2")
+    _check_exact(B, w)
+
+
+def test_indexer_batch_with_empty_sequences(B):
+    w = wl.custom(301, q_counts=[0, 4, 0, 2, 0], k_lens=[0, 2500, 10, 3000, 0], kind="int2")
+    _check_exact(B, w)
+
+
+def test_indexer_zero_queries(B):
+    w = wl.custom(302, q_counts=[0], k_lens=[100], kind="int2")
+    d = to_device(w)
+    idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], 100)
+    torch.cuda.synchronize()
+    assert idx.shape == (0, 2048) and cnt.shape == (0,)
+
+
+def test_indexer_output_guard_bands_untouched(B):
+    w = wl.custom(303, q_counts=[20], k_lens=[4000], kind="int2")
+    d = to_device(w)
+    guard = 4096
+    buf = torch.full((w.T * 2048 + 2 * guard,), -7, dtype=torch.int32, device="cuda")
+    cbuf = torch.full((w.T + 2 * 64,), -7, dtype=torch.int32, device="cuda")
+    idx = buf[guard:guard + w.T * 2048].view(w.T, 2048)
+    cnt = cbuf[64:64 + w.T]
+    B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len, idx=idx,
+                 cnt=cnt)
+    b = buf.cpu().numpy()
+    c = cbuf.cpu().numpy()
+    assert (b[:guard] == -7).all() and (b[-guard:] == -7).all()
+    assert (c[:64] == -7).all() and (c[-64:] == -7).all()
+    ridx, _, _ = oracle_rows(w, range(w.T), want_scores=False)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+
+
+def test_device_argument_error_is_reported_and_row_skipped(B):
+    w = wl.custom(304, q_counts=[3], k_lens=[3000], kind="int2")
+    bad = w.q_pos.copy()
+    bad[1] = 3000                                   # == len_k: outside the sequence
+    d = to_device(w)
+    d["q_pos"] = torch.from_numpy(bad).cuda()
+    ws = B.workspace(B.score_topk_workspace_size(1, 3, 3001), "cuda")
+    idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], 3001, ws=ws)
+    code, detail = B.get_status(ws)
+    assert code == 6 and detail == 1
+    ridx, _, _ = oracle_rows(w, [0, 2], want_scores=False)
+    got = idx.cpu().numpy()
+    assert np.array_equal(got[0], ridx[0]) and np.array_equal(got[2], ridx[2])
+    # a later good call on the same workspace clears the status
+    d["q_pos"] = torch.from_numpy(w.q_pos).cuda()
+    B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], 3001, ws=ws)
+    assert B.get_status(ws) == (0, 0)
+
+
+def test_host_argument_errors_raise(B):
+    w = wl.custom(305, q_counts=[2], k_lens=[100], kind="int2")
+    d = to_device(w)
+    with pytest.raises(B.IndexerError) as e:
+        B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], 100, topk=4096)
+    assert e.value.code == 1
+    ws = B.workspace(256, "cuda")
+    with pytest.raises(B.IndexerError) as e:
+        B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], 100, ws=ws)
+    assert e.value.code == 3

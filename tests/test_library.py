@@ -1,0 +1,140 @@
+"""The C-ABI library without a GPU: it builds, loads, exports exactly what the
+header declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_key_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lightning_indexer.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    path = lib_build.build()
+    from sparse_attention_key_gb300 import binding
+    return binding.lib() if binding.library_path() == path else ctypes.CDLL(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return re.findall(r"IDX_API\s+[\w\s\*]+?\b(idx_\w+)\s*\(", src)
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    assert {"idx_key_layernorm", "idx_score", "idx_topk", "idx_score_topk"} <= set(names)
+    assert len(names) == len(set(names))
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_library_exports_nothing_else():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.split()[1] in ("T", "t")}
+    assert exported == set(declared_functions())
+
+
+def test_binding_export_list_matches_header():
+    from sparse_attention_key_gb300 import binding
+    assert set(binding.EXPORTS) == set(declared_functions())
+
+
+def test_version(L):
+    from sparse_attention_key_gb300 import binding
+    assert binding.version() >= 100
+
+
+def test_workspace_sizes_are_host_only(L):
+    from sparse_attention_key_gb300 import binding
+    assert binding.topk_workspace_size(10, 5000, 2048) >= 256
+    s = binding.score_topk_workspace_size(4, 3200, 50800, 2048)
+    assert s >= 3200 * 50800 * 4
+    assert s % 256 == 0
+
+
+# Host argument errors: each returns its code with no CUDA call (no GPU here).
+FAKE = ctypes.c_void_p(4096)      # a non-null, aligned, never dereferenced address
+NULL = None
+
+
+def _score_topk(L, **kw):
+    a = dict(q=FAKE, k=FAKE, w=FAKE, q_pos=FAKE, cu_q=FAKE, cu_k=FAKE, B=1, T=4, max_len=100,
+             topk=2048, idx=FAKE, cnt=NULL, ws=FAKE, ws_bytes=1 << 30, stream=NULL)
+    a.update(kw)
+    return L.idx_score_topk(a["q"], a["k"], a["w"], a["q_pos"], a["cu_q"], a["cu_k"], a["B"],
+                            a["T"], a["max_len"], a["topk"], a["idx"], a["cnt"], a["ws"],
+                            a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=NULL), 1), (dict(k=NULL), 1), (dict(w=NULL), 1), (dict(q_pos=NULL), 1),
+    (dict(cu_q=NULL), 1), (dict(cu_k=NULL), 1), (dict(idx=NULL), 1),
+    (dict(B=0), 1), (dict(T=-1), 1), (dict(max_len=0), 1), (dict(topk=0), 1),
+    (dict(topk=2049), 1), (dict(q=ctypes.c_void_p(4098)), 1),
+    (dict(ws=NULL), 3), (dict(ws_bytes=16), 3), (dict(ws=ctypes.c_void_p(4096 + 16)), 3),
+])
+def test_score_topk_host_errors(L, kw, code):
+    assert _score_topk(L, **kw) == code
+    assert L.idx_last_error()  # a message is set
+
+
+def test_topk_host_errors(L):
+    ok = dict(scores=FAKE, ld=4096, n_valid=FAKE, T=3, max_len=4000, topk=16, idx=FAKE,
+              cnt=NULL, ws=FAKE, ws_bytes=1 << 20, stream=NULL)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return L.idx_topk(a["scores"], a["ld"], a["n_valid"], a["T"], a["max_len"], a["topk"],
+                          a["idx"], a["cnt"], a["ws"], a["ws_bytes"], a["stream"])
+    assert call(ld=4098) == 1          # not a multiple of 4
+    assert call(topk=0) == 1
+    assert call(topk=4096) == 1
+    assert call(scores=NULL) == 1
+    assert call(n_valid=NULL) == 1
+    assert call(ws_bytes=8) == 3
+    assert call(T=-2) == 1
+
+
+def test_score_host_errors(L):
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, w=FAKE, q_pos=FAKE, cu_q=FAKE, cu_k=FAKE, B=1, T=2, max_len=64,
+                 scores=FAKE, ld=64, ws=FAKE, ws_bytes=1 << 20, stream=NULL)
+        a.update(kw)
+        return L.idx_score(a["q"], a["k"], a["w"], a["q_pos"], a["cu_q"], a["cu_k"], a["B"],
+                           a["T"], a["max_len"], a["scores"], a["ld"], a["ws"], a["ws_bytes"],
+                           a["stream"])
+    assert call(ld=60) == 1            # ld < max_len
+    assert call(ld=66) == 1            # not a multiple of 4
+    assert call(scores=NULL) == 1
+    assert call(ws=NULL) == 3
+
+
+def test_layernorm_host_errors(L):
+    def call(**kw):
+        a = dict(k_raw=FAKE, w=FAKE, b=FAKE, dt=0, eps=1e-6, out=FAKE, n=10, stream=NULL)
+        a.update(kw)
+        return L.idx_key_layernorm(a["k_raw"], a["w"], a["b"], a["dt"], ctypes.c_float(a["eps"]),
+                                   a["out"], a["n"], a["stream"])
+    assert call(n=-1) == 1
+    assert call(dt=7) == 1
+    assert call(eps=float("nan")) == 1
+    assert call(k_raw=NULL) == 1
+    assert call(n=0) == 0             # nothing to do: no device needed
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from sparse_attention_key_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.lib()
