@@ -141,6 +141,34 @@ IDX_API idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const fl
 IDX_API size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_len, int32_t topk);
 
 /*
+ * idx_score_topk without a workspace argument. The port notes have no
+ * counterpart: this entry point exists for callers that cannot give the
+ * library any extra device memory — an engine that plans all of its device
+ * memory ahead and bans cudaMalloc while serving (it may synchronise the device
+ * and may fail under memory pressure), or a plugin that its host framework
+ * hands only input and output buffers. Same arguments and results as
+ * idx_score_topk, minus ws/ws_bytes; it allocates nothing.
+ *   Scratch   a fixed 32 MiB (+256 B) array inside the library's device image,
+ *             reserved on every GPU that loads the library until process exit.
+ *   Limit     T * round_up(max_len, 4) * 4 <= 32 MiB (e.g. 64 queries of up to
+ *             131,072 keys); larger calls return IDX_ERR_WORKSPACE, enqueue
+ *             nothing, and idx_last_error() says why.
+ *   Sharing   every call on a device uses the same array, which keeps the last
+ *             call's contents; calls that can overlap on the GPU (other streams,
+ *             unordered host threads) race on it and must be serialised.
+ *   Set-up    the first call on each device looks up the array's device address
+ *             (cudaGetSymbolAddress, with that device current); make that first
+ *             call before any stream capture.
+ *   Errors    host checks as idx_score_topk; a row skipped for a device-side
+ *             argument error shows cnt[t] == 0 and idx -1 (no status word).
+ */
+IDX_API idx_status idx_score_topk_noalloc(const uint16_t* q, const uint16_t* k, const float* w,
+                                          const int32_t* q_pos, const int32_t* cu_q,
+                                          const int32_t* cu_k, int32_t B, int32_t T,
+                                          int64_t max_len, int32_t topk, int32_t* idx,
+                                          int32_t* cnt, void* stream);
+
+/*
  * Device status word of a workspace, written by the kernels of the last call
  * that used it: IDX_OK, IDX_ERR_DEVICE_ARG or IDX_ERR_TIMEOUT. Synchronises
  * `stream` (a blocking read of 8 bytes). *detail (may be NULL) receives the

@@ -32,7 +32,8 @@ _lock = threading.Lock()
 
 EXPORTS = ("idx_key_layernorm", "idx_score", "idx_score_workspace_size", "idx_topk",
            "idx_topk_workspace_size", "idx_score_topk", "idx_score_topk_workspace_size",
-           "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches")
+           "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches",
+           "idx_score_topk_noalloc")
 
 
 class IndexerError(RuntimeError):
@@ -246,3 +247,30 @@ def version() -> int:
 def kernel_launches() -> int:
     """Kernels this library has enqueued in this process."""
     return int(lib().idx_kernel_launches())
+
+
+def score_topk_noalloc(q, k, w, q_pos, cu_q, cu_k, max_len: int, topk: int = TOPK_MAX,
+                       idx: torch.Tensor | None = None, cnt: torch.Tensor | None = None):
+    """The whole indexer with no workspace: scratch lives inside the library.
+
+    For callers that cannot supply extra device memory (a fixed memory plan, or
+    a host that hands over only inputs and outputs). The library's scratch is
+    32 MiB per GPU: T * round_up(max_len, 4) * 4 bytes must fit. All calls on a
+    device share it, so calls that may overlap on the GPU must be serialised;
+    the first call on a device resolves the scratch address and should precede
+    any stream capture. ``idx``/``cnt`` may be preallocated by the caller.
+    """
+    T, B = _batch(q, k, w, q_pos, cu_q, cu_k)
+    if idx is None:
+        idx = torch.empty((T, topk), dtype=torch.int32, device=q.device)
+    if cnt is None:
+        cnt = torch.empty((T,), dtype=torch.int32, device=q.device)
+    _dev(idx, "idx", _I32, (T, topk))
+    _dev(cnt, "cnt", _I32, (T,))
+    fn = lib().idx_score_topk_noalloc
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    fn.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, P, P, P]
+    fn.restype = ctypes.c_int
+    _check(fn(_ptr(q), _ptr(k), _ptr(w), _ptr(q_pos), _ptr(cu_q), _ptr(cu_k), B, T, max_len, topk,
+              _ptr(idx), _ptr(cnt), _stream()), "idx_score_topk_noalloc")
+    return idx, cnt

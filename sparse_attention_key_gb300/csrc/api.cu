@@ -23,6 +23,9 @@ static idx_status fail(idx_status code, const char* fmt, ...) {
     return code;
 }
 
+// Lets other translation units of the library report through idx_last_error().
+void set_last_error_text(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 static idx_status cuda_fail(cudaError_t e, const char* where) {
     return fail(IDX_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }

@@ -16,6 +16,9 @@ struct DeviceInfo {
     size_t l2_bytes = 0;
 };
 
+// Set the calling thread's idx_last_error() text.
+void set_last_error_text(const char* msg);
+
 // Count one kernel launch (reported by idx_kernel_launches).
 void count_launch(int n = 1);
 

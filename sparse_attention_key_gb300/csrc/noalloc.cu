@@ -1,0 +1,125 @@
+// idx_score_topk_noalloc: the whole indexer without a caller-provided workspace.
+//
+// Some callers cannot hand this library any device memory beyond the tensors
+// they already own: an inference engine that plans every device allocation up
+// front and forbids cudaMalloc on its request path (cudaMalloc can synchronise
+// the device and can fail under memory pressure mid-request), or a plugin
+// that is given only its input and output buffers by a host framework that
+// owns the allocator. For them this entry point keeps its scratch — the staged
+// fp32 scores and the device status word — in one fixed array that lives in
+// this library's own device memory, and allocates nothing.
+//
+// Limits and sharing:
+//   - The scratch array holds kNoAllocScoreBytes (32 MiB) of staged scores:
+//     T * round_up(max_len, 4) * 4 bytes must fit, e.g. 64 queries with up to
+//     131,072 keys each. Larger calls are rejected on the host (IDX_ERR_WORKSPACE).
+//   - Every GPU that loads the library reserves the array (32 MiB + 256 B)
+//     until the process exits.
+//   - All calls on a device share the one array and it keeps the contents of
+//     the last call: calls that can overlap on the GPU (different streams, or
+//     different host threads without ordering) race on it. Serialise them.
+//   - The first call on each device looks up the array's device address with
+//     cudaGetSymbolAddress (with that device current); make that first call
+//     before any stream capture.
+//   - Device-side argument errors are not reported through a status word: a
+//     skipped row shows cnt[t] == 0 and an idx row of -1.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace lidx {
+
+constexpr size_t kNoAllocScoreBytes = size_t(32) << 20;                 // staged fp32 scores
+constexpr size_t kNoAllocScratchBytes = kWsHeader + kNoAllocScoreBytes;  // + status header
+
+// Library-owned scratch. Host code must not use this name as a pointer: on the
+// host it only stands for the symbol; its device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+idx_status noalloc_fail(idx_status code, const char* msg) {
+    set_last_error_text(msg);
+    return code;
+}
+
+// Device address of the scratch array on the current device (looked up once
+// per device, with that device current). Returns nullptr and fills `err` on
+// failure.
+void* noalloc_scratch(cudaError_t* err) {
+    static std::mutex mu;
+    static void* addr[kNoAllocMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+        *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            *err = e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    *err = cudaSuccess;
+    return addr[dev];
+}
+
+bool is_aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+}  // namespace lidx
+
+using namespace lidx;
+
+extern "C" IDX_API idx_status idx_score_topk_noalloc(
+    const uint16_t* q, const uint16_t* k, const float* w, const int32_t* q_pos,
+    const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t T, int64_t max_len,
+    int32_t topk, int32_t* idx, int32_t* cnt, void* stream) {
+    set_last_error_text("");
+    if (B < 1 || T < 0) return noalloc_fail(IDX_ERR_INVALID_ARG, "B must be >= 1 and T >= 0");
+    if (max_len < 1 || max_len > 0x7fffffffLL)
+        return noalloc_fail(IDX_ERR_INVALID_ARG, "max_len must be in [1, 2^31-1]");
+    if (topk < 1 || topk > IDX_TOPK_MAX)
+        return noalloc_fail(IDX_ERR_INVALID_ARG, "topk must be in [1, 2048]");
+    if (!cu_q || !cu_k || (T > 0 && (!q || !k || !w || !q_pos || !idx)))
+        return noalloc_fail(IDX_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!is_aligned(q, 16) || !is_aligned(k, 16) || !is_aligned(w, 16) || !is_aligned(q_pos, 4) ||
+        !is_aligned(cu_q, 4) || !is_aligned(cu_k, 4) || !is_aligned(idx, 4) || !is_aligned(cnt, 4))
+        return noalloc_fail(IDX_ERR_INVALID_ARG, "q, k, w must be 16-byte aligned; int32 arrays 4-byte");
+    const int64_t ld = (int64_t)align_up((size_t)max_len, 4);
+    if ((size_t)T * (size_t)ld * sizeof(float) > kNoAllocScoreBytes)
+        return noalloc_fail(IDX_ERR_WORKSPACE,
+                            "T * round_up(max_len, 4) * 4 bytes exceeds the 32 MiB scratch of "
+                            "idx_score_topk_noalloc; use idx_score_topk with a workspace");
+    const DeviceInfo& dev = device_info();
+    if (dev.device < 0) return noalloc_fail(IDX_ERR_CUDA, "no current CUDA device");
+    if (!(dev.cc_major == 10 && dev.cc_minor == 3))
+        return noalloc_fail(IDX_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300) only");
+    cudaError_t e = cudaSuccess;
+    unsigned char* scratch = static_cast<unsigned char*>(noalloc_scratch(&e));
+    if (!scratch) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) return IDX_OK;
+    // Only the status word must start at zero; every staged score is written
+    // before it is read within the same call.
+    DeviceStatus* status = reinterpret_cast<DeviceStatus*>(scratch);
+    e = cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s);
+    if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
+    float* scores = reinterpret_cast<float*>(scratch + kWsHeader);
+    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, max_len, scores, ld, status};
+    e = launch_score_simt(sa, s);
+    if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
+    TopkArgs ta{scores, ld, q_pos, true, T, max_len, topk, idx, cnt, status, cu_q, cu_k, B};
+    e = launch_topk(ta, s);
+    if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
+    return IDX_OK;
+}
