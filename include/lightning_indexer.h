@@ -97,14 +97,16 @@ IDX_API idx_status idx_key_layernorm(const uint16_t* k_raw, const void* ln_w, co
  *     scores[t*ld + s] = sum_h w[t,h] * max(sum_d q[t,h,d] * k[cu_k[b]+s, d], 0)
  * for every query t (of sequence b) and every s < n(t), bf16 products with
  * fp32 accumulation. Entries s >= n(t) of a row are left untouched.
- *   q      bf16 [T,32,128]     k  bf16 [cu_k[B],128] (post-LayerNorm key cache)
+ *   q      bf16 [T,32,128]     k  bf16 [n_keys,128] (post-LayerNorm key cache)
  *   w      fp32 [T,32]         q_pos, cu_q, cu_k: int32 (see Batches)
+ *   n_keys rows of k (>= cu_k[B]); bounds every key read
  *   max_len  an upper bound on n(t) over the batch (host value, >= 1)
  *   scores fp32 [T,ld], ld >= max_len and a multiple of 4
  */
 IDX_API idx_status idx_score(const uint16_t* q, const uint16_t* k, const float* w,
                      const int32_t* q_pos, const int32_t* cu_q, const int32_t* cu_k,
-                     int32_t B, int32_t T, int64_t max_len, float* scores, int64_t ld,
+                     int32_t B, int32_t T, int64_t n_keys, int64_t max_len, float* scores,
+                     int64_t ld,
                      void* ws, size_t ws_bytes, void* stream);
 IDX_API size_t idx_score_workspace_size(int32_t B, int32_t T, int64_t max_len);
 
@@ -136,7 +138,8 @@ IDX_API size_t idx_topk_workspace_size(int32_t T, int64_t max_len, int32_t topk)
  */
 IDX_API idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
                           const int32_t* q_pos, const int32_t* cu_q, const int32_t* cu_k,
-                          int32_t B, int32_t T, int64_t max_len, int32_t topk, int32_t* idx,
+                          int32_t B, int32_t T, int64_t n_keys, int64_t max_len, int32_t topk,
+                          int32_t* idx,
                           int32_t* cnt, void* ws, size_t ws_bytes, void* stream);
 IDX_API size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_len, int32_t topk);
 
@@ -148,11 +151,11 @@ IDX_API size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_l
  * and may fail under memory pressure), or a plugin that its host framework
  * hands only input and output buffers. Same arguments and results as
  * idx_score_topk, minus ws/ws_bytes; it allocates nothing.
- *   Scratch   a fixed 32 MiB (+256 B) array inside the library's device image,
+ *   Scratch   a fixed 33 MiB (+256 B) array inside the library's device image,
  *             reserved on every GPU that loads the library until process exit.
  *   Limit     T * round_up(max_len, 4) * 4 <= 32 MiB (e.g. 64 queries of up to
- *             131,072 keys); larger calls return IDX_ERR_WORKSPACE, enqueue
- *             nothing, and idx_last_error() says why.
+ *             131,072 keys) and T + B <= 40,000; larger calls return
+ *             IDX_ERR_WORKSPACE, enqueue nothing, and idx_last_error() says why.
  *   Sharing   every call on a device uses the same array, which keeps the last
  *             call's contents; calls that can overlap on the GPU (other streams,
  *             unordered host threads) race on it and must be serialised.
@@ -165,7 +168,8 @@ IDX_API size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_l
 IDX_API idx_status idx_score_topk_noalloc(const uint16_t* q, const uint16_t* k, const float* w,
                                           const int32_t* q_pos, const int32_t* cu_q,
                                           const int32_t* cu_k, int32_t B, int32_t T,
-                                          int64_t max_len, int32_t topk, int32_t* idx,
+                                          int64_t n_keys, int64_t max_len, int32_t topk,
+                                          int32_t* idx,
                                           int32_t* cnt, void* stream);
 
 /*

@@ -58,13 +58,14 @@ def lib():
             L = ctypes.CDLL(_LIB_PATH)
             P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
             L.idx_key_layernorm.argtypes = [P, P, P, ctypes.c_int, ctypes.c_float, P, i64, P]
-            L.idx_score.argtypes = [P, P, P, P, P, P, i32, i32, i64, P, i64, P, sz, P]
+            L.idx_score.argtypes = [P, P, P, P, P, P, i32, i32, i64, i64, P, i64, P, sz, P]
             L.idx_score_workspace_size.argtypes = [i32, i32, i64]
             L.idx_score_workspace_size.restype = sz
             L.idx_topk.argtypes = [P, i64, P, i32, i64, i32, P, P, P, sz, P]
             L.idx_topk_workspace_size.argtypes = [i32, i64, i32]
             L.idx_topk_workspace_size.restype = sz
-            L.idx_score_topk.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, P, P, P, sz, P]
+            L.idx_score_topk.argtypes = [P, P, P, P, P, P, i32, i32, i64, i64, i32, P, P, P, sz,
+                                         P]
             L.idx_score_topk_workspace_size.argtypes = [i32, i32, i64, i32]
             L.idx_score_topk_workspace_size.restype = sz
             L.idx_get_status.argtypes = [P, P, ctypes.POINTER(i32)]
@@ -186,7 +187,8 @@ def score(q, k, w, q_pos, cu_q, cu_k, max_len: int, ld: int | None = None,
     if ws is None:
         ws = workspace(need, q.device)
     _check(lib().idx_score(_ptr(q), _ptr(k), _ptr(w), _ptr(q_pos), _ptr(cu_q), _ptr(cu_k), B, T,
-                           max_len, _ptr(out), ld, _ptr(ws), ws.numel(), _stream()), "idx_score")
+                           k.shape[0], max_len, _ptr(out), ld, _ptr(ws), ws.numel(), _stream()),
+           "idx_score")
     return out
 
 
@@ -228,8 +230,8 @@ def score_topk(q, k, w, q_pos, cu_q, cu_k, max_len: int, topk: int = TOPK_MAX,
     if ws is None:
         ws = workspace(need, q.device)
     _check(lib().idx_score_topk(_ptr(q), _ptr(k), _ptr(w), _ptr(q_pos), _ptr(cu_q), _ptr(cu_k), B,
-                                T, max_len, topk, _ptr(idx), _ptr(cnt), _ptr(ws), ws.numel(),
-                                _stream()), "idx_score_topk")
+                                T, k.shape[0], max_len, topk, _ptr(idx), _ptr(cnt), _ptr(ws),
+                                ws.numel(), _stream()), "idx_score_topk")
     return idx, cnt
 
 
@@ -269,8 +271,8 @@ def score_topk_noalloc(q, k, w, q_pos, cu_q, cu_k, max_len: int, topk: int = TOP
     _dev(cnt, "cnt", _I32, (T,))
     fn = lib().idx_score_topk_noalloc
     P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-    fn.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, P, P, P]
+    fn.argtypes = [P, P, P, P, P, P, i32, i32, i64, i64, i32, P, P, P]
     fn.restype = ctypes.c_int
-    _check(fn(_ptr(q), _ptr(k), _ptr(w), _ptr(q_pos), _ptr(cu_q), _ptr(cu_k), B, T, max_len, topk,
-              _ptr(idx), _ptr(cnt), _stream()), "idx_score_topk_noalloc")
+    _check(fn(_ptr(q), _ptr(k), _ptr(w), _ptr(q_pos), _ptr(cu_q), _ptr(cu_k), B, T, k.shape[0],
+              max_len, topk, _ptr(idx), _ptr(cnt), _stream()), "idx_score_topk_noalloc")
     return idx, cnt

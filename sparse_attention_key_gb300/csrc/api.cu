@@ -95,13 +95,16 @@ static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 // Staged-score row stride used inside a fused call's workspace.
 static int64_t staged_ld(int64_t max_len) { return (int64_t)align_up((size_t)max_len, 4); }
 
-static size_t score_plan_bytes(int32_t /*B*/, int32_t /*T*/) { return 0; }
+static size_t score_plan_bytes(int32_t B, int32_t T) { return tc_plan_bytes(B, T); }
 
 static idx_status check_batch(const void* q, const void* k, const void* w, const void* q_pos,
                               const void* cu_q, const void* cu_k, int32_t B, int32_t T,
-                              int64_t max_len) {
+                              int64_t n_keys, int64_t max_len) {
     if (B < 1) return fail(IDX_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
     if (T < 0) return fail(IDX_ERR_INVALID_ARG, "T must be >= 0 (got %d)", T);
+    if (n_keys < 0 || n_keys > 0x7fffffffLL)
+        return fail(IDX_ERR_INVALID_ARG, "n_keys must be in [0, 2^31-1] (got %lld)",
+                    (long long)n_keys);
     if (max_len < 1 || max_len > 0x7fffffffLL)
         return fail(IDX_ERR_INVALID_ARG, "max_len must be in [1, 2^31-1] (got %lld)",
                     (long long)max_len);
@@ -165,10 +168,10 @@ size_t idx_score_workspace_size(int32_t B, int32_t T, int64_t /*max_len*/) {
 
 idx_status idx_score(const uint16_t* q, const uint16_t* k, const float* w, const int32_t* q_pos,
                      const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t T,
-                     int64_t max_len, float* scores, int64_t ld, void* ws, size_t ws_bytes,
-                     void* stream) {
+                     int64_t n_keys, int64_t max_len, float* scores, int64_t ld, void* ws,
+                     size_t ws_bytes, void* stream) {
     g_last_error[0] = 0;
-    if (idx_status st = check_batch(q, k, w, q_pos, cu_q, cu_k, B, T, max_len)) return st;
+    if (idx_status st = check_batch(q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len)) return st;
     if (ld < max_len || ld % 4 != 0)
         return fail(IDX_ERR_INVALID_ARG, "ld must be >= max_len and a multiple of 4");
     if (T > 0 && (!scores || !aligned(scores, 16)))
@@ -178,8 +181,8 @@ idx_status idx_score(const uint16_t* q, const uint16_t* k, const float* w, const
     cudaStream_t s = (cudaStream_t)stream;
     if (idx_status st = clear_status(ws, s)) return st;
     if (T == 0) return IDX_OK;
-    ScoreArgs a{q, k, w, q_pos, cu_q, cu_k, B, T, max_len, scores, ld, (DeviceStatus*)ws};
-    cudaError_t e = launch_score_simt(a, s);
+    ScoreArgs a{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, (DeviceStatus*)ws};
+    cudaError_t e = launch_score_tc(a, (char*)ws + kWsHeader, s);
     return e == cudaSuccess ? IDX_OK : cuda_fail(e, "score launch");
 }
 
@@ -219,10 +222,10 @@ size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_len, int3
 
 idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
                           const int32_t* q_pos, const int32_t* cu_q, const int32_t* cu_k,
-                          int32_t B, int32_t T, int64_t max_len, int32_t topk, int32_t* idx,
-                          int32_t* cnt, void* ws, size_t ws_bytes, void* stream) {
+                          int32_t B, int32_t T, int64_t n_keys, int64_t max_len, int32_t topk,
+                          int32_t* idx, int32_t* cnt, void* ws, size_t ws_bytes, void* stream) {
     g_last_error[0] = 0;
-    if (idx_status st = check_batch(q, k, w, q_pos, cu_q, cu_k, B, T, max_len)) return st;
+    if (idx_status st = check_batch(q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len)) return st;
     if (topk < 1 || topk > IDX_TOPK_MAX)
         return fail(IDX_ERR_INVALID_ARG, "topk must be in [1, %d] (got %d)", IDX_TOPK_MAX, topk);
     if (T > 0 && !idx) return fail(IDX_ERR_INVALID_ARG, "idx must not be NULL");
@@ -238,8 +241,8 @@ idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
     char* base = (char*)ws + kWsHeader + align_up(score_plan_bytes(B, T), 256);
     float* scores = (float*)base;
     DeviceStatus* status = (DeviceStatus*)ws;
-    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, max_len, scores, ld, status};
-    cudaError_t e = launch_score_simt(sa, s);
+    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, status};
+    cudaError_t e = launch_score_tc(sa, (char*)ws + kWsHeader, s);
     if (e != cudaSuccess) return cuda_fail(e, "score launch");
     TopkArgs ta{scores, ld, q_pos, true, T, max_len, topk, idx, cnt, status, cu_q, cu_k, B};
     e = launch_topk(ta, s);

@@ -41,6 +41,7 @@ struct ScoreArgs {
     const int32_t* cu_q;
     const int32_t* cu_k;
     int32_t B, T;
+    int64_t n_keys;    // rows of k
     int64_t max_len;
     float* scores;
     int64_t ld;
@@ -49,6 +50,11 @@ struct ScoreArgs {
 
 // CUDA-core scorer: one thread per key, streams K with 16-byte loads.
 cudaError_t launch_score_simt(const ScoreArgs& a, cudaStream_t stream);
+
+// Tensor-core scorer (tcgen05/TMEM/TMA): a plan kernel, then the persistent
+// scorer. `plan_ws` holds tc_plan_bytes(B, T) bytes of device scratch.
+size_t tc_plan_bytes(int32_t B, int32_t T);
+cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream);
 
 // Arguments of one top-K call.
 struct TopkArgs {

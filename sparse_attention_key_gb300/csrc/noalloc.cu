@@ -12,8 +12,9 @@
 // Limits and sharing:
 //   - The scratch array holds kNoAllocScoreBytes (32 MiB) of staged scores:
 //     T * round_up(max_len, 4) * 4 bytes must fit, e.g. 64 queries with up to
-//     131,072 keys each. Larger calls are rejected on the host (IDX_ERR_WORKSPACE).
-//   - Every GPU that loads the library reserves the array (32 MiB + 256 B)
+//     131,072 keys each; and 1 MiB of tile plan: T + B <= 40,000. Larger calls
+//     are rejected on the host (IDX_ERR_WORKSPACE).
+//   - Every GPU that loads the library reserves the array (33 MiB + 256 B)
 //     until the process exits.
 //   - All calls on a device share the one array and it keeps the contents of
 //     the last call: calls that can overlap on the GPU (different streams, or
@@ -30,8 +31,9 @@
 
 namespace lidx {
 
-constexpr size_t kNoAllocScoreBytes = size_t(32) << 20;                 // staged fp32 scores
-constexpr size_t kNoAllocScratchBytes = kWsHeader + kNoAllocScoreBytes;  // + status header
+constexpr size_t kNoAllocScoreBytes = size_t(32) << 20;  // staged fp32 scores
+constexpr size_t kNoAllocPlanBytes = size_t(1) << 20;    // tile plan of the scorer
+constexpr size_t kNoAllocScratchBytes = kWsHeader + kNoAllocPlanBytes + kNoAllocScoreBytes;
 
 // Library-owned scratch. Host code must not use this name as a pointer: on the
 // host it only stands for the symbol; its device address comes from
@@ -82,10 +84,12 @@ using namespace lidx;
 
 extern "C" IDX_API idx_status idx_score_topk_noalloc(
     const uint16_t* q, const uint16_t* k, const float* w, const int32_t* q_pos,
-    const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t T, int64_t max_len,
-    int32_t topk, int32_t* idx, int32_t* cnt, void* stream) {
+    const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t T, int64_t n_keys,
+    int64_t max_len, int32_t topk, int32_t* idx, int32_t* cnt, void* stream) {
     set_last_error_text("");
     if (B < 1 || T < 0) return noalloc_fail(IDX_ERR_INVALID_ARG, "B must be >= 1 and T >= 0");
+    if (n_keys < 0 || n_keys > 0x7fffffffLL)
+        return noalloc_fail(IDX_ERR_INVALID_ARG, "n_keys must be in [0, 2^31-1]");
     if (max_len < 1 || max_len > 0x7fffffffLL)
         return noalloc_fail(IDX_ERR_INVALID_ARG, "max_len must be in [1, 2^31-1]");
     if (topk < 1 || topk > IDX_TOPK_MAX)
@@ -100,6 +104,10 @@ extern "C" IDX_API idx_status idx_score_topk_noalloc(
         return noalloc_fail(IDX_ERR_WORKSPACE,
                             "T * round_up(max_len, 4) * 4 bytes exceeds the 32 MiB scratch of "
                             "idx_score_topk_noalloc; use idx_score_topk with a workspace");
+    if (tc_plan_bytes(B, T) > kNoAllocPlanBytes || (int64_t)T + B > 40000)
+        return noalloc_fail(IDX_ERR_WORKSPACE,
+                            "T + B exceeds the 40,000 query rows and sequences that the 1 MiB plan "
+                            "of idx_score_topk_noalloc holds; use idx_score_topk with a workspace");
     const DeviceInfo& dev = device_info();
     if (dev.device < 0) return noalloc_fail(IDX_ERR_CUDA, "no current CUDA device");
     if (!(dev.cc_major == 10 && dev.cc_minor == 3))
@@ -114,9 +122,10 @@ extern "C" IDX_API idx_status idx_score_topk_noalloc(
     DeviceStatus* status = reinterpret_cast<DeviceStatus*>(scratch);
     e = cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s);
     if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
-    float* scores = reinterpret_cast<float*>(scratch + kWsHeader);
-    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, max_len, scores, ld, status};
-    e = launch_score_simt(sa, s);
+    void* plan = scratch + kWsHeader;
+    float* scores = reinterpret_cast<float*>(scratch + kWsHeader + kNoAllocPlanBytes);
+    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, status};
+    e = launch_score_tc(sa, plan, s);
     if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
     TopkArgs ta{scores, ld, q_pos, true, T, max_len, topk, idx, cnt, status, cu_q, cu_k, B};
     e = launch_topk(ta, s);

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kSimtKeys)
 score_simt_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                   const float* __restrict__ w, const int32_t* __restrict__ q_pos,
                   const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B,
-                  int T, int64_t max_len, float* __restrict__ scores, int64_t ld,
+                  int T, int64_t n_keys, int64_t max_len, float* __restrict__ scores, int64_t ld,
                   DeviceStatus* status) {
     __shared__ __align__(16) float qs[kHeads * kDim];  // 16 KB
     __shared__ float ws[kHeads];
@@ -46,7 +46,7 @@ score_simt_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k
         const int64_t key0 = __ldg(cu_k + b);
         const int64_t len_k = (int64_t)__ldg(cu_k + b + 1) - key0;
         const int64_t n = (int64_t)__ldg(q_pos + t) + 1;
-        if (n < 1 || n > len_k || n > max_len) {
+        if (n < 1 || n > len_k || n > max_len || key0 < 0 || key0 + len_k > n_keys) {
             if (blockIdx.x == 0 && threadIdx.x == 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
             continue;
         }
@@ -104,7 +104,8 @@ cudaError_t launch_score_simt(const ScoreArgs& a, cudaStream_t stream) {
     if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
     dim3 grid((unsigned)tiles, (unsigned)(a.T < 65535 ? a.T : 65535));
     score_simt_kernel<<<grid, kSimtKeys, 0, stream>>>(a.q, a.k, a.w, a.q_pos, a.cu_q, a.cu_k, a.B,
-                                                      a.T, a.max_len, a.scores, a.ld, a.status);
+                                                      a.T, a.n_keys, a.max_len, a.scores, a.ld,
+                                                      a.status);
     count_launch();
     return cudaGetLastError();
 }

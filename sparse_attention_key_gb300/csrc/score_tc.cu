@@ -1,0 +1,568 @@
+// Tensor-core scorer of the Lightning Indexer (tcgen05 + TMEM + TMA, sm_103a).
+//
+//   S[t,s] = sum_h w[t,h] * max(q[t,h,:] . k[s,:], 0)     for s < n(t) = q_pos[t] + 1
+//
+// ("Notes from an NVFP4 port of Kimi K3.1 Pro", indexer paragraph; no rotary,
+// item (3) of "Details that silently change the answer".)
+//
+// The per-head dot products are one dense contraction per (query group, key
+// tile): D[key, (query, head)] = K_tile[128 x 128] . Q_group[(query,head) x 128]^T,
+// i.e. M = 128 keys, N = 32 heads x NQ queries, K = 128 dims. Keys are the M
+// side so that one TMEM lane holds one key and the relu / head-weighted sum of
+// a query is a loop over 32 consecutive accumulator columns inside one thread:
+// the [T,32,L] intermediate never leaves TMEM and registers.
+//
+// Work decomposition. Queries of a sequence form groups of GQ = NQ * NSUB
+// consecutive rows; a group needs ceil(max n(t) / 128) key tiles ("steps"). A
+// plan kernel lists the groups and prefix-sums their steps; the scorer runs
+// one CTA per SM and gives each CTA an equal contiguous range of steps, so a
+// CTA streams key tiles of one group while the group's queries stay resident
+// in shared memory.
+//
+// Roles inside a CTA (warp specialisation):
+//   warp 0        TMA producer: the group's Q tile once per group, then key
+//                 tiles into a STAGES-deep ring (128-byte swizzle).
+//   warp 1        TMEM allocator and MMA issuer (one thread): per key tile and
+//                 sub-group, 8 MMAs of K = 16 into one of NACC accumulators.
+//   warps 2..     epilogue: tcgen05.ld of 32 columns per query, relu, weight,
+//                 head sum, coalesced store of the fp32 score (masked to the
+//                 causal length).
+// Every wait is bounded (globaltimer); a timeout records IDX_ERR_TIMEOUT in
+// the status word, raises a shared abort flag that ends all roles, waits for
+// copies and MMAs still in flight (bounded) and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_primitives.cuh"
+
+namespace lidx {
+
+// ---------------------------------------------------------------------------
+// plan
+// ---------------------------------------------------------------------------
+struct TcPlanHeader {
+    int32_t n_groups;
+    int32_t total_steps;
+    int32_t pad[2];
+};
+
+size_t tc_plan_bytes(int32_t B, int32_t T) {
+    const size_t g = (size_t)T + (size_t)B + 1;  // >= number of groups for any GQ >= 1
+    return align_up(sizeof(TcPlanHeader), 256) + align_up(g * sizeof(int4), 256) +
+           align_up((g + 1) * sizeof(int32_t), 256);
+}
+
+struct TcPlan {
+    TcPlanHeader* hdr;
+    int4* groups;        // {sequence, first query row, queries, key tiles}
+    int32_t* step_begin; // [n_groups + 1]
+    int32_t capacity;    // entries of groups
+};
+
+static TcPlan plan_layout(void* base, int32_t B, int32_t T) {
+    const size_t g = (size_t)T + (size_t)B + 1;
+    char* p = static_cast<char*>(base);
+    TcPlan pl;
+    pl.hdr = reinterpret_cast<TcPlanHeader*>(p);
+    pl.groups = reinterpret_cast<int4*>(p + align_up(sizeof(TcPlanHeader), 256));
+    pl.step_begin = reinterpret_cast<int32_t*>(p + align_up(sizeof(TcPlanHeader), 256) +
+                                               align_up(g * sizeof(int4), 256));
+    pl.capacity = (int32_t)g;
+    return pl;
+}
+
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ int block_exclusive_sum(int v, int* warp_sums, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int ws = warp_sums[lane];
+        int wi = ws;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += x;
+        }
+        warp_sums[lane] = wi - ws;
+        if (lane == 31) warp_sums[32] = wi;
+    }
+    __syncthreads();
+    const int res = warp_sums[warp] + incl - v;
+    *total = warp_sums[32];
+    __syncthreads();
+    return res;
+}
+
+template <int GQ>
+__global__ void __launch_bounds__(kPlanThreads)
+tc_plan_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu_q,
+               const int32_t* __restrict__ cu_k, int B, int T, int64_t n_keys, int64_t max_len,
+               TcPlan plan, DeviceStatus* status) {
+    __shared__ int warp_sums[33];
+    __shared__ int overflow;
+    if (threadIdx.x == 0) overflow = 0;
+    __syncthreads();
+
+    // groups of each sequence
+    int carry = 0;
+    for (int base = 0; base < B; base += kPlanThreads) {
+        const int b = base + threadIdx.x;
+        int cnt = 0, nq = 0, q0 = 0;
+        if (b < B) {
+            q0 = __ldg(cu_q + b);
+            nq = __ldg(cu_q + b + 1) - q0;
+            if (q0 < 0 || nq < 0 || (int64_t)q0 + nq > T) {
+                report_error(status, IDX_ERR_DEVICE_ARG, -1 - b);
+                nq = 0;
+            }
+            cnt = (nq + GQ - 1) / GQ;
+        }
+        int total;
+        const int off = carry + block_exclusive_sum(cnt, warp_sums, &total);
+        for (int j = 0; j < cnt; ++j) {
+            if (off + j < plan.capacity)
+                plan.groups[off + j] = make_int4(b, q0 + j * GQ, min(GQ, nq - j * GQ), 0);
+            else
+                overflow = 1;
+        }
+        carry += total;
+    }
+    __syncthreads();
+    if (overflow || carry >= plan.capacity) {  // cu_q is not a partition of 0..T
+        if (threadIdx.x == 0) {
+            report_error(status, IDX_ERR_DEVICE_ARG, -1);
+            plan.hdr->n_groups = 0;
+            plan.hdr->total_steps = 0;
+            plan.step_begin[0] = 0;
+        }
+        return;
+    }
+    const int n_groups = carry;
+
+    // key tiles of each group: the longest valid causal history among its queries
+    for (int g = threadIdx.x; g < n_groups; g += kPlanThreads) {
+        int4 d = plan.groups[g];
+        const int64_t k0 = __ldg(cu_k + d.x), k1 = __ldg(cu_k + d.x + 1);
+        const bool seq_ok = k0 >= 0 && k1 >= k0 && k1 <= n_keys;
+        int64_t nmax = 0;
+        for (int i = 0; i < d.z; ++i) {
+            const int t = d.y + i;
+            const int64_t n = (int64_t)__ldg(q_pos + t) + 1;
+            if (!seq_ok || n < 1 || n > k1 - k0 || n > max_len) {
+                report_error(status, IDX_ERR_DEVICE_ARG, t);
+                continue;
+            }
+            nmax = n > nmax ? n : nmax;
+        }
+        d.w = (int)((nmax + 127) / 128);
+        plan.groups[g] = d;
+    }
+    __syncthreads();
+
+    // prefix sum of steps
+    carry = 0;
+    for (int base = 0; base < n_groups; base += kPlanThreads) {
+        const int g = base + threadIdx.x;
+        const int v = g < n_groups ? plan.groups[g].w : 0;
+        int total;
+        const int off = carry + block_exclusive_sum(v, warp_sums, &total);
+        if (g < n_groups) plan.step_begin[g] = off;
+        carry += total;
+    }
+    if (threadIdx.x == 0) {
+        plan.step_begin[n_groups] = carry;
+        plan.hdr->n_groups = n_groups;
+        plan.hdr->total_steps = carry;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// scorer
+// ---------------------------------------------------------------------------
+template <int NQ_, int NSUB_, int NACC_, int STAGES_, int EPI_WARPS_>
+struct TcCfg {
+    static constexpr int NQ = NQ_;          // queries per MMA
+    static constexpr int NSUB = NSUB_;      // MMAs (sub-groups) per key tile
+    static constexpr int NACC = NACC_;      // TMEM accumulators in flight
+    static constexpr int STAGES = STAGES_;  // key-tile ring depth
+    static constexpr int EPI_WARPS = EPI_WARPS_;
+    static constexpr int N = NQ * 32;
+    static constexpr int GQ = NQ * NSUB;
+    static constexpr int QROWS = GQ * 32;
+    static constexpr int Q_HALF = QROWS * 128;       // bytes of one 64-dim half of Q
+    static constexpr int Q_BYTES = 2 * Q_HALF;
+    static constexpr int K_HALF = 128 * 128;
+    static constexpr int K_STAGE = 2 * K_HALF;        // 32 KB per key tile
+    static constexpr int Q_BOX_ROWS = QROWS < 256 ? QROWS : 256;
+    static constexpr int TMEM_COLS = NACC * N;
+    static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * NACC + 3) + 16;
+    static constexpr int SMEM = 1024 + Q_BYTES + STAGES * K_STAGE + BAR_BYTES;
+    static_assert(N % 16 == 0 && N >= 32 && N <= 256, "MMA N");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "TMEM allocation must be a power of two in [32, 512]");
+    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps cover the 4 lane quarters");
+    static_assert(NQ % (EPI_WARPS / 4) == 0, "queries split evenly over a quarter's warps");
+    static_assert(QROWS % Q_BOX_ROWS == 0, "Q box");
+};
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: no legitimate wait comes close
+constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms to drain after an abort
+
+// Walks the steps [beg, end) of a CTA: which group, which key tile.
+struct StepCursor {
+    int g;
+    int j;                 // key tile within the group
+    int32_t next_begin;    // first step of the next group
+    int4 desc;
+
+    __device__ __forceinline__ void init(int32_t s, const TcPlan& p, int n_groups) {
+        int lo = 0, hi = n_groups - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.step_begin + mid) <= s) lo = mid; else hi = mid - 1;
+        }
+        g = lo;
+        desc = p.groups[g];
+        j = s - __ldg(p.step_begin + g);
+        next_begin = __ldg(p.step_begin + g + 1);
+    }
+    // Move to step s (= previous + 1); true when the group changed.
+    __device__ __forceinline__ bool advance(int32_t s, const TcPlan& p) {
+        ++j;
+        if (s < next_begin) return false;
+        do {
+            ++g;
+            next_begin = __ldg(p.step_begin + g + 1);
+        } while (s >= next_begin);
+        desc = p.groups[g];
+        j = s - __ldg(p.step_begin + g);
+        return true;
+    }
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                const float* __restrict__ w, const int32_t* __restrict__ q_pos,
+                const int32_t* __restrict__ cu_k, int64_t max_len, float* __restrict__ scores,
+                int64_t ld, TcPlan plan, DeviceStatus* status) {
+    using namespace ptx;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* q_smem = smem;
+    uint8_t* k_smem = smem + C::Q_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(k_smem + C::STAGES * C::K_STAGE);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = bars + C::STAGES;
+    uint64_t* acc_full = bars + 2 * C::STAGES;
+    uint64_t* acc_empty = acc_full + C::NACC;
+    uint64_t* q_full = acc_empty + C::NACC;
+    uint64_t* q_empty = q_full + 1;
+    uint64_t* done_bar = q_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(k_full + s, 1);
+            mbar_init(k_empty + s, 1);
+        }
+        for (int a = 0; a < C::NACC; ++a) {
+            mbar_init(acc_full + a, 1);
+            mbar_init(acc_empty + a, C::EPI_WARPS);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_groups = plan.hdr->n_groups;
+    const int64_t total = plan.hdr->total_steps;
+    const int32_t beg = (int32_t)(total * blockIdx.x / gridDim.x);
+    const int32_t end = (int32_t)(total * (blockIdx.x + 1) / gridDim.x);
+
+    bool aborted = false;
+    auto give_up = [&](int site) {
+        if (!*abort_flag) report_error(status, IDX_ERR_TIMEOUT, site);
+        *abort_flag = 1;
+        aborted = true;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && beg < end) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int q_loads = 0;
+            int issued[C::STAGES];
+#pragma unroll
+            for (int s = 0; s < C::STAGES; ++s) issued[s] = 0;
+            StepCursor cur;
+            cur.init(beg, plan, n_groups);
+            bool new_group = true;
+            for (int32_t s = beg; s < end; ++s) {
+                if (s > beg) new_group = cur.advance(s, plan);
+                if (new_group) {
+                    if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, abort_flag, kWaitLimitNs)) {
+                        give_up(1);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+                    const int32_t qrow0 = cur.desc.y * 32;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+#pragma unroll
+                        for (int r = 0; r < C::QROWS; r += C::Q_BOX_ROWS)
+                            tma_load_2d(smem_addr(q_smem + half * C::Q_HALF + r * 128), &tmap_q,
+                                        q_full, half * 64, qrow0 + r);
+                    ++q_loads;
+                }
+                if (!mbar_wait(k_empty + stage, phase ^ 1, abort_flag, kWaitLimitNs)) {
+                    give_up(2);
+                    break;
+                }
+                mbar_arrive_expect_tx(k_full + stage, C::K_STAGE);
+                const int32_t key_row = __ldg(cu_k + cur.desc.x) + cur.j * 128;
+                uint8_t* dst = k_smem + stage * C::K_STAGE;
+                tma_load_2d(smem_addr(dst), &tmap_k, k_full + stage, 0, key_row);
+                tma_load_2d(smem_addr(dst + C::K_HALF), &tmap_k, k_full + stage, 64, key_row);
+                ++issued[stage];
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (aborted || *abort_flag) {  // let every copy already issued land
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (issued[s] > 0) mbar_wait(k_full + s, (issued[s] - 1) & 1, nullptr, kDrainLimitNs);
+                if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, nullptr, kDrainLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0 && beg < end) {
+            constexpr uint32_t kIdesc = idesc_bf16_f32(128, C::N);
+            const uint32_t q_base = smem_addr(q_smem), k_base = smem_addr(k_smem);
+            int stage = 0, acc = 0, q_uses = 0;
+            uint32_t phase = 0, aphase = 0;
+            StepCursor cur;
+            cur.init(beg, plan, n_groups);
+            bool new_group = true;
+            for (int32_t s = beg; s < end && !aborted; ++s) {
+                if (s > beg) new_group = cur.advance(s, plan);
+                if (new_group) {
+                    if (!mbar_wait(q_full, q_uses & 1, abort_flag, kWaitLimitNs)) {
+                        give_up(3);
+                        break;
+                    }
+                    ++q_uses;
+                }
+                if (!mbar_wait(k_full + stage, phase, abort_flag, kWaitLimitNs)) {
+                    give_up(4);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t k_addr = k_base + stage * C::K_STAGE;
+#pragma unroll 1
+                for (int sub = 0; sub < C::NSUB; ++sub) {
+                    if (!mbar_wait(acc_empty + acc, aphase ^ 1, abort_flag, kWaitLimitNs)) {
+                        give_up(5);
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d_tmem = tmem_base + acc * C::N;
+                    const uint32_t b_addr = q_base + sub * C::N * 128;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk & 3) * 32;
+                        const uint64_t a_desc = smem_desc_sw128(k_addr + (kk >> 2) * C::K_HALF + koff);
+                        const uint64_t b_desc = smem_desc_sw128(b_addr + (kk >> 2) * C::Q_HALF + koff);
+                        tc_mma_bf16(d_tmem, a_desc, b_desc, kIdesc, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(acc_full + acc);
+                    if (++acc == C::NACC) {
+                        acc = 0;
+                        aphase ^= 1;
+                    }
+                }
+                if (aborted) break;
+                tc_commit(k_empty + stage);
+                if (s + 1 == end || s + 1 >= cur.next_begin) tc_commit(q_empty);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            // Wait for every MMA issued so far (and thereby for the arrivals of
+            // the commits before this one) before shared memory is released.
+            tc_commit(done_bar);
+            mbar_wait(done_bar, 0, nullptr, kDrainLimitNs);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        constexpr int kSplit = C::EPI_WARPS / 4;      // warps sharing a TMEM lane quarter
+        constexpr int kQpw = C::NQ / kSplit;          // queries per warp per sub-group
+        const int quarter = warp & 3;
+        const int qoff = ((warp - 2) / 4) * kQpw;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+        int acc = 0;
+        uint32_t aphase = 0;
+        if (beg < end) {
+            StepCursor cur;
+            cur.init(beg, plan, n_groups);
+            for (int32_t s = beg; s < end && !aborted; ++s) {
+                if (s > beg) cur.advance(s, plan);
+                const int b = cur.desc.x, q0 = cur.desc.y, nq = cur.desc.z;
+                const int64_t k0 = __ldg(cu_k + b);
+                const int64_t len_k = (int64_t)__ldg(cu_k + b + 1) - k0;
+                const int64_t key = (int64_t)cur.j * 128 + quarter * 32 + lane;
+#pragma unroll 1
+                for (int sub = 0; sub < C::NSUB; ++sub) {
+                    if (!mbar_wait(acc_full + acc, aphase, abort_flag, kWaitLimitNs)) {
+                        give_up(6);
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    uint32_t v[kQpw][32];
+#pragma unroll
+                    for (int qi = 0; qi < kQpw; ++qi)
+                        tmem_ld_x32(lane_base + acc * C::N + (qoff + qi) * 32, v[qi]);
+                    tmem_ld_wait(v[0]);
+#pragma unroll
+                    for (int qi = 1; qi < kQpw; ++qi) reg_fence(v[qi]);
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty + acc);
+                    if (++acc == C::NACC) {
+                        acc = 0;
+                        aphase ^= 1;
+                    }
+#pragma unroll
+                    for (int qi = 0; qi < kQpw; ++qi) {
+                        const int qrow = sub * C::NQ + qoff + qi;
+                        if (qrow >= nq) continue;
+                        const int t = q0 + qrow;
+                        const int64_t n = (int64_t)__ldg(q_pos + t) + 1;
+                        if (n < 1 || n > len_k || n > max_len || key >= n) continue;
+                        const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)t * 32);
+                        float S = 0.f;
+#pragma unroll
+                        for (int h4 = 0; h4 < 8; ++h4) {
+                            const float4 ww = __ldg(w4 + h4);
+                            S = fmaf(ww.x, fmaxf(__uint_as_float(v[qi][4 * h4 + 0]), 0.f), S);
+                            S = fmaf(ww.y, fmaxf(__uint_as_float(v[qi][4 * h4 + 1]), 0.f), S);
+                            S = fmaf(ww.z, fmaxf(__uint_as_float(v[qi][4 * h4 + 2]), 0.f), S);
+                            S = fmaf(ww.w, fmaxf(__uint_as_float(v[qi][4 * h4 + 3]), 0.f), S);
+                        }
+                        scores[(int64_t)t * ld + key] = S;
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, 128] with 256-byte rows, loaded as {64, box_rows}
+// boxes with the 128-byte swizzle; rows past the end read as zero.
+static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {128, (cuuint64_t)(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Prefill: 16 queries per group as 2 MMAs of N = 256, two 256-column TMEM
+// accumulators, 2-stage key ring, 8 epilogue warps.
+using PrefillCfg = TcCfg<8, 2, 2, 2, 8>;
+// Decode: one query per group, N = 32, four accumulators, 6-stage key ring.
+using DecodeCfg = TcCfg<1, 1, 4, 6, 4>;
+
+template <class C>
+static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream_t stream) {
+    CUtensorMap tk, tq;
+    if (!make_tmap(&tk, a.k, a.n_keys, 128) || !make_tmap(&tq, a.q, (int64_t)a.T * 32, C::Q_BOX_ROWS))
+        return cudaErrorInvalidValue;
+    tc_plan_kernel<C::GQ><<<1, kPlanThreads, 0, stream>>>(a.q_pos, a.cu_q, a.cu_k, a.B, a.T,
+                                                          a.n_keys, a.max_len, plan, a.status);
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_optin((const void*)score_tc_kernel<C>, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const DeviceInfo& dev = device_info();
+    score_tc_kernel<C><<<dev.sm_count, C::THREADS, C::SMEM, stream>>>(
+        tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan, a.status);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream) {
+    const TcPlan plan = plan_layout(plan_ws, a.B, a.T);
+    // Mostly one query per sequence (decode) vs. many (prefill / chunks).
+    if ((int64_t)a.T <= 2 * (int64_t)a.B) return launch_cfg<DecodeCfg>(a, plan, stream);
+    return launch_cfg<PrefillCfg>(a, plan, stream);
+}
+
+}  // namespace lidx

@@ -67,18 +67,18 @@ NULL = None
 
 
 def _score_topk(L, **kw):
-    a = dict(q=FAKE, k=FAKE, w=FAKE, q_pos=FAKE, cu_q=FAKE, cu_k=FAKE, B=1, T=4, max_len=100,
-             topk=2048, idx=FAKE, cnt=NULL, ws=FAKE, ws_bytes=1 << 30, stream=NULL)
+    a = dict(q=FAKE, k=FAKE, w=FAKE, q_pos=FAKE, cu_q=FAKE, cu_k=FAKE, B=1, T=4, n_keys=100,
+             max_len=100, topk=2048, idx=FAKE, cnt=NULL, ws=FAKE, ws_bytes=1 << 30, stream=NULL)
     a.update(kw)
     return L.idx_score_topk(a["q"], a["k"], a["w"], a["q_pos"], a["cu_q"], a["cu_k"], a["B"],
-                            a["T"], a["max_len"], a["topk"], a["idx"], a["cnt"], a["ws"],
-                            a["ws_bytes"], a["stream"])
+                            a["T"], a["n_keys"], a["max_len"], a["topk"], a["idx"], a["cnt"],
+                            a["ws"], a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=NULL), 1), (dict(k=NULL), 1), (dict(w=NULL), 1), (dict(q_pos=NULL), 1),
     (dict(cu_q=NULL), 1), (dict(cu_k=NULL), 1), (dict(idx=NULL), 1),
-    (dict(B=0), 1), (dict(T=-1), 1), (dict(max_len=0), 1), (dict(topk=0), 1),
+    (dict(B=0), 1), (dict(T=-1), 1), (dict(max_len=0), 1), (dict(topk=0), 1), (dict(n_keys=-1), 1),
     (dict(topk=2049), 1), (dict(q=ctypes.c_void_p(4098)), 1),
     (dict(ws=NULL), 3), (dict(ws_bytes=16), 3), (dict(ws=ctypes.c_void_p(4096 + 16)), 3),
 ])
@@ -107,12 +107,12 @@ def test_topk_host_errors(L):
 
 def test_score_host_errors(L):
     def call(**kw):
-        a = dict(q=FAKE, k=FAKE, w=FAKE, q_pos=FAKE, cu_q=FAKE, cu_k=FAKE, B=1, T=2, max_len=64,
-                 scores=FAKE, ld=64, ws=FAKE, ws_bytes=1 << 20, stream=NULL)
+        a = dict(q=FAKE, k=FAKE, w=FAKE, q_pos=FAKE, cu_q=FAKE, cu_k=FAKE, B=1, T=2, n_keys=64,
+                 max_len=64, scores=FAKE, ld=64, ws=FAKE, ws_bytes=1 << 20, stream=NULL)
         a.update(kw)
         return L.idx_score(a["q"], a["k"], a["w"], a["q_pos"], a["cu_q"], a["cu_k"], a["B"],
-                           a["T"], a["max_len"], a["scores"], a["ld"], a["ws"], a["ws_bytes"],
-                           a["stream"])
+                           a["T"], a["n_keys"], a["max_len"], a["scores"], a["ld"], a["ws"],
+                           a["ws_bytes"], a["stream"])
     assert call(ld=60) == 1            # ld < max_len
     assert call(ld=66) == 1            # not a multiple of 4
     assert call(scores=NULL) == 1

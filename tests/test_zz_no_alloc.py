@@ -30,7 +30,7 @@ def L():
     from sparse_attention_key_gb300 import binding
     lib = binding.lib()
     P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-    lib.idx_score_topk_noalloc.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, P, P, P]
+    lib.idx_score_topk_noalloc.argtypes = [P, P, P, P, P, P, i32, i32, i64, i64, i32, P, P, P]
     lib.idx_score_topk_noalloc.restype = ctypes.c_int
     return lib
 
@@ -44,8 +44,8 @@ def _noalloc(L, d, T, B, max_len, K):
     cnt = torch.full((T,), -7, dtype=torch.int32, device="cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rc = L.idx_score_topk_noalloc(_p(d["q"]), _p(d["k"]), _p(d["w"]), _p(d["q_pos"]),
-                                  _p(d["cu_q"]), _p(d["cu_k"]), B, T, max_len, K, _p(idx),
-                                  _p(cnt), stream)
+                                  _p(d["cu_q"]), _p(d["cu_k"]), B, T, d["k"].shape[0], max_len,
+                                  K, _p(idx), _p(cnt), stream)
     assert rc == 0, L.idx_last_error()
     return idx, cnt
 
@@ -79,7 +79,7 @@ def test_noalloc_rejects_calls_beyond_its_scratch(L):
     idx = torch.empty((T, 2048), dtype=torch.int32, device="cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rc = L.idx_score_topk_noalloc(_p(d["q"]), _p(d["k"]), _p(d["w"]), _p(d["q_pos"]),
-                                  _p(d["cu_q"]), _p(d["cu_k"]), 1, T, too_long, 2048, _p(idx),
-                                  None, stream)
+                                  _p(d["cu_q"]), _p(d["cu_k"]), 1, T, d["k"].shape[0], too_long,
+                                  2048, _p(idx), None, stream)
     assert rc == 3
     assert b"32 MiB" in L.idx_last_error()
