@@ -186,8 +186,8 @@ idx_status idx_score(const uint16_t* q, const uint16_t* k, const float* w, const
     return e == cudaSuccess ? IDX_OK : cuda_fail(e, "score launch");
 }
 
-size_t idx_topk_workspace_size(int32_t /*T*/, int64_t /*max_len*/, int32_t /*topk*/) {
-    return kWsHeader;
+size_t idx_topk_workspace_size(int32_t T, int64_t max_len, int32_t /*topk*/) {
+    return kWsHeader + align_up(topk_scratch_bytes(T, max_len), 256);
 }
 
 idx_status idx_topk(const float* scores, int64_t ld, const int32_t* n_valid, int32_t T,
@@ -210,6 +210,7 @@ idx_status idx_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
     if (idx_status st = clear_status(ws, s)) return st;
     if (T == 0) return IDX_OK;
     TopkArgs a{scores, ld, n_valid, false, T, max_len, topk, idx, cnt, (DeviceStatus*)ws};
+    a.bits_scratch = topk_scratch_bytes(T, max_len) ? (uint32_t*)((char*)ws + kWsHeader) : nullptr;
     cudaError_t e = launch_topk(a, s);
     return e == cudaSuccess ? IDX_OK : cuda_fail(e, "topk launch");
 }
@@ -217,7 +218,8 @@ idx_status idx_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
 size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_len, int32_t /*topk*/) {
     if (T < 0 || max_len < 1) return kWsHeader;
     return kWsHeader + align_up(score_plan_bytes(B, T), 256) +
-           align_up((size_t)T * (size_t)staged_ld(max_len) * sizeof(float), 256);
+           align_up((size_t)T * (size_t)staged_ld(max_len) * sizeof(float), 256) +
+           align_up(topk_scratch_bytes(T, max_len), 256);
 }
 
 idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
@@ -245,6 +247,9 @@ idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
     cudaError_t e = launch_score_tc(sa, (char*)ws + kWsHeader, s);
     if (e != cudaSuccess) return cuda_fail(e, "score launch");
     TopkArgs ta{scores, ld, q_pos, true, T, max_len, topk, idx, cnt, status, cu_q, cu_k, B};
+    if (topk_scratch_bytes(T, max_len))
+        ta.bits_scratch = (uint32_t*)((char*)scores +
+                                      align_up((size_t)T * (size_t)ld * sizeof(float), 256));
     e = launch_topk(ta, s);
     return e == cudaSuccess ? IDX_OK : cuda_fail(e, "topk launch");
 }

@@ -73,8 +73,13 @@ struct TopkArgs {
     const int32_t* cu_q = nullptr;
     const int32_t* cu_k = nullptr;
     int32_t B = 0;
+    // Global scratch for the position bitmaps of rows too long for shared
+    // memory (topk_scratch_bytes); NULL when that size is 0.
+    uint32_t* bits_scratch = nullptr;
 };
 
+// Device scratch launch_topk needs for rows of up to max_len (often 0).
+size_t topk_scratch_bytes(int32_t T, int64_t max_len);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
 }  // namespace lidx

@@ -104,6 +104,10 @@ extern "C" IDX_API idx_status idx_score_topk_noalloc(
         return noalloc_fail(IDX_ERR_WORKSPACE,
                             "T * round_up(max_len, 4) * 4 bytes exceeds the 32 MiB scratch of "
                             "idx_score_topk_noalloc; use idx_score_topk with a workspace");
+    if (topk_scratch_bytes(T, max_len) != 0)
+        return noalloc_fail(IDX_ERR_WORKSPACE,
+                            "max_len is too long for the shared-memory selection of "
+                            "idx_score_topk_noalloc; use idx_score_topk with a workspace");
     if (tc_plan_bytes(B, T) > kNoAllocPlanBytes || (int64_t)T + B > 40000)
         return noalloc_fail(IDX_ERR_WORKSPACE,
                             "T + B exceeds the 40,000 query rows and sequences that the 1 MiB plan "

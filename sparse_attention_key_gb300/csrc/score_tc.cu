@@ -209,11 +209,19 @@ struct TcCfg {
     static constexpr int TMEM_COLS = NACC * N;
     static constexpr int THREADS = (2 + EPI_WARPS) * 32;
     static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * NACC + 3) + 16;
-    static constexpr int SMEM = 1024 + Q_BYTES + STAGES * K_STAGE + BAR_BYTES;
+    // Epilogue copy of the current group: weights [GQ][32] fp32, causal length
+    // (0 = no output) and score row pointer per query.
+    static constexpr int EPI_BYTES = (GQ * 32 * 4 + GQ * 8 + GQ * 4 + 15) / 16 * 16;
+    static constexpr int EPI_THREADS = EPI_WARPS * 32;
+    // The dynamic shared-memory window starts 1024-byte aligned (the kernel has
+    // no static shared memory); the kernel checks this before using it.
+    static constexpr int SMEM = Q_BYTES + STAGES * K_STAGE + EPI_BYTES + BAR_BYTES;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(N % 16 == 0 && N >= 32 && N <= 256, "MMA N");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
-    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps cover the 4 lane quarters");
+    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8 || EPI_WARPS == 16,
+                  "epilogue warps cover the 4 TMEM lane quarters evenly");
     static_assert(NQ % (EPI_WARPS / 4) == 0, "queries split evenly over a quarter's warps");
     static_assert(QROWS % Q_BOX_ROWS == 0, "Q box");
 };
@@ -260,12 +268,20 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                 const int32_t* __restrict__ cu_k, int64_t max_len, float* __restrict__ scores,
                 int64_t ld, TcPlan plan, DeviceStatus* status) {
     using namespace ptx;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if ((smem_addr(smem_raw) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) report_error(status, IDX_ERR_UNSUPPORTED, 1024);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     uint8_t* q_smem = smem;
     uint8_t* k_smem = smem + C::Q_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(k_smem + C::STAGES * C::K_STAGE);
+    float* epi_w = reinterpret_cast<float*>(k_smem + C::STAGES * C::K_STAGE);
+    float** epi_row = reinterpret_cast<float**>(epi_w + C::GQ * 32);
+    int32_t* epi_n = reinterpret_cast<int32_t*>(epi_row + C::GQ);
+    // mbarriers: 16-byte aligned, after the epilogue area
+    uint64_t* bars = reinterpret_cast<uint64_t*>(k_smem + C::STAGES * C::K_STAGE + C::EPI_BYTES);
+    static_assert((C::Q_BYTES + C::STAGES * C::K_STAGE + C::EPI_BYTES) % 16 == 0, "barrier alignment");
     uint64_t* k_full = bars;
     uint64_t* k_empty = bars + C::STAGES;
     uint64_t* acc_full = bars + 2 * C::STAGES;
@@ -432,6 +448,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         constexpr int kSplit = C::EPI_WARPS / 4;      // warps sharing a TMEM lane quarter
         constexpr int kQpw = C::NQ / kSplit;          // queries per warp per sub-group
         const int quarter = warp & 3;
+        const int et = threadIdx.x - 64;              // 0 .. EPI_THREADS-1
         const int qoff = ((warp - 2) / 4) * kQpw;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         int acc = 0;
@@ -439,12 +456,31 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         if (beg < end) {
             StepCursor cur;
             cur.init(beg, plan, n_groups);
+            bool new_group = true;
             for (int32_t s = beg; s < end && !aborted; ++s) {
-                if (s > beg) cur.advance(s, plan);
-                const int b = cur.desc.x, q0 = cur.desc.y, nq = cur.desc.z;
-                const int64_t k0 = __ldg(cu_k + b);
-                const int64_t len_k = (int64_t)__ldg(cu_k + b + 1) - k0;
-                const int64_t key = (int64_t)cur.j * 128 + quarter * 32 + lane;
+                if (s > beg) new_group = cur.advance(s, plan);
+                if (new_group) {
+                    // copy the group's weights, causal lengths and row pointers
+                    named_bar_sync(1, C::EPI_THREADS);
+                    const int q0 = cur.desc.y, nq = cur.desc.z;
+                    for (int i = et; i < C::GQ * 32; i += C::EPI_THREADS) {
+                        const int qi = i >> 5;
+                        epi_w[i] = qi < nq ? __ldg(w + (int64_t)(q0 + qi) * 32 + (i & 31)) : 0.f;
+                    }
+                    if (et < C::GQ) {
+                        const int64_t k0 = __ldg(cu_k + cur.desc.x);
+                        const int64_t len_k = (int64_t)__ldg(cu_k + cur.desc.x + 1) - k0;
+                        int32_t ne = 0;
+                        if (et < nq) {
+                            const int64_t n = (int64_t)__ldg(q_pos + q0 + et) + 1;
+                            if (n >= 1 && n <= len_k && n <= max_len) ne = (int32_t)n;
+                        }
+                        epi_n[et] = ne;
+                        epi_row[et] = scores + (int64_t)(q0 + et) * ld;
+                    }
+                    named_bar_sync(1, C::EPI_THREADS);
+                }
+                const int32_t key = cur.j * 128 + quarter * 32 + lane;
 #pragma unroll 1
                 for (int sub = 0; sub < C::NSUB; ++sub) {
                     if (!mbar_wait(acc_full + acc, aphase, abort_flag, kWaitLimitNs)) {
@@ -468,22 +504,21 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                     }
 #pragma unroll
                     for (int qi = 0; qi < kQpw; ++qi) {
-                        const int qrow = sub * C::NQ + qoff + qi;
-                        if (qrow >= nq) continue;
-                        const int t = q0 + qrow;
-                        const int64_t n = (int64_t)__ldg(q_pos + t) + 1;
-                        if (n < 1 || n > len_k || n > max_len || key >= n) continue;
-                        const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)t * 32);
-                        float S = 0.f;
+                        const int q = sub * C::NQ + qoff + qi;
+                        if (key >= epi_n[q]) continue;
+                        const float4* w4 = reinterpret_cast<const float4*>(epi_w + q * 32);
+                        float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int h4 = 0; h4 < 8; ++h4) {
-                            const float4 ww = __ldg(w4 + h4);
-                            S = fmaf(ww.x, fmaxf(__uint_as_float(v[qi][4 * h4 + 0]), 0.f), S);
-                            S = fmaf(ww.y, fmaxf(__uint_as_float(v[qi][4 * h4 + 1]), 0.f), S);
-                            S = fmaf(ww.z, fmaxf(__uint_as_float(v[qi][4 * h4 + 2]), 0.f), S);
-                            S = fmaf(ww.w, fmaxf(__uint_as_float(v[qi][4 * h4 + 3]), 0.f), S);
+                            const float4 ww = w4[h4];
+                            const float2 r0 = make_float2(fmaxf(__uint_as_float(v[qi][4 * h4 + 0]), 0.f),
+                                                          fmaxf(__uint_as_float(v[qi][4 * h4 + 1]), 0.f));
+                            const float2 r1 = make_float2(fmaxf(__uint_as_float(v[qi][4 * h4 + 2]), 0.f),
+                                                          fmaxf(__uint_as_float(v[qi][4 * h4 + 3]), 0.f));
+                            acc2 = __ffma2_rn(make_float2(ww.x, ww.y), r0, acc2);
+                            acc2 = __ffma2_rn(make_float2(ww.z, ww.w), r1, acc2);
                         }
-                        scores[(int64_t)t * ld + key] = S;
+                        epi_row[q][key] = acc2.x + acc2.y;
                     }
                 }
             }
@@ -534,8 +569,9 @@ static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int box_
 }
 
 // Prefill: 16 queries per group as 2 MMAs of N = 256, two 256-column TMEM
-// accumulators, 2-stage key ring, 8 epilogue warps.
-using PrefillCfg = TcCfg<8, 2, 2, 2, 8>;
+// accumulators, 3-stage key ring, 16 epilogue warps (4 per TMEM lane quarter,
+// 2 queries each per MMA).
+using PrefillCfg = TcCfg<8, 2, 2, 3, 16>;
 // Decode: one query per group, N = 32, four accumulators, 6-stage key ring.
 using DecodeCfg = TcCfg<1, 1, 4, 6, 4>;
 

@@ -8,90 +8,54 @@
 // change the answer"); a history of K or fewer keys keeps every position
 // (closing paragraph).
 //
-// Per row (one 1024-thread block):
-//   1. n <= K: emit 0..n-1, pad with -1.
-//   2. Radix select of the K-th largest key over order-preserving uint32 keys of
-//      the fp32 scores (-0 folded onto +0), most significant digit first, digits
-//      of 11/11/10 bits. Each pass builds a shared-memory histogram of the
-//      elements that match the digits chosen so far; lanes of a warp that hit
-//      the same bin are merged with a match-any vote so ties cost one atomic.
-//      After the last pass the threshold tau is exact, count_above = #(key >
-//      tau) and need = K - count_above.
-//   3. Stable compaction: one ordered sweep in chunks of 4096 positions; a block
-//      scan gives each thread its offsets into the "above" list and into the tie
-//      list; ties past `need` are dropped. The sweep stops once both lists are
-//      complete.
-// Rows that fit in shared memory are read from global memory once (pass 1 runs
-// on the way in); longer rows are re-read (from L2) by each pass.
+// Scores become order-preserving uint32 keys (-0 folded onto +0). The K-th
+// largest key tau is found by most-significant-digit radix select over three
+// digits: bits 31..(32-D1), (31-D1)..10 and 9..0. One block per row:
+//
+//   pass A   histogram of the first digit; the bin b1 holding rank K (counted
+//            from the top) follows. Short rows are copied into shared memory
+//            on the way and every later pass reads that copy.
+//   pass B   (long rows) one more read of the row: positions whose first digit
+//            is above b1 are certainly kept (fewer than K of them) and get a bit
+//            in the "above" bitmap; keys and positions of bin b1 go to a shared
+//            candidate list.
+//   digits   2 and 3 are histogrammed over bin b1 only (the candidate list, or a
+//            rescan of the row if the list overflowed) -> tau, and need = the
+//            number of tau-valued keys to keep.
+//   mark     keys of bin b1 above tau get an "above" bit, keys equal to tau a
+//            "tie" bit (short rows mark every key above tau here).
+//   emit     two ordered scans of the bitmaps (n/32 words each; each thread owns
+//            a contiguous word range, a block scan of bit counts gives offsets):
+//            all above positions in increasing order, then the first `need` tie
+//            positions in increasing order.
+// The full row is read twice at most (once for short rows); everything after
+// that touches only bin b1 and the bitmaps. No block waits on another.
 #include "common.cuh"
 #include "launch.h"
 
 namespace lidx {
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kBins = 2048;                 // 11-bit digit
-constexpr int kChunk = kTopkThreads * 4;    // compaction chunk (4 positions per thread)
+namespace {
 
-struct TopkShared {
-    uint32_t hist[kBins];
-    uint32_t warp_tot[kTopkWarps];
-    uint32_t sel_bin;
-    uint32_t sel_rank;
+constexpr int kD3Bits = 10;                 // last digit: bits 9..0
+constexpr int kStagedThreads = 256;
+constexpr int kStreamThreads = 1024;
+constexpr int64_t kStageCap = 12288;        // longest row staged in shared memory
+constexpr int kCandCap = 8192;              // long rows: candidates kept in shared memory
+constexpr int kUnroll = 4;                  // independent 16-byte loads per thread in flight
+constexpr int kScratchBlocks = 512;         // blocks when the bitmaps live in global scratch
+
+template <int THREADS, int D1BITS>
+struct TopkSmem {
+    static constexpr int kWarps = THREADS / 32;
+    uint32_t hist[1 << D1BITS];
+    uint32_t scan[THREADS / 32 + 1];
+    uint32_t sel_bin, sel_rank, cand_count;
 };
 
-// Add the elements of `u` that match (prefix, mask) into hist[(u >> shift) & (bins-1)].
-// All 32 lanes of the warp must call this together.
-__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t u, bool valid, uint32_t prefix,
-                                         uint32_t mask, int shift, uint32_t bin_mask) {
-    const bool match = valid && ((u & mask) == prefix);
-    const uint32_t bin = match ? ((u >> shift) & bin_mask) : 0xFFFFFFFFu;
-    if (__any_sync(0xffffffffu, match)) {
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        const int lane = threadIdx.x & 31;
-        if (match && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], __popc(peers));
-    }
-}
-
-// Warp 0 finds the bin (scanning from the top) holding the rank-`rank` element
-// (1-based from the largest). Writes sel_bin and the rank inside that bin.
-__device__ __forceinline__ void find_bin(TopkShared& sh, int nbins, uint32_t rank) {
-    if (threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
-    const int per = nbins / 32;               // bins per lane, lane 0 owns the top ones
-    const int top = nbins - 1 - lane * per;   // this lane's highest bin
-    uint32_t sum = 0;
-    for (int i = 0; i < per; ++i) sum += sh.hist[top - i];
-    // exclusive prefix over lanes (lane 0 first = largest bins)
-    uint32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    const uint32_t excl = incl - sum;
-    if (excl < rank && rank <= incl) {        // exactly one lane
-        uint32_t acc = excl;
-        for (int i = 0; i < per; ++i) {
-            const uint32_t c = sh.hist[top - i];
-            if (acc + c >= rank) {
-                sh.sel_bin = (uint32_t)(top - i);
-                sh.sel_rank = rank - acc;
-                break;
-            }
-            acc += c;
-        }
-    }
-}
-
-__device__ __forceinline__ void zero_hist(TopkShared& sh) {
-    for (int i = threadIdx.x; i < kBins; i += kTopkThreads) sh.hist[i] = 0;
-}
-
-// Exclusive block scan of one packed counter per thread; returns the exclusive
-// prefix and writes the block total to *total.
-__device__ __forceinline__ uint32_t block_exclusive_scan(TopkShared& sh, uint32_t v,
-                                                         uint32_t* total) {
+// Exclusive block scan of one value per thread (sh.scan as scratch).
+template <int THREADS, class S>
+__device__ __forceinline__ uint32_t block_excl_scan(S& sh, uint32_t v) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t incl = v;
 #pragma unroll
@@ -99,39 +63,128 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(TopkShared& sh, uint32_
         const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += x;
     }
-    if (lane == 31) sh.warp_tot[warp] = incl;
+    __syncthreads();   // sh.scan may still be read after a previous scan
+    if (lane == 31) sh.scan[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const uint32_t wt = sh.warp_tot[lane];
-        uint32_t wi = wt;
+        const uint32_t x0 = lane < S::kWarps ? sh.scan[lane] : 0u;
+        uint32_t wi = x0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t x = __shfl_up_sync(0xffffffffu, wi, o);
             if (lane >= o) wi += x;
         }
-        sh.warp_tot[lane] = wi - wt;  // exclusive warp offsets
-        if (lane == 31) sh.sel_rank = wi;  // reuse as the block total
+        if (lane < S::kWarps) sh.scan[lane] = wi - x0;
     }
     __syncthreads();
-    const uint32_t res = sh.warp_tot[warp] + incl - v;
-    *total = sh.sel_rank;
-    __syncthreads();  // warp_tot / sel_rank are reused by the next call
-    return res;
+    return sh.scan[warp] + incl - v;
 }
 
-template <bool kRowInSmem>
-__global__ void __launch_bounds__(kTopkThreads)
+// The bin (counting from the highest) holding the element of rank `rank`
+// (1-based from the largest) in hist[0..nbins); writes sh.sel_bin and the rank
+// inside that bin to sh.sel_rank.
+template <int THREADS, class S>
+__device__ __forceinline__ void select_bin(S& sh, int nbins, uint32_t rank) {
+    const int per = (nbins + THREADS - 1) / THREADS;       // bins per thread
+    const int hi = nbins - 1 - (int)threadIdx.x * per;     // this thread's highest bin
+    uint32_t sum = 0;
+    for (int i = 0; i < per; ++i)
+        if (hi - i >= 0) sum += sh.hist[hi - i];
+    const uint32_t excl = block_excl_scan<THREADS>(sh, sum);
+    if (excl < rank && rank <= excl + sum) {   // exactly one thread
+        uint32_t acc = excl;
+        for (int i = 0; i < per; ++i) {
+            const uint32_t c = sh.hist[hi - i];
+            if (acc + c >= rank) {
+                sh.sel_bin = (uint32_t)(hi - i);
+                sh.sel_rank = rank - acc;
+                break;
+            }
+            acc += c;
+        }
+    }
+    __syncthreads();
+}
+
+template <int THREADS>
+__device__ __forceinline__ void zero(uint32_t* p, int64_t n) {
+    for (int64_t i = threadIdx.x; i < n; i += THREADS) p[i] = 0;
+}
+
+// Order-preserving key of a score: a > b (numerically) iff fkey(a) > fkey(b).
+// Adding +0 turns -0 into +0 first, so the two zeros share one key.
+__device__ __forceinline__ uint32_t fkey(float x) {
+    const uint32_t u = __float_as_uint(__fadd_rn(x, 0.0f));
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+
+// Keys of the 4 scores of vector v (elements 4v..4v+3) of a row, from global.
+__device__ __forceinline__ uint4 gkeys(const float* row, int32_t v) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(row) + v);
+    return make_uint4(fkey(x.x), fkey(x.y), fkey(x.z), fkey(x.w));
+}
+
+// Keys of vector v, from the staged copy or from global.
+template <bool STAGED>
+__device__ __forceinline__ uint4 vkeys(const float* row, const uint32_t* staged, int32_t v) {
+    if (STAGED) return reinterpret_cast<const uint4*>(staged)[v];
+    return gkeys(row, v);
+}
+
+__device__ __forceinline__ uint32_t comp(const uint4& k, int j) {
+    return j == 0 ? k.x : j == 1 ? k.y : j == 2 ? k.z : k.w;
+}
+
+__device__ __forceinline__ void set_bit(uint32_t* bits, int64_t pos) {
+    atomicOr(bits + (pos >> 5), 1u << (pos & 31));
+}
+
+// Write the positions of the set bits of bits[0..nw) in increasing order to
+// out[0..limit) (set bits past the first `limit` are dropped).
+template <int THREADS, class S>
+__device__ __forceinline__ void emit_ordered(S& sh, const uint32_t* bits, int64_t nw, int32_t* out,
+                                             uint32_t limit) {
+    const int64_t per = (nw + THREADS - 1) / THREADS;
+    const int64_t w0 = threadIdx.x * per;
+    const int64_t w1 = w0 + per < nw ? w0 + per : nw;
+    uint32_t c = 0;
+    for (int64_t w = w0; w < w1; ++w) c += __popc(bits[w]);
+    uint32_t pos = block_excl_scan<THREADS>(sh, c);
+    for (int64_t w = w0; w < w1 && pos < limit; ++w) {
+        uint32_t m = bits[w];
+        while (m && pos < limit) {
+            const int b = __ffs(m) - 1;
+            out[pos++] = (int32_t)(w * 32 + b);
+            m &= m - 1u;
+        }
+    }
+}
+
+template <int THREADS, int D1BITS, bool STAGED>
+__global__ void __launch_bounds__(THREADS, STAGED ? 4 : 1)
 topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
             bool n_from_pos, int T, int64_t max_len, int K, int32_t* __restrict__ idx,
             int32_t* __restrict__ cnt, DeviceStatus* status, const int32_t* __restrict__ cu_q,
-            const int32_t* __restrict__ cu_k, int B) {
-    __shared__ TopkShared sh;
-    extern __shared__ __align__(16) uint32_t row_keys[];  // used when kRowInSmem
+            const int32_t* __restrict__ cu_k, int B, int64_t stage_cap, int64_t nw_cap,
+            int cand_cap, uint32_t* __restrict__ gbits) {
+    using S = TopkSmem<THREADS, D1BITS>;
+    constexpr int kD1Shift = 32 - D1BITS;
+    constexpr int kD2Bits = 22 - D1BITS;        // bits (31-D1)..10
+    static_assert(kD2Bits <= D1BITS, "histogram holds the second digit");
+    __shared__ S sh;
+    // dynamic: [staged row: stage_cap][bitmaps: 2*nw_cap, unless global][cand keys][cand pos]
+    extern __shared__ __align__(16) uint32_t dyn[];
+    uint32_t* staged = dyn;
+    uint32_t* bits_sm = dyn + (STAGED ? stage_cap : 0);
+    uint32_t* above_bits = gbits ? gbits + (int64_t)blockIdx.x * 2 * nw_cap : bits_sm;
+    uint32_t* tie_bits = above_bits + nw_cap;
+    uint32_t* cand_key = bits_sm + (gbits ? 0 : 2 * nw_cap);
+    int32_t* cand_pos = reinterpret_cast<int32_t*>(cand_key + cand_cap);
 
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        int64_t n = (int64_t)__ldg(n_valid + t) + (n_from_pos ? 1 : 0);
+        const int64_t n64 = (int64_t)__ldg(n_valid + t) + (n_from_pos ? 1 : 0);
         int32_t* out = idx + (int64_t)t * K;
-        bool bad = n < 0 || n > max_len || n > ld;
+        bool bad = n64 < 0 || n64 > max_len || n64 > ld;
         if (cu_q != nullptr) {  // fused call: the row must lie inside its sequence
             int lo = 0, hi = B - 1;
             while (lo < hi) {
@@ -139,170 +192,210 @@ topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restr
                 if (__ldg(cu_q + mid) <= t) lo = mid; else hi = mid - 1;
             }
             const int64_t len_k = (int64_t)__ldg(cu_k + lo + 1) - __ldg(cu_k + lo);
-            bad = bad || n < 1 || n > len_k;
+            bad = bad || n64 < 1 || n64 > len_k;
         }
         if (bad) {
             if (threadIdx.x == 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
-            for (int i = threadIdx.x; i < K; i += kTopkThreads) out[i] = -1;
+            for (int i = threadIdx.x; i < K; i += THREADS) out[i] = -1;
             if (cnt && threadIdx.x == 0) cnt[t] = 0;
             continue;
         }
-        if (n <= K) {  // dormant selection
-            for (int i = threadIdx.x; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
-            if (cnt && threadIdx.x == 0) cnt[t] = (int32_t)n;
+        if (n64 <= K) {  // dormant selection: every position
+            for (int i = threadIdx.x; i < K; i += THREADS) out[i] = i < n64 ? i : -1;
+            if (cnt && threadIdx.x == 0) cnt[t] = (int32_t)n64;
             continue;
         }
+        const int32_t n = (int32_t)n64;           // max_len < 2^31
+        const int32_t nvec = n >> 2;              // full 4-element vectors
+        const int32_t tail0 = nvec << 2;          // first element of the (< 4) tail
         const float* row = scores + (int64_t)t * ld;
-        const float4* row4 = reinterpret_cast<const float4*>(row);
+        const int32_t nw = (n + 31) >> 5;
 
-        // ---- pass 1: top 11 bits (fused with the staging copy when the row fits)
+        // ---- pass A: first digit (short rows: staged on the way)
         __syncthreads();
-        zero_hist(sh);
+        zero<THREADS>(sh.hist, 1 << D1BITS);
+        zero<THREADS>(above_bits, nw);
+        zero<THREADS>(tie_bits, nw);
+        if (threadIdx.x == 0) sh.cand_count = 0;
         __syncthreads();
-        for (int64_t base = 0; base < n; base += kChunk) {
-            const int64_t i = base + 4 * threadIdx.x;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i + 3 < n) v = __ldg(row4 + (i >> 2));
-            else if (i < n) {
-                v.x = row[i];
-                if (i + 1 < n) v.y = row[i + 1];
-                if (i + 2 < n) v.z = row[i + 2];
-            }
-            const uint32_t u[4] = {score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w)};
-            if (kRowInSmem && i < n) {
-                if (i + 3 < n) *reinterpret_cast<uint4*>(row_keys + i) = make_uint4(u[0], u[1], u[2], u[3]);
-                else for (int j = 0; j < 4 && i + j < n; ++j) row_keys[i + j] = u[j];
-            }
+        for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += kUnroll * THREADS) {
+            uint4 k[kUnroll];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) hist_add(sh.hist, u[j], i + j < n, 0u, 0u, 21, kBins - 1);
+            for (int u = 0; u < kUnroll; ++u)   // all loads first
+                if (v0 + u * THREADS < nvec) k[u] = gkeys(row, v0 + u * THREADS);
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (v0 + u * THREADS >= nvec) break;
+                if (STAGED) reinterpret_cast<uint4*>(staged)[v0 + u * THREADS] = k[u];
+                atomicAdd(&sh.hist[k[u].x >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[k[u].y >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[k[u].z >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[k[u].w >> kD1Shift], 1u);
+            }
+        }
+        if (threadIdx.x < n - tail0) {
+            const uint32_t kk = fkey(__ldg(row + tail0 + threadIdx.x));
+            if (STAGED) staged[tail0 + threadIdx.x] = kk;
+            atomicAdd(&sh.hist[kk >> kD1Shift], 1u);
         }
         __syncthreads();
-        find_bin(sh, kBins, (uint32_t)K);
-        __syncthreads();
-        uint32_t prefix = sh.sel_bin << 21;
-        uint32_t mask = 0xFFE00000u;
+        select_bin<THREADS>(sh, 1 << D1BITS, (uint32_t)K);
+        const uint32_t b1 = sh.sel_bin;
         uint32_t rank = sh.sel_rank;
+        uint32_t prefix = b1 << kD1Shift;
 
-        // ---- passes 2 and 3: bits 20..10, then 9..0, among matching elements
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-            const int shift = pass == 0 ? 10 : 0;
-            const int nbins = pass == 0 ? 2048 : 1024;
-            __syncthreads();
-            zero_hist(sh);
-            __syncthreads();
-            for (int64_t base = 0; base < n; base += kChunk) {
-                const int64_t i = base + 4 * threadIdx.x;
-                uint32_t u[4] = {0u, 0u, 0u, 0u};
-                if (kRowInSmem) {
-                    if (i + 3 < n) {
-                        const uint4 x = *reinterpret_cast<const uint4*>(row_keys + i);
-                        u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
-                    } else {
-                        for (int j = 0; j < 4; ++j) if (i + j < n) u[j] = row_keys[i + j];
+        // ---- pass B (long rows): certain positions -> bits, bin b1 -> candidates
+        bool use_cand = false;
+        if (!STAGED) {
+            auto visit = [&](uint32_t kk, int32_t pos) {
+                const uint32_t d = kk >> kD1Shift;
+                if (d > b1) {
+                    set_bit(above_bits, pos);
+                } else if (d == b1) {
+                    const uint32_t slot = atomicAdd(&sh.cand_count, 1u);
+                    if (slot < (uint32_t)cand_cap) {
+                        cand_key[slot] = kk;
+                        cand_pos[slot] = pos;
                     }
-                } else {
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (i + 3 < n) v = __ldg(row4 + (i >> 2));
-                    else if (i < n) {
-                        v.x = row[i];
-                        if (i + 1 < n) v.y = row[i + 1];
-                        if (i + 2 < n) v.z = row[i + 2];
-                    }
-                    u[0] = score_key(v.x); u[1] = score_key(v.y);
-                    u[2] = score_key(v.z); u[3] = score_key(v.w);
                 }
+            };
+            for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += kUnroll * THREADS) {
+                uint4 k[kUnroll];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    hist_add(sh.hist, u[j], i + j < n, prefix, mask, shift, (uint32_t)nbins - 1);
+                for (int u = 0; u < kUnroll; ++u)
+                    if (v0 + u * THREADS < nvec) k[u] = gkeys(row, v0 + u * THREADS);
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int32_t v = v0 + u * THREADS;
+                    if (v >= nvec) break;
+                    // one test per vector: most vectors hold nothing >= b1
+                    const uint32_t mx = max(max(k[u].x, k[u].y), max(k[u].z, k[u].w));
+                    if ((mx >> kD1Shift) < b1) continue;
+                    visit(k[u].x, 4 * v);
+                    visit(k[u].y, 4 * v + 1);
+                    visit(k[u].z, 4 * v + 2);
+                    visit(k[u].w, 4 * v + 3);
+                }
+            }
+            if (threadIdx.x < n - tail0)
+                visit(fkey(__ldg(row + tail0 + threadIdx.x)), tail0 + threadIdx.x);
+            __syncthreads();
+            use_cand = sh.cand_count <= (uint32_t)cand_cap;
+        }
+        const int n_cand = use_cand ? (int)sh.cand_count : 0;
+
+        // ---- digits 2 and 3 among keys that match the digits chosen so far
+#pragma unroll 1
+        for (int d = 0; d < 2; ++d) {
+            const int shift = d == 0 ? kD3Bits : 0;
+            const int bits = d == 0 ? kD2Bits : kD3Bits;
+            const uint32_t mask_hi = d == 0 ? (0xFFFFFFFFu << kD1Shift) : (0xFFFFFFFFu << kD3Bits);
+            const uint32_t bin_mask = (1u << bits) - 1u;
+            __syncthreads();
+            zero<THREADS>(sh.hist, 1 << bits);
+            __syncthreads();
+            auto add = [&](uint32_t kk) {
+                if ((kk & mask_hi) == prefix) atomicAdd(&sh.hist[(kk >> shift) & bin_mask], 1u);
+            };
+            if (use_cand) {
+                for (int i = threadIdx.x; i < n_cand; i += THREADS) add(cand_key[i]);
+            } else {
+                for (int32_t v = threadIdx.x; v < nvec; v += THREADS) {
+                    const uint4 k = vkeys<STAGED>(row, staged, v);
+                    add(k.x); add(k.y); add(k.z); add(k.w);
+                }
+                if (threadIdx.x < n - tail0)
+                    add(STAGED ? staged[tail0 + threadIdx.x] : fkey(__ldg(row + tail0 + threadIdx.x)));
             }
             __syncthreads();
-            find_bin(sh, nbins, rank);
-            __syncthreads();
+            select_bin<THREADS>(sh, 1 << bits, rank);
             prefix |= sh.sel_bin << shift;
-            mask |= (uint32_t)(nbins - 1) << shift;
             rank = sh.sel_rank;
         }
         const uint32_t tau = prefix;
-        const uint32_t need = rank;                     // members of the tie group to keep
-        const uint32_t n_above = (uint32_t)K - need;    // every key > tau is kept
+        const uint32_t need = rank;                   // members of the tie group kept
+        const uint32_t n_above = (uint32_t)K - need;  // every key > tau is kept
 
-        // ---- stable compaction in position order
-        uint32_t done_above = 0, done_tie = 0;
-        for (int64_t base = 0; base < n; base += kChunk) {
-            const int64_t i = base + 4 * threadIdx.x;
-            uint32_t u[4] = {0u, 0u, 0u, 0u};
-            if (kRowInSmem) {
-                if (i + 3 < n) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(row_keys + i);
-                    u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
-                } else {
-                    for (int j = 0; j < 4; ++j) if (i + j < n) u[j] = row_keys[i + j];
-                }
-            } else {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i + 3 < n) v = __ldg(row4 + (i >> 2));
-                else if (i < n) {
-                    v.x = row[i];
-                    if (i + 1 < n) v.y = row[i + 1];
-                    if (i + 2 < n) v.z = row[i + 2];
-                }
-                u[0] = score_key(v.x); u[1] = score_key(v.y);
-                u[2] = score_key(v.z); u[3] = score_key(v.w);
+        // ---- mark keys above / equal to tau not marked yet
+        if (use_cand) {
+            for (int i = threadIdx.x; i < n_cand; i += THREADS) {
+                const uint32_t kk = cand_key[i];
+                if (kk > tau) set_bit(above_bits, cand_pos[i]);
+                else if (kk == tau) set_bit(tie_bits, cand_pos[i]);
             }
-            uint32_t a = 0, e = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool ok = i + j < n;
-                a += (ok && u[j] > tau) ? 1u : 0u;
-                e += (ok && u[j] == tau) ? 1u : 0u;
-            }
-            uint32_t total;
-            const uint32_t off = block_exclusive_scan(sh, a | (e << 16), &total);
-            uint32_t pa = done_above + (off & 0xFFFFu);
-            uint32_t pe = done_tie + (off >> 16);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool ok = i + j < n;
-                if (ok && u[j] > tau) out[pa++] = (int32_t)(i + j);
-                else if (ok && u[j] == tau) {
-                    if (pe < need) out[n_above + pe] = (int32_t)(i + j);
-                    ++pe;
+        } else {
+            // staged rows never ran pass B, so every key above tau is marked here;
+            // streamed rows marked first digits above b1 in pass B already
+            auto mark = [&](uint32_t kk, int32_t pos) {
+                if (kk > tau) {
+                    if (STAGED || (kk >> kD1Shift) == b1) set_bit(above_bits, pos);
+                } else if (kk == tau) {
+                    set_bit(tie_bits, pos);
                 }
+            };
+            for (int32_t v = threadIdx.x; v < nvec; v += THREADS) {
+                const uint4 k = vkeys<STAGED>(row, staged, v);
+                const uint32_t mx = max(max(k.x, k.y), max(k.z, k.w));
+                if (mx < tau) continue;
+                mark(k.x, 4 * v); mark(k.y, 4 * v + 1); mark(k.z, 4 * v + 2); mark(k.w, 4 * v + 3);
             }
-            done_above += total & 0xFFFFu;
-            done_tie += total >> 16;
-            if (done_above >= n_above && done_tie >= need) break;  // block-uniform
+            if (threadIdx.x < n - tail0)
+                mark(STAGED ? staged[tail0 + threadIdx.x] : fkey(__ldg(row + tail0 + threadIdx.x)),
+                     tail0 + threadIdx.x);
         }
+        __syncthreads();
+
+        // ---- emit: above positions ascending, then the first `need` ties ascending
+        emit_ordered<THREADS>(sh, above_bits, nw, out, n_above);
+        emit_ordered<THREADS>(sh, tie_bits, nw, out + n_above, need);
         if (cnt && threadIdx.x == 0) cnt[t] = K;
     }
 }
 
-// Largest row (in elements) staged in shared memory.
-static int64_t smem_row_cap(const DeviceInfo& dev) {
-    const int64_t avail = (int64_t)dev.max_smem_optin - (int64_t)sizeof(TopkShared) - 1024;
-    return avail > 0 ? avail / 4 : 0;
+constexpr size_t kStreamStatic = sizeof(TopkSmem<kStreamThreads, 12>);
+
+// Shared memory a block may use in total (GB300 opt-in limit, 227 KB).
+constexpr int64_t kBlockSmem = 227 * 1024;
+
+bool bitmaps_fit_in_smem(int64_t row_cap) {
+    const int64_t nw_cap = (row_cap + 31) / 32;
+    return (int64_t)kCandCap * 8 + 2 * nw_cap * 4 + (int64_t)kStreamStatic <= kBlockSmem;
+}
+
+}  // namespace
+
+size_t topk_scratch_bytes(int32_t T, int64_t max_len) {
+    if (T <= 0 || max_len <= kStageCap || bitmaps_fit_in_smem(max_len)) return 0;
+    return (size_t)kScratchBlocks * 2 * (size_t)((max_len + 31) / 32) * 4;
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
-    const DeviceInfo& dev = device_info();
+    if (a.T <= 0) return cudaSuccess;
     const int64_t row_cap = a.max_len < a.ld ? a.max_len : a.ld;
-    const int64_t padded = align_up((size_t)row_cap, 4);
-    const int grid = a.T < dev.sm_count * 64 ? a.T : dev.sm_count * 64;
-    if (grid <= 0) return cudaSuccess;
-    if (padded <= smem_row_cap(dev)) {
-        const size_t smem = (size_t)padded * 4;
-        cudaError_t e = ensure_smem_optin((const void*)topk_kernel<true>, smem_row_cap(dev) * 4);
+    const int64_t nw_cap = (row_cap + 31) / 32;
+    const int grid = a.T < 65535 ? a.T : 65535;
+    if (row_cap <= kStageCap) {
+        const int64_t stage = (int64_t)align_up((size_t)row_cap, 4);
+        const size_t smem = (size_t)(stage + 2 * nw_cap) * 4;
+        auto kern = topk_kernel<kStagedThreads, 11, true>;
+        cudaError_t e = ensure_smem_optin(
+            (const void*)kern, (kStageCap + 2 * ((kStageCap + 31) / 32)) * 4);
         if (e != cudaSuccess) return e;
-        topk_kernel<true><<<grid, kTopkThreads, smem, stream>>>(a.scores, a.ld, a.n_valid,
-                                                                a.n_from_pos, a.T, a.max_len,
-                                                                a.topk, a.idx, a.cnt, a.status,
-                                                                a.cu_q, a.cu_k, a.B);
+        kern<<<grid, kStagedThreads, smem, stream>>>(a.scores, a.ld, a.n_valid, a.n_from_pos, a.T,
+                                                     a.max_len, a.topk, a.idx, a.cnt, a.status,
+                                                     a.cu_q, a.cu_k, a.B, stage, nw_cap, 0, nullptr);
     } else {
-        topk_kernel<false><<<grid, kTopkThreads, 0, stream>>>(a.scores, a.ld, a.n_valid,
-                                                              a.n_from_pos, a.T, a.max_len,
-                                                              a.topk, a.idx, a.cnt, a.status,
-                                                                a.cu_q, a.cu_k, a.B);
+        const bool in_smem = bitmaps_fit_in_smem(row_cap);
+        if (!in_smem && a.bits_scratch == nullptr) return cudaErrorInvalidValue;
+        const size_t smem = (size_t)kCandCap * 8 + (in_smem ? (size_t)(2 * nw_cap * 4) : 0);
+        const int g = in_smem ? grid : (grid < kScratchBlocks ? grid : kScratchBlocks);
+        auto kern = topk_kernel<kStreamThreads, 12, false>;
+        cudaError_t e = ensure_smem_optin((const void*)kern, kBlockSmem - (int64_t)kStreamStatic);
+        if (e != cudaSuccess) return e;
+        kern<<<g, kStreamThreads, smem, stream>>>(a.scores, a.ld, a.n_valid, a.n_from_pos, a.T,
+                                                  a.max_len, a.topk, a.idx, a.cnt, a.status,
+                                                  a.cu_q, a.cu_k, a.B, 0, nw_cap, kCandCap,
+                                                  in_smem ? nullptr : a.bits_scratch);
     }
     count_launch();
     return cudaGetLastError();

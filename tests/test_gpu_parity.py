@@ -157,8 +157,10 @@ def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
     if lens == "short":
         n_valid = np.concatenate([[0, 1, K - 1 if K > 1 else 0, K, K + 1, 2047, 2048, 2049, 4096],
                                   rng.integers(1, 20000, size=20), [50_000]]).astype(np.int32)
-    else:   # beyond the shared-memory row cap: the multi-pass global path
+    else:   # longer than the shared-memory staging cap; one row needs global bitmaps
         n_valid = np.array([70_000, 131_072, 65_537, K + 3, 100_001], np.int32)
+        if kind in ("normal", "ties"):
+            n_valid = np.append(n_valid, np.int32(700_001))
     max_len = int(n_valid.max())
     ld = (max_len + 3) // 4 * 4
     S = wl.score_rows(int(rng.integers(1 << 30)), n_valid.size, n_valid, ld, kind=kind)
