@@ -59,6 +59,25 @@ const DeviceInfo& device_info() {
     return infos[dev];
 }
 
+// Static shared memory of a kernel (as compiled), cached per kernel.
+int64_t kernel_static_smem(const void* kernel) {
+    static std::mutex mu;
+    static const void* keys[256];
+    static int64_t vals[256];
+    static int n = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (keys[i] == kernel) return vals[i];
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return -1;
+    if (n < 256) {
+        keys[n] = kernel;
+        vals[n] = (int64_t)attr.sharedSizeBytes;
+        ++n;
+    }
+    return (int64_t)attr.sharedSizeBytes;
+}
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device).
 cudaError_t ensure_smem_optin(const void* kernel, int64_t bytes) {
     static std::mutex mu;

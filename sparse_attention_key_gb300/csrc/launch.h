@@ -28,6 +28,9 @@ const DeviceInfo& device_info();
 // Raise `kernel`'s dynamic shared-memory limit to `bytes` once per device.
 cudaError_t ensure_smem_optin(const void* kernel, int64_t bytes);
 
+// Static shared memory of `kernel` as compiled (bytes), or -1.
+int64_t kernel_static_smem(const void* kernel);
+
 cudaError_t launch_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
                                  bool f32_params, float eps, uint16_t* k_out, int64_t n_rows,
                                  cudaStream_t stream);

@@ -10,26 +10,27 @@
 //
 // Scores become order-preserving uint32 keys (-0 folded onto +0). The K-th
 // largest key tau is found by most-significant-digit radix select over three
-// digits: bits 31..(32-D1), (31-D1)..10 and 9..0. One block per row:
+// digits: bits 31..(32-D1), (31-D1)..10 and 9..0. One block per row, with the
+// row's positions tracked in bitmaps (one bit per position):
 //
 //   pass A   histogram of the first digit; the bin b1 holding rank K (counted
-//            from the top) follows. Short rows are copied into shared memory
-//            on the way and every later pass reads that copy.
-//   pass B   (long rows) one more read of the row: positions whose first digit
-//            is above b1 are certainly kept (fewer than K of them) and get a bit
-//            in the "above" bitmap; keys and positions of bin b1 go to a shared
-//            candidate list.
-//   digits   2 and 3 are histogrammed over bin b1 only (the candidate list, or a
-//            rescan of the row if the list overflowed) -> tau, and need = the
-//            number of tau-valued keys to keep.
-//   mark     keys of bin b1 above tau get an "above" bit, keys equal to tau a
-//            "tie" bit (short rows mark every key above tau here).
-//   emit     two ordered scans of the bitmaps (n/32 words each; each thread owns
-//            a contiguous word range, a block scan of bit counts gives offsets):
-//            all above positions in increasing order, then the first `need` tie
-//            positions in increasing order.
-// The full row is read twice at most (once for short rows); everything after
-// that touches only bin b1 and the bitmaps. No block waits on another.
+//            from the top) follows.
+//   split    positions whose first digit is above b1 are certainly kept (fewer
+//            than K of them) -> "above" bits; positions in bin b1 are the
+//            candidates -> "cand" bits (set as 4-bit masks, one per thread and
+//            4-position vector).
+//   digits   2 and 3 are histogrammed over the candidates only -> tau, and
+//            need = the number of tau-valued keys kept.
+//   mark     candidates above tau join the "above" bits, candidates equal to
+//            tau get "tie" bits.
+//   emit     one ordered scan of the bitmaps (each thread owns a contiguous word
+//            range; a block scan of packed bit counts gives offsets): all above
+//            positions in increasing order, then the first `need` tie positions
+//            in increasing order.
+// Short rows (staged kernel) are copied into shared memory as keys during pass
+// A; every later step reads that copy. Long rows (streamed kernel) are read
+// twice from global memory (pass A and the split); the candidates' keys are
+// gathered from global memory again where needed. No block waits on another.
 #include "common.cuh"
 #include "launch.h"
 
@@ -39,9 +40,8 @@ namespace {
 
 constexpr int kD3Bits = 10;                 // last digit: bits 9..0
 constexpr int kStagedThreads = 256;
-constexpr int kStreamThreads = 1024;
+constexpr int kStreamThreads = 512;         // two blocks per SM overlap their phases
 constexpr int64_t kStageCap = 12288;        // longest row staged in shared memory
-constexpr int kCandCap = 8192;              // long rows: candidates kept in shared memory
 constexpr int kUnroll = 4;                  // independent 16-byte loads per thread in flight
 constexpr int kScratchBlocks = 512;         // blocks when the bitmaps live in global scratch
 
@@ -50,6 +50,7 @@ struct TopkSmem {
     static constexpr int kWarps = THREADS / 32;
     uint32_t hist[1 << D1BITS];
     uint32_t scan[THREADS / 32 + 1];
+    uint64_t scan64[THREADS / 32];
     uint32_t sel_bin, sel_rank, cand_count;
 };
 
@@ -78,6 +79,33 @@ __device__ __forceinline__ uint32_t block_excl_scan(S& sh, uint32_t v) {
     }
     __syncthreads();
     return sh.scan[warp] + incl - v;
+}
+
+// Exclusive block scan of one 64-bit value per thread (sh.scan64 as scratch).
+template <int THREADS, class S>
+__device__ __forceinline__ uint64_t block_excl_scan64(S& sh, uint64_t v) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    __syncthreads();
+    if (lane == 31) sh.scan64[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint64_t x0 = lane < S::kWarps ? sh.scan64[lane] : 0ull;
+        uint64_t wi = x0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t x = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += x;
+        }
+        if (lane < S::kWarps) sh.scan64[lane] = wi - x0;
+    }
+    __syncthreads();
+    return sh.scan64[warp] + incl - v;
 }
 
 // The bin (counting from the highest) holding the element of rank `rank`
@@ -124,13 +152,6 @@ __device__ __forceinline__ uint4 gkeys(const float* row, int32_t v) {
     return make_uint4(fkey(x.x), fkey(x.y), fkey(x.z), fkey(x.w));
 }
 
-// Keys of vector v, from the staged copy or from global.
-template <bool STAGED>
-__device__ __forceinline__ uint4 vkeys(const float* row, const uint32_t* staged, int32_t v) {
-    if (STAGED) return reinterpret_cast<const uint4*>(staged)[v];
-    return gkeys(row, v);
-}
-
 __device__ __forceinline__ uint32_t comp(const uint4& k, int j) {
     return j == 0 ? k.x : j == 1 ? k.y : j == 2 ? k.z : k.w;
 }
@@ -139,94 +160,122 @@ __device__ __forceinline__ void set_bit(uint32_t* bits, int64_t pos) {
     atomicOr(bits + (pos >> 5), 1u << (pos & 31));
 }
 
-// Write the positions of the set bits of bits[0..nw) in increasing order to
-// out[0..limit) (set bits past the first `limit` are dropped).
+// Ordered output from the two bitmaps: the set positions of `above` in
+// increasing order to out[0..n_above), then the first `need` set positions of
+// `tie` in increasing order to out[n_above..). Each thread owns a contiguous
+// range of words; one block scan of packed (above, tie) counts gives offsets.
 template <int THREADS, class S>
-__device__ __forceinline__ void emit_ordered(S& sh, const uint32_t* bits, int64_t nw, int32_t* out,
-                                             uint32_t limit) {
-    const int64_t per = (nw + THREADS - 1) / THREADS;
-    const int64_t w0 = threadIdx.x * per;
-    const int64_t w1 = w0 + per < nw ? w0 + per : nw;
-    uint32_t c = 0;
-    for (int64_t w = w0; w < w1; ++w) c += __popc(bits[w]);
-    uint32_t pos = block_excl_scan<THREADS>(sh, c);
-    for (int64_t w = w0; w < w1 && pos < limit; ++w) {
-        uint32_t m = bits[w];
-        while (m && pos < limit) {
-            const int b = __ffs(m) - 1;
-            out[pos++] = (int32_t)(w * 32 + b);
+__device__ __forceinline__ void emit_ordered(S& sh, const uint32_t* above, const uint32_t* tie,
+                                             int32_t nw, int32_t* out, uint32_t n_above,
+                                             uint32_t need) {
+    const int32_t per = (nw + THREADS - 1) / THREADS;
+    const int32_t w0 = threadIdx.x * per;
+    const int32_t w1 = w0 + per < nw ? w0 + per : nw;
+    uint32_t ca = 0, ct = 0;
+    for (int32_t w = w0; w < w1; ++w) {
+        ca += __popc(above[w]);
+        ct += __popc(tie[w]);
+    }
+    ct = ct < need ? ct : need;   // ties past `need` are never emitted
+    const uint64_t off = block_excl_scan64<THREADS>(sh, (uint64_t)ca | ((uint64_t)ct << 32));
+    uint32_t pa = (uint32_t)off, pt = (uint32_t)(off >> 32);
+    for (int32_t w = w0; w < w1; ++w) {
+        uint32_t m = above[w];
+        while (m) {
+            out[pa++] = w * 32 + (__ffs(m) - 1);
+            m &= m - 1u;
+        }
+        m = tie[w];
+        while (m && pt < need) {
+            out[n_above + pt++] = w * 32 + (__ffs(m) - 1);
             m &= m - 1u;
         }
     }
 }
 
-template <int THREADS, int D1BITS, bool STAGED>
-__global__ void __launch_bounds__(THREADS, STAGED ? 4 : 1)
-topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
-            bool n_from_pos, int T, int64_t max_len, int K, int32_t* __restrict__ idx,
-            int32_t* __restrict__ cnt, DeviceStatus* status, const int32_t* __restrict__ cu_q,
-            const int32_t* __restrict__ cu_k, int B, int64_t stage_cap, int64_t nw_cap,
-            int cand_cap, uint32_t* __restrict__ gbits) {
-    using S = TopkSmem<THREADS, D1BITS>;
-    constexpr int kD1Shift = 32 - D1BITS;
-    constexpr int kD2Bits = 22 - D1BITS;        // bits (31-D1)..10
-    static_assert(kD2Bits <= D1BITS, "histogram holds the second digit");
+// Row checks shared by both kernels. Returns the row length, or -1 after
+// writing the output of a bad row (-1s, cnt 0, status) or of a row that keeps
+// every position (n <= K).
+template <int THREADS>
+__device__ __forceinline__ int64_t row_prologue(int t, const int32_t* __restrict__ n_valid,
+                                                bool n_from_pos, int64_t max_len, int64_t ld,
+                                                int K, int32_t* out, int32_t* __restrict__ cnt,
+                                                DeviceStatus* status,
+                                                const int32_t* __restrict__ cu_q,
+                                                const int32_t* __restrict__ cu_k, int B) {
+    const int64_t n = (int64_t)__ldg(n_valid + t) + (n_from_pos ? 1 : 0);
+    bool bad = n < 0 || n > max_len || n > ld;
+    if (cu_q != nullptr) {  // fused call: the row must lie inside its sequence
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+        }
+        const int64_t len_k = (int64_t)__ldg(cu_k + lo + 1) - __ldg(cu_k + lo);
+        bad = bad || n < 1 || n > len_k;
+    }
+    if (bad) {
+        if (threadIdx.x == 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
+        for (int i = threadIdx.x; i < K; i += THREADS) out[i] = -1;
+        if (cnt && threadIdx.x == 0) cnt[t] = 0;
+        return -1;
+    }
+    if (n <= K) {  // dormant selection: every position
+        for (int i = threadIdx.x; i < K; i += THREADS) out[i] = i < n ? i : -1;
+        if (cnt && threadIdx.x == 0) cnt[t] = (int32_t)n;
+        return -1;
+    }
+    return n;
+}
+
+// ---------------------------------------------------------------------------
+// Short rows: staged in shared memory as keys.
+// ---------------------------------------------------------------------------
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 4)
+topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
+                   bool n_from_pos, int T, int64_t max_len, int K, int32_t* __restrict__ idx,
+                   int32_t* __restrict__ cnt, DeviceStatus* status, const int32_t* __restrict__ cu_q,
+                   const int32_t* __restrict__ cu_k, int B, int32_t stage_cap) {
+    constexpr int D1 = 11;                      // digits: bits 31..21, 20..10, 9..0
+    constexpr int kD1Shift = 32 - D1;
+    using S = TopkSmem<THREADS, D1>;
     __shared__ S sh;
-    // dynamic: [staged row: stage_cap][bitmaps: 2*nw_cap, unless global][cand keys][cand pos]
+    // dynamic: keys[stage_cap] | above[nw_cap] | tie[nw_cap]
     extern __shared__ __align__(16) uint32_t dyn[];
-    uint32_t* staged = dyn;
-    uint32_t* bits_sm = dyn + (STAGED ? stage_cap : 0);
-    uint32_t* above_bits = gbits ? gbits + (int64_t)blockIdx.x * 2 * nw_cap : bits_sm;
-    uint32_t* tie_bits = above_bits + nw_cap;
-    uint32_t* cand_key = bits_sm + (gbits ? 0 : 2 * nw_cap);
-    int32_t* cand_pos = reinterpret_cast<int32_t*>(cand_key + cand_cap);
+    uint32_t* keys = dyn;
+    const int32_t nw_cap = (stage_cap + 31) >> 5;
+    uint32_t* above = dyn + stage_cap;
+    uint32_t* tie = above + nw_cap;
 
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        const int64_t n64 = (int64_t)__ldg(n_valid + t) + (n_from_pos ? 1 : 0);
         int32_t* out = idx + (int64_t)t * K;
-        bool bad = n64 < 0 || n64 > max_len || n64 > ld;
-        if (cu_q != nullptr) {  // fused call: the row must lie inside its sequence
-            int lo = 0, hi = B - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (__ldg(cu_q + mid) <= t) lo = mid; else hi = mid - 1;
-            }
-            const int64_t len_k = (int64_t)__ldg(cu_k + lo + 1) - __ldg(cu_k + lo);
-            bad = bad || n64 < 1 || n64 > len_k;
-        }
-        if (bad) {
-            if (threadIdx.x == 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
-            for (int i = threadIdx.x; i < K; i += THREADS) out[i] = -1;
-            if (cnt && threadIdx.x == 0) cnt[t] = 0;
-            continue;
-        }
-        if (n64 <= K) {  // dormant selection: every position
-            for (int i = threadIdx.x; i < K; i += THREADS) out[i] = i < n64 ? i : -1;
-            if (cnt && threadIdx.x == 0) cnt[t] = (int32_t)n64;
-            continue;
-        }
-        const int32_t n = (int32_t)n64;           // max_len < 2^31
-        const int32_t nvec = n >> 2;              // full 4-element vectors
-        const int32_t tail0 = nvec << 2;          // first element of the (< 4) tail
-        const float* row = scores + (int64_t)t * ld;
+        const int64_t n64 = row_prologue<THREADS>(t, n_valid, n_from_pos, max_len, ld, K, out, cnt,
+                                                  status, cu_q, cu_k, B);
+        if (n64 < 0) continue;
+        const int32_t n = (int32_t)n64;
+        const int32_t nvec = n >> 2, tail0 = nvec << 2;
         const int32_t nw = (n + 31) >> 5;
+        const float* row = scores + (int64_t)t * ld;
 
-        // ---- pass A: first digit (short rows: staged on the way)
+        // ---- pass A: stage keys, first digit
         __syncthreads();
-        zero<THREADS>(sh.hist, 1 << D1BITS);
-        zero<THREADS>(above_bits, nw);
-        zero<THREADS>(tie_bits, nw);
-        if (threadIdx.x == 0) sh.cand_count = 0;
+        zero<THREADS>(sh.hist, 1 << D1);
+        zero<THREADS>(above, nw);
+        zero<THREADS>(tie, nw);
         __syncthreads();
-        for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += kUnroll * THREADS) {
+        for (int32_t vb = 0; vb < nvec; vb += kUnroll * THREADS) {
             uint4 k[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u)   // all loads first
-                if (v0 + u * THREADS < nvec) k[u] = gkeys(row, v0 + u * THREADS);
+            for (int u = 0; u < kUnroll; ++u) {   // loads first
+                const int32_t v = vb + u * THREADS + threadIdx.x;
+                if (v < nvec) k[u] = gkeys(row, v);
+            }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                if (v0 + u * THREADS >= nvec) break;
-                if (STAGED) reinterpret_cast<uint4*>(staged)[v0 + u * THREADS] = k[u];
+                const int32_t v = vb + u * THREADS + threadIdx.x;
+                if (v >= nvec) break;
+                reinterpret_cast<uint4*>(keys)[v] = k[u];
                 atomicAdd(&sh.hist[k[u].x >> kD1Shift], 1u);
                 atomicAdd(&sh.hist[k[u].y >> kD1Shift], 1u);
                 atomicAdd(&sh.hist[k[u].z >> kD1Shift], 1u);
@@ -235,60 +284,19 @@ topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restr
         }
         if (threadIdx.x < n - tail0) {
             const uint32_t kk = fkey(__ldg(row + tail0 + threadIdx.x));
-            if (STAGED) staged[tail0 + threadIdx.x] = kk;
+            keys[tail0 + threadIdx.x] = kk;
             atomicAdd(&sh.hist[kk >> kD1Shift], 1u);
         }
         __syncthreads();
-        select_bin<THREADS>(sh, 1 << D1BITS, (uint32_t)K);
-        const uint32_t b1 = sh.sel_bin;
+        select_bin<THREADS>(sh, 1 << D1, (uint32_t)K);
+        uint32_t prefix = sh.sel_bin << kD1Shift;
         uint32_t rank = sh.sel_rank;
-        uint32_t prefix = b1 << kD1Shift;
 
-        // ---- pass B (long rows): certain positions -> bits, bin b1 -> candidates
-        bool use_cand = false;
-        if (!STAGED) {
-            auto visit = [&](uint32_t kk, int32_t pos) {
-                const uint32_t d = kk >> kD1Shift;
-                if (d > b1) {
-                    set_bit(above_bits, pos);
-                } else if (d == b1) {
-                    const uint32_t slot = atomicAdd(&sh.cand_count, 1u);
-                    if (slot < (uint32_t)cand_cap) {
-                        cand_key[slot] = kk;
-                        cand_pos[slot] = pos;
-                    }
-                }
-            };
-            for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += kUnroll * THREADS) {
-                uint4 k[kUnroll];
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u)
-                    if (v0 + u * THREADS < nvec) k[u] = gkeys(row, v0 + u * THREADS);
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int32_t v = v0 + u * THREADS;
-                    if (v >= nvec) break;
-                    // one test per vector: most vectors hold nothing >= b1
-                    const uint32_t mx = max(max(k[u].x, k[u].y), max(k[u].z, k[u].w));
-                    if ((mx >> kD1Shift) < b1) continue;
-                    visit(k[u].x, 4 * v);
-                    visit(k[u].y, 4 * v + 1);
-                    visit(k[u].z, 4 * v + 2);
-                    visit(k[u].w, 4 * v + 3);
-                }
-            }
-            if (threadIdx.x < n - tail0)
-                visit(fkey(__ldg(row + tail0 + threadIdx.x)), tail0 + threadIdx.x);
-            __syncthreads();
-            use_cand = sh.cand_count <= (uint32_t)cand_cap;
-        }
-        const int n_cand = use_cand ? (int)sh.cand_count : 0;
-
-        // ---- digits 2 and 3 among keys that match the digits chosen so far
+        // ---- digits 2 and 3 among the keys that match the digits so far
 #pragma unroll 1
         for (int d = 0; d < 2; ++d) {
             const int shift = d == 0 ? kD3Bits : 0;
-            const int bits = d == 0 ? kD2Bits : kD3Bits;
+            const int bits = d == 0 ? 22 - D1 : kD3Bits;
             const uint32_t mask_hi = d == 0 ? (0xFFFFFFFFu << kD1Shift) : (0xFFFFFFFFu << kD3Bits);
             const uint32_t bin_mask = (1u << bits) - 1u;
             __syncthreads();
@@ -297,15 +305,152 @@ topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restr
             auto add = [&](uint32_t kk) {
                 if ((kk & mask_hi) == prefix) atomicAdd(&sh.hist[(kk >> shift) & bin_mask], 1u);
             };
-            if (use_cand) {
-                for (int i = threadIdx.x; i < n_cand; i += THREADS) add(cand_key[i]);
-            } else {
-                for (int32_t v = threadIdx.x; v < nvec; v += THREADS) {
-                    const uint4 k = vkeys<STAGED>(row, staged, v);
-                    add(k.x); add(k.y); add(k.z); add(k.w);
+            for (int32_t v = threadIdx.x; v < nvec; v += THREADS) {
+                const uint4 k = reinterpret_cast<const uint4*>(keys)[v];
+                add(k.x); add(k.y); add(k.z); add(k.w);
+            }
+            if (threadIdx.x < n - tail0) add(keys[tail0 + threadIdx.x]);
+            __syncthreads();
+            select_bin<THREADS>(sh, 1 << bits, rank);
+            prefix |= sh.sel_bin << shift;
+            rank = sh.sel_rank;
+        }
+        const uint32_t tau = prefix;
+        const uint32_t need = rank;                   // tau-valued keys kept
+        const uint32_t n_above = (uint32_t)K - need;  // every key above tau is kept
+
+        // ---- mark: one thread per 32-position word, no atomics
+        for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
+            uint32_t a = 0, e = 0;
+            const int32_t p0 = w << 5;
+            const int32_t m = n - p0 < 32 ? n - p0 : 32;
+            for (int32_t b = 0; b < m; ++b) {
+                const uint32_t kk = keys[p0 + b];
+                a |= (kk > tau ? 1u : 0u) << b;
+                e |= (kk == tau ? 1u : 0u) << b;
+            }
+            above[w] = a;
+            tie[w] = e;
+        }
+        __syncthreads();
+
+        // ---- emit: above positions ascending, then the first `need` ties ascending
+        emit_ordered<THREADS>(sh, above, tie, nw, out, n_above, need);
+        if (cnt && threadIdx.x == 0) cnt[t] = K;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Long rows: streamed from global memory (L2), bitmaps in shared memory, or in
+// per-block global scratch when a row's bitmaps do not fit.
+// ---------------------------------------------------------------------------
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 2)
+topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
+                   bool n_from_pos, int T, int64_t max_len, int K, int32_t* __restrict__ idx,
+                   int32_t* __restrict__ cnt, DeviceStatus* status, const int32_t* __restrict__ cu_q,
+                   const int32_t* __restrict__ cu_k, int B, int64_t nw_cap,
+                   uint32_t* __restrict__ gbits) {
+    constexpr int D1 = 12;                      // digits: bits 31..20, 19..10, 9..0
+    constexpr int kD1Shift = 32 - D1;
+    using S = TopkSmem<THREADS, D1>;
+    __shared__ S sh;
+    extern __shared__ __align__(16) uint32_t dyn[];   // above | tie | cand bitmaps
+    uint32_t* above = gbits ? gbits + (int64_t)blockIdx.x * 3 * nw_cap : dyn;
+    uint32_t* tie = above + nw_cap;
+    uint32_t* cand = tie + nw_cap;
+
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        int32_t* out = idx + (int64_t)t * K;
+        const int64_t n64 = row_prologue<THREADS>(t, n_valid, n_from_pos, max_len, ld, K, out, cnt,
+                                                  status, cu_q, cu_k, B);
+        if (n64 < 0) continue;
+        const int32_t n = (int32_t)n64;
+        const int32_t nvec = n >> 2, tail0 = nvec << 2;
+        const int32_t nw = (n + 31) >> 5;
+        const float* row = scores + (int64_t)t * ld;
+
+        // ---- pass A: first digit
+        __syncthreads();
+        zero<THREADS>(sh.hist, 1 << D1);
+        zero<THREADS>(above, nw);
+        zero<THREADS>(tie, nw);
+        zero<THREADS>(cand, nw);
+        __syncthreads();
+        for (int32_t vb = 0; vb < nvec; vb += kUnroll * THREADS) {
+            uint4 k[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int32_t v = vb + u * THREADS + threadIdx.x;
+                if (v < nvec) k[u] = gkeys(row, v);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (vb + u * THREADS + threadIdx.x >= nvec) break;
+                atomicAdd(&sh.hist[k[u].x >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[k[u].y >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[k[u].z >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[k[u].w >> kD1Shift], 1u);
+            }
+        }
+        if (threadIdx.x < n - tail0)
+            atomicAdd(&sh.hist[fkey(__ldg(row + tail0 + threadIdx.x)) >> kD1Shift], 1u);
+        __syncthreads();
+        select_bin<THREADS>(sh, 1 << D1, (uint32_t)K);
+        const uint32_t b1 = sh.sel_bin;
+        uint32_t prefix = b1 << kD1Shift;
+        uint32_t rank = sh.sel_rank;
+
+        // ---- split: above b1 -> above bits, in b1 -> cand bits (4-bit masks)
+        for (int32_t vb = 0; vb < nvec; vb += kUnroll * THREADS) {
+            uint4 k[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int32_t v = vb + u * THREADS + threadIdx.x;
+                if (v < nvec) k[u] = gkeys(row, v);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int32_t v = vb + u * THREADS + threadIdx.x;
+                if (v >= nvec) break;
+                uint32_t ma = 0, mc = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t d = comp(k[u], j) >> kD1Shift;
+                    ma |= (d > b1 ? 1u : 0u) << j;
+                    mc |= (d == b1 ? 1u : 0u) << j;
                 }
-                if (threadIdx.x < n - tail0)
-                    add(STAGED ? staged[tail0 + threadIdx.x] : fkey(__ldg(row + tail0 + threadIdx.x)));
+                const uint32_t sh4 = (uint32_t)(v & 7) * 4;   // 4 positions of word v/8
+                if (ma) atomicOr(above + (v >> 3), ma << sh4);
+                if (mc) atomicOr(cand + (v >> 3), mc << sh4);
+            }
+        }
+        if (threadIdx.x < n - tail0) {
+            const int32_t p = tail0 + threadIdx.x;
+            const uint32_t d = fkey(__ldg(row + p)) >> kD1Shift;
+            if (d > b1) set_bit(above, p);
+            else if (d == b1) set_bit(cand, p);
+        }
+        __syncthreads();
+
+        // ---- digits 2 and 3 over the candidates (keys gathered from the row)
+#pragma unroll 1
+        for (int d = 0; d < 2; ++d) {
+            const int shift = d == 0 ? kD3Bits : 0;
+            const int bits = d == 0 ? 22 - D1 : kD3Bits;
+            const uint32_t mask_hi = d == 0 ? (0xFFFFFFFFu << kD1Shift) : (0xFFFFFFFFu << kD3Bits);
+            const uint32_t bin_mask = (1u << bits) - 1u;
+            __syncthreads();
+            zero<THREADS>(sh.hist, 1 << bits);
+            __syncthreads();
+            for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
+                uint32_t m = cand[w];
+                while (m) {
+                    const int32_t p = (w << 5) + (__ffs(m) - 1);
+                    m &= m - 1u;
+                    const uint32_t kk = fkey(__ldg(row + p));
+                    if ((kk & mask_hi) == prefix) atomicAdd(&sh.hist[(kk >> shift) & bin_mask], 1u);
+                }
             }
             __syncthreads();
             select_bin<THREADS>(sh, 1 << bits, rank);
@@ -313,60 +458,48 @@ topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restr
             rank = sh.sel_rank;
         }
         const uint32_t tau = prefix;
-        const uint32_t need = rank;                   // members of the tie group kept
-        const uint32_t n_above = (uint32_t)K - need;  // every key > tau is kept
+        const uint32_t need = rank;                   // tau-valued keys kept
+        const uint32_t n_above = (uint32_t)K - need;  // every key above tau is kept
 
-        // ---- mark keys above / equal to tau not marked yet
-        if (use_cand) {
-            for (int i = threadIdx.x; i < n_cand; i += THREADS) {
-                const uint32_t kk = cand_key[i];
-                if (kk > tau) set_bit(above_bits, cand_pos[i]);
-                else if (kk == tau) set_bit(tie_bits, cand_pos[i]);
+        // ---- mark: candidates above tau -> above bits, equal -> tie bits
+        for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
+            uint32_t m = cand[w];
+            if (!m) continue;
+            uint32_t a = 0, e = 0;
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1u;
+                const uint32_t kk = fkey(__ldg(row + (w << 5) + b));
+                a |= (kk > tau ? 1u : 0u) << b;
+                e |= (kk == tau ? 1u : 0u) << b;
             }
-        } else {
-            // staged rows never ran pass B, so every key above tau is marked here;
-            // streamed rows marked first digits above b1 in pass B already
-            auto mark = [&](uint32_t kk, int32_t pos) {
-                if (kk > tau) {
-                    if (STAGED || (kk >> kD1Shift) == b1) set_bit(above_bits, pos);
-                } else if (kk == tau) {
-                    set_bit(tie_bits, pos);
-                }
-            };
-            for (int32_t v = threadIdx.x; v < nvec; v += THREADS) {
-                const uint4 k = vkeys<STAGED>(row, staged, v);
-                const uint32_t mx = max(max(k.x, k.y), max(k.z, k.w));
-                if (mx < tau) continue;
-                mark(k.x, 4 * v); mark(k.y, 4 * v + 1); mark(k.z, 4 * v + 2); mark(k.w, 4 * v + 3);
-            }
-            if (threadIdx.x < n - tail0)
-                mark(STAGED ? staged[tail0 + threadIdx.x] : fkey(__ldg(row + tail0 + threadIdx.x)),
-                     tail0 + threadIdx.x);
+            above[w] |= a;   // this thread owns word w in this step
+            tie[w] = e;
         }
         __syncthreads();
 
-        // ---- emit: above positions ascending, then the first `need` ties ascending
-        emit_ordered<THREADS>(sh, above_bits, nw, out, n_above);
-        emit_ordered<THREADS>(sh, tie_bits, nw, out + n_above, need);
+        // ---- emit
+        emit_ordered<THREADS>(sh, above, tie, nw, out, n_above, need);
         if (cnt && threadIdx.x == 0) cnt[t] = K;
     }
 }
 
-constexpr size_t kStreamStatic = sizeof(TopkSmem<kStreamThreads, 12>);
-
-// Shared memory a block may use in total (GB300 opt-in limit, 227 KB).
+// Shared memory a block may use in total (GB300 opt-in limit, 227 KB), and a
+// bound on the streamed kernel's static part (histogram, scans, counters, with
+// alignment padding).
 constexpr int64_t kBlockSmem = 227 * 1024;
+constexpr int64_t kStreamStaticBound = (int64_t)sizeof(TopkSmem<kStreamThreads, 12>) + 256;
 
 bool bitmaps_fit_in_smem(int64_t row_cap) {
     const int64_t nw_cap = (row_cap + 31) / 32;
-    return (int64_t)kCandCap * 8 + 2 * nw_cap * 4 + (int64_t)kStreamStatic <= kBlockSmem;
+    return 3 * nw_cap * 4 + kStreamStaticBound <= kBlockSmem;
 }
 
 }  // namespace
 
 size_t topk_scratch_bytes(int32_t T, int64_t max_len) {
     if (T <= 0 || max_len <= kStageCap || bitmaps_fit_in_smem(max_len)) return 0;
-    return (size_t)kScratchBlocks * 2 * (size_t)((max_len + 31) / 32) * 4;
+    return (size_t)kScratchBlocks * 3 * (size_t)((max_len + 31) / 32) * 4;
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
@@ -375,26 +508,28 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     const int64_t nw_cap = (row_cap + 31) / 32;
     const int grid = a.T < 65535 ? a.T : 65535;
     if (row_cap <= kStageCap) {
-        const int64_t stage = (int64_t)align_up((size_t)row_cap, 4);
-        const size_t smem = (size_t)(stage + 2 * nw_cap) * 4;
-        auto kern = topk_kernel<kStagedThreads, 11, true>;
+        const int32_t stage = (int32_t)align_up((size_t)row_cap, 4);
+        const size_t smem = ((size_t)stage + 2 * (size_t)nw_cap) * 4;
+        auto kern = topk_staged_kernel<kStagedThreads>;
         cudaError_t e = ensure_smem_optin(
             (const void*)kern, (kStageCap + 2 * ((kStageCap + 31) / 32)) * 4);
         if (e != cudaSuccess) return e;
         kern<<<grid, kStagedThreads, smem, stream>>>(a.scores, a.ld, a.n_valid, a.n_from_pos, a.T,
                                                      a.max_len, a.topk, a.idx, a.cnt, a.status,
-                                                     a.cu_q, a.cu_k, a.B, stage, nw_cap, 0, nullptr);
+                                                     a.cu_q, a.cu_k, a.B, stage);
     } else {
         const bool in_smem = bitmaps_fit_in_smem(row_cap);
         if (!in_smem && a.bits_scratch == nullptr) return cudaErrorInvalidValue;
-        const size_t smem = (size_t)kCandCap * 8 + (in_smem ? (size_t)(2 * nw_cap * 4) : 0);
+        const size_t smem = in_smem ? (size_t)(3 * nw_cap * 4) : 0;
         const int g = in_smem ? grid : (grid < kScratchBlocks ? grid : kScratchBlocks);
-        auto kern = topk_kernel<kStreamThreads, 12, false>;
-        cudaError_t e = ensure_smem_optin((const void*)kern, kBlockSmem - (int64_t)kStreamStatic);
+        auto kern = topk_stream_kernel<kStreamThreads>;
+        const int64_t st = kernel_static_smem((const void*)kern);
+        if (st < 0 || st > kStreamStaticBound) return cudaErrorInvalidValue;
+        cudaError_t e = ensure_smem_optin((const void*)kern, kBlockSmem - kStreamStaticBound);
         if (e != cudaSuccess) return e;
         kern<<<g, kStreamThreads, smem, stream>>>(a.scores, a.ld, a.n_valid, a.n_from_pos, a.T,
                                                   a.max_len, a.topk, a.idx, a.cnt, a.status,
-                                                  a.cu_q, a.cu_k, a.B, 0, nw_cap, kCandCap,
+                                                  a.cu_q, a.cu_k, a.B, nw_cap,
                                                   in_smem ? nullptr : a.bits_scratch);
     }
     count_launch();

@@ -151,13 +151,16 @@ def test_scores_real_inputs_within_tolerance(B):
 
 @pytest.mark.parametrize("kind", ["ties", "normal", "mixed", "const"])
 @pytest.mark.parametrize("K", [1, 7, 2048])
-@pytest.mark.parametrize("lens", ["short", "long"])
+@pytest.mark.parametrize("lens", ["short", "mid", "long"])
 def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
     rng = np.random.default_rng(zlib.crc32(f"{kind}/{K}/{lens}".encode()))
     if lens == "short":
         n_valid = np.concatenate([[0, 1, K - 1 if K > 1 else 0, K, K + 1, 2047, 2048, 2049, 4096],
                                   rng.integers(1, 20000, size=20), [50_000]]).astype(np.int32)
-    else:   # longer than the shared-memory staging cap; one row needs global bitmaps
+    elif lens == "mid":   # many rows of 16K..32K positions: clusters of 2 CTAs
+        n_valid = rng.integers(16_000, 30_001, size=400).astype(np.int32)
+        n_valid[:3] = [30_000, 16_385, K + 1]
+    else:   # up to 8 x 16K positions (clusters of 8); one row beyond: streamed path
         n_valid = np.array([70_000, 131_072, 65_537, K + 3, 100_001], np.int32)
         if kind in ("normal", "ties"):
             n_valid = np.append(n_valid, np.int32(700_001))
