@@ -151,10 +151,12 @@ IDX_API size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_l
  * and may fail under memory pressure), or a plugin that its host framework
  * hands only input and output buffers. Same arguments and results as
  * idx_score_topk, minus ws/ws_bytes; it allocates nothing.
- *   Scratch   a fixed 33 MiB (+256 B) array inside the library's device image,
+ *   Scratch   a fixed 39 MiB (+256 B) array inside the library's device image,
  *             reserved on every GPU that loads the library until process exit.
  *   Limit     T * round_up(max_len, 4) * 4 <= 32 MiB (e.g. 64 queries of up to
- *             131,072 keys) and T + B <= 40,000; larger calls return
+ *             131,072 keys), T + B <= 40,000, and at most 6 MiB of selection
+ *             scratch (histograms and bitmaps of batches of up to 128
+ *             queries with long histories); larger calls return
  *             IDX_ERR_WORKSPACE, enqueue nothing, and idx_last_error() says why.
  *   Sharing   every call on a device uses the same array, which keeps the last
  *             call's contents; calls that can overlap on the GPU (other streams,

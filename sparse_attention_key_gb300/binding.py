@@ -257,7 +257,8 @@ def score_topk_noalloc(q, k, w, q_pos, cu_q, cu_k, max_len: int, topk: int = TOP
 
     For callers that cannot supply extra device memory (a fixed memory plan, or
     a host that hands over only inputs and outputs). The library's scratch is
-    32 MiB per GPU: T * round_up(max_len, 4) * 4 bytes must fit. All calls on a
+    39 MiB per GPU: T * round_up(max_len, 4) * 4 bytes must fit in its 32 MiB
+    of staged scores, T + B <= 40,000, and the selection scratch in 6 MiB. All calls on a
     device share it, so calls that may overlap on the GPU must be serialised;
     the first call on a device resolves the scratch address and should precede
     any stream capture. ``idx``/``cnt`` may be preallocated by the caller.

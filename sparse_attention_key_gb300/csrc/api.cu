@@ -262,13 +262,19 @@ idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
     char* base = (char*)ws + kWsHeader + align_up(score_plan_bytes(B, T), 256);
     float* scores = (float*)base;
     DeviceStatus* status = (DeviceStatus*)ws;
-    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, status};
-    cudaError_t e = launch_score_tc(sa, (char*)ws + kWsHeader, s);
-    if (e != cudaSuccess) return cuda_fail(e, "score launch");
     TopkArgs ta{scores, ld, q_pos, true, T, max_len, topk, idx, cnt, status, cu_q, cu_k, B};
     if (topk_scratch_bytes(T, max_len))
         ta.bits_scratch = (uint32_t*)((char*)scores +
                                       align_up((size_t)T * (size_t)ld * sizeof(float), 256));
+    // few long rows: the scorer also histograms the rows for the selection
+    cudaError_t e = topk_prepare(&ta, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(selection histograms)");
+    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, status};
+    sa.row_hist = topk_split_row_hist(ta);
+    bool hist_filled = false;
+    e = launch_score_tc(sa, (char*)ws + kWsHeader, s, &hist_filled);
+    if (e != cudaSuccess) return cuda_fail(e, "score launch");
+    if (hist_filled) ta.hist_state = 2;
     e = launch_topk(ta, s);
     return e == cudaSuccess ? IDX_OK : cuda_fail(e, "topk launch");
 }

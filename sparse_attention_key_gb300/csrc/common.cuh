@@ -45,11 +45,15 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
 }
 
 // Order-preserving map of an fp32 score to uint32: a > b (numerically) iff
-// key(a) > key(b). -0.0 maps to the key of +0.0 so that the two compare equal.
+// score_key(a) > score_key(b). Adding +0 first turns -0 into +0, so the two
+// zeros share one key; then negative values have all bits flipped and
+// non-negative ones the sign bit set.
 __device__ __forceinline__ uint32_t score_key(float x) {
-    uint32_t u = __float_as_uint(x);
-    if (u == 0x80000000u) u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t u = __float_as_uint(__fadd_rn(x, 0.0f));
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
+
+// Bins of the first radix digit of the exact top-K (key bits 31..20).
+constexpr int kTopkDigit1Bins = 4096;
 
 }  // namespace lidx

@@ -49,6 +49,9 @@ struct ScoreArgs {
     float* scores;
     int64_t ld;
     DeviceStatus* status;
+    // Optional [T][kTopkDigit1Bins] first-digit histograms of the written
+    // scores (zeroed by the caller), filled by scorers that support it.
+    uint32_t* row_hist = nullptr;
 };
 
 // CUDA-core scorer: one thread per key, streams K with 16-byte loads.
@@ -57,7 +60,9 @@ cudaError_t launch_score_simt(const ScoreArgs& a, cudaStream_t stream);
 // Tensor-core scorer (tcgen05/TMEM/TMA): a plan kernel, then the persistent
 // scorer. `plan_ws` holds tc_plan_bytes(B, T) bytes of device scratch.
 size_t tc_plan_bytes(int32_t B, int32_t T);
-cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream);
+// *hist_filled (may be NULL) tells whether a.row_hist was filled.
+cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream,
+                            bool* hist_filled = nullptr);
 
 // Arguments of one top-K call.
 struct TopkArgs {
@@ -76,13 +81,21 @@ struct TopkArgs {
     const int32_t* cu_q = nullptr;
     const int32_t* cu_k = nullptr;
     int32_t B = 0;
-    // Global scratch for the position bitmaps of rows too long for shared
-    // memory (topk_scratch_bytes); NULL when that size is 0.
+    // Global scratch (topk_scratch_bytes; NULL when that size is 0): position
+    // bitmaps of very long rows, or the split path's row histograms and bitmaps.
     uint32_t* bits_scratch = nullptr;
+    // Split path only: 0 = row histograms not prepared, 1 = zeroed,
+    // 2 = first-digit histograms already filled by the scorer.
+    int hist_state = 0;
 };
 
 // Device scratch launch_topk needs for rows of up to max_len (often 0).
 size_t topk_scratch_bytes(int32_t T, int64_t max_len);
+// Split path (few long rows): its [T][kTopkDigit1Bins] first-digit row
+// histograms inside bits_scratch, or NULL when the call does not take it.
+uint32_t* topk_split_row_hist(const TopkArgs& a);
+// Zero the split path's row histograms (sets a->hist_state = 1); no-op otherwise.
+cudaError_t topk_prepare(TopkArgs* a, cudaStream_t stream);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
 }  // namespace lidx

@@ -12,9 +12,10 @@
 // Limits and sharing:
 //   - The scratch array holds kNoAllocScoreBytes (32 MiB) of staged scores:
 //     T * round_up(max_len, 4) * 4 bytes must fit, e.g. 64 queries with up to
-//     131,072 keys each; and 1 MiB of tile plan: T + B <= 40,000. Larger calls
-//     are rejected on the host (IDX_ERR_WORKSPACE).
-//   - Every GPU that loads the library reserves the array (33 MiB + 256 B)
+//     131,072 keys each; 1 MiB of tile plan: T + B <= 40,000; and 6 MiB of
+//     selection scratch (histograms and position bitmaps of decode-sized
+//     batches). Larger calls are rejected on the host (IDX_ERR_WORKSPACE).
+//   - Every GPU that loads the library reserves the array (39 MiB + 256 B)
 //     until the process exits.
 //   - All calls on a device share the one array and it keeps the contents of
 //     the last call: calls that can overlap on the GPU (different streams, or
@@ -33,7 +34,9 @@ namespace lidx {
 
 constexpr size_t kNoAllocScoreBytes = size_t(32) << 20;  // staged fp32 scores
 constexpr size_t kNoAllocPlanBytes = size_t(1) << 20;    // tile plan of the scorer
-constexpr size_t kNoAllocScratchBytes = kWsHeader + kNoAllocPlanBytes + kNoAllocScoreBytes;
+constexpr size_t kNoAllocTopkBytes = size_t(6) << 20;    // selection scratch
+constexpr size_t kNoAllocScratchBytes =
+    kWsHeader + kNoAllocPlanBytes + kNoAllocScoreBytes + kNoAllocTopkBytes;
 
 // Library-owned scratch. Host code must not use this name as a pointer: on the
 // host it only stands for the symbol; its device address comes from
@@ -104,9 +107,9 @@ extern "C" IDX_API idx_status idx_score_topk_noalloc(
         return noalloc_fail(IDX_ERR_WORKSPACE,
                             "T * round_up(max_len, 4) * 4 bytes exceeds the 32 MiB scratch of "
                             "idx_score_topk_noalloc; use idx_score_topk with a workspace");
-    if (topk_scratch_bytes(T, max_len) != 0)
+    if (topk_scratch_bytes(T, max_len) > kNoAllocTopkBytes)
         return noalloc_fail(IDX_ERR_WORKSPACE,
-                            "max_len is too long for the shared-memory selection of "
+                            "the selection scratch for this T and max_len exceeds the 6 MiB of "
                             "idx_score_topk_noalloc; use idx_score_topk with a workspace");
     if (tc_plan_bytes(B, T) > kNoAllocPlanBytes || (int64_t)T + B > 40000)
         return noalloc_fail(IDX_ERR_WORKSPACE,
@@ -128,10 +131,18 @@ extern "C" IDX_API idx_status idx_score_topk_noalloc(
     if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
     void* plan = scratch + kWsHeader;
     float* scores = reinterpret_cast<float*>(scratch + kWsHeader + kNoAllocPlanBytes);
-    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, status};
-    e = launch_score_tc(sa, plan, s);
-    if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
     TopkArgs ta{scores, ld, q_pos, true, T, max_len, topk, idx, cnt, status, cu_q, cu_k, B};
+    if (topk_scratch_bytes(T, max_len))
+        ta.bits_scratch = reinterpret_cast<uint32_t*>(scratch + kWsHeader + kNoAllocPlanBytes +
+                                                      kNoAllocScoreBytes);
+    e = topk_prepare(&ta, s);   // zeroes the selection histograms when used
+    if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
+    ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, status};
+    sa.row_hist = topk_split_row_hist(ta);
+    bool hist_filled = false;
+    e = launch_score_tc(sa, plan, s, &hist_filled);
+    if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
+    if (hist_filled) ta.hist_state = 2;
     e = launch_topk(ta, s);
     if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
     return IDX_OK;

@@ -208,14 +208,18 @@ struct TcCfg {
     static constexpr int Q_BOX_ROWS = QROWS < 256 ? QROWS : 256;
     static constexpr int TMEM_COLS = NACC * N;
     static constexpr int THREADS = (2 + EPI_WARPS) * 32;
-    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * NACC + 3) + 16;
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * NACC + 4) + 16;
     // Epilogue copy of the current group: weights [GQ][32] fp32, causal length
     // (0 = no output) and score row pointer per query.
     static constexpr int EPI_BYTES = (GQ * 32 * 4 + GQ * 8 + GQ * 4 + 15) / 16 * 16;
     static constexpr int EPI_THREADS = EPI_WARPS * 32;
     // The dynamic shared-memory window starts 1024-byte aligned (the kernel has
     // no static shared memory); the kernel checks this before using it.
-    static constexpr int SMEM = Q_BYTES + STAGES * K_STAGE + EPI_BYTES + BAR_BYTES;
+    // One query per group (decode): the epilogue also histograms the first
+    // radix digit of each written score for the exact top-K that follows.
+    static constexpr int HIST_BINS = NQ * NSUB == 1 ? kTopkDigit1Bins : 0;
+    static constexpr int HIST_OFF = (Q_BYTES + STAGES * K_STAGE + EPI_BYTES + BAR_BYTES + 15) / 16 * 16;
+    static constexpr int SMEM = HIST_OFF + HIST_BINS * 4;
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(N % 16 == 0 && N >= 32 && N <= 256, "MMA N");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
@@ -266,7 +270,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                 const float* __restrict__ w, const int32_t* __restrict__ q_pos,
                 const int32_t* __restrict__ cu_k, int64_t max_len, float* __restrict__ scores,
-                int64_t ld, TcPlan plan, DeviceStatus* status) {
+                int64_t ld, TcPlan plan, DeviceStatus* status, uint32_t* __restrict__ row_hist) {
     using namespace ptx;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_addr(smem_raw) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
@@ -289,7 +293,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
     uint64_t* q_full = acc_empty + C::NACC;
     uint64_t* q_empty = q_full + 1;
     uint64_t* done_bar = q_empty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+    uint64_t* epi_bar = done_bar + 1;   // epilogue warps' own barrier (bounded waits)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
+    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::HIST_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -305,6 +311,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
         mbar_init(done_bar, 1);
+        mbar_init(epi_bar, C::EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -452,7 +459,31 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         const int qoff = ((warp - 2) / 4) * kQpw;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         int acc = 0;
-        uint32_t aphase = 0;
+        uint32_t aphase = 0, ephase = 0;
+        const bool hist_on = C::HIST_BINS > 0 && row_hist != nullptr;
+        // Barrier of the epilogue warps; false when the CTA is giving up.
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_bar);
+            const bool ok = mbar_wait(epi_bar, ephase, abort_flag, kWaitLimitNs);
+            ephase ^= 1;
+            if (!ok) give_up(7);
+            return ok;
+        };
+        // Add the shared first-digit histogram into row `t`'s and clear it.
+        auto flush_hist = [&](int t) {
+            uint32_t* g = row_hist + (int64_t)t * C::HIST_BINS;
+            for (int b = et; b < C::HIST_BINS; b += C::EPI_THREADS) {
+                const uint32_t v = hist_s[b];
+                if (v) {
+                    atomicAdd(g + b, v);
+                    hist_s[b] = 0;
+                }
+            }
+        };
+        if (hist_on)
+            for (int b = et; b < C::HIST_BINS; b += C::EPI_THREADS) hist_s[b] = 0;
+        int hist_row = -1;
         if (beg < end) {
             StepCursor cur;
             cur.init(beg, plan, n_groups);
@@ -461,8 +492,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                 if (s > beg) new_group = cur.advance(s, plan);
                 if (new_group) {
                     // copy the group's weights, causal lengths and row pointers
-                    named_bar_sync(1, C::EPI_THREADS);
+                    if (!epi_sync()) break;
+                    if (hist_on && hist_row >= 0) flush_hist(hist_row);
                     const int q0 = cur.desc.y, nq = cur.desc.z;
+                    hist_row = q0;
                     for (int i = et; i < C::GQ * 32; i += C::EPI_THREADS) {
                         const int qi = i >> 5;
                         epi_w[i] = qi < nq ? __ldg(w + (int64_t)(q0 + qi) * 32 + (i & 31)) : 0.f;
@@ -478,7 +511,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                         epi_n[et] = ne;
                         epi_row[et] = scores + (int64_t)(q0 + et) * ld;
                     }
-                    named_bar_sync(1, C::EPI_THREADS);
+                    if (!epi_sync()) break;
                 }
                 const int32_t key = cur.j * 128 + quarter * 32 + lane;
 #pragma unroll 1
@@ -518,10 +551,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                             acc2 = __ffma2_rn(make_float2(ww.x, ww.y), r0, acc2);
                             acc2 = __ffma2_rn(make_float2(ww.z, ww.w), r1, acc2);
                         }
-                        epi_row[q][key] = acc2.x + acc2.y;
+                        const float S = acc2.x + acc2.y;
+                        epi_row[q][key] = S;
+                        if (hist_on) atomicAdd(&hist_s[score_key(S) >> 20], 1u);
                     }
                 }
             }
+            if (hist_on && !aborted && hist_row >= 0 && epi_sync()) flush_hist(hist_row);
         }
     }
 
@@ -576,7 +612,10 @@ using PrefillCfg = TcCfg<8, 2, 2, 3, 16>;
 using DecodeCfg = TcCfg<1, 1, 4, 6, 4>;
 
 template <class C>
-static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream_t stream) {
+static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream_t stream,
+                             bool* hist_filled) {
+    uint32_t* row_hist = C::HIST_BINS > 0 ? a.row_hist : nullptr;
+    if (hist_filled) *hist_filled = row_hist != nullptr;
     CUtensorMap tk, tq;
     if (!make_tmap(&tk, a.k, a.n_keys, 128) || !make_tmap(&tq, a.q, (int64_t)a.T * 32, C::Q_BOX_ROWS))
         return cudaErrorInvalidValue;
@@ -589,16 +628,17 @@ static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream
     if (e != cudaSuccess) return e;
     const DeviceInfo& dev = device_info();
     score_tc_kernel<C><<<dev.sm_count, C::THREADS, C::SMEM, stream>>>(
-        tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan, a.status);
+        tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan, a.status, row_hist);
     count_launch();
     return cudaGetLastError();
 }
 
-cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream) {
+cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream,
+                            bool* hist_filled) {
     const TcPlan plan = plan_layout(plan_ws, a.B, a.T);
     // Mostly one query per sequence (decode) vs. many (prefill / chunks).
-    if ((int64_t)a.T <= 2 * (int64_t)a.B) return launch_cfg<DecodeCfg>(a, plan, stream);
-    return launch_cfg<PrefillCfg>(a, plan, stream);
+    if ((int64_t)a.T <= 2 * (int64_t)a.B) return launch_cfg<DecodeCfg>(a, plan, stream, hist_filled);
+    return launch_cfg<PrefillCfg>(a, plan, stream, hist_filled);
 }
 
 }  // namespace lidx

@@ -51,6 +51,7 @@ struct TopkSmem {
     uint32_t hist[1 << D1BITS];
     uint32_t scan[THREADS / 32 + 1];
     uint64_t scan64[THREADS / 32];
+    uint32_t super[128];           // sums of 32-bin groups (select_bin)
     uint32_t sel_bin, sel_rank, cand_count;
 };
 
@@ -109,26 +110,64 @@ __device__ __forceinline__ uint64_t block_excl_scan64(S& sh, uint64_t v) {
 }
 
 // The bin (counting from the highest) holding the element of rank `rank`
-// (1-based from the largest) in hist[0..nbins); writes sh.sel_bin and the rank
-// inside that bin to sh.sel_rank.
+// (1-based from the largest) in sh.hist[0..nbins); writes sh.sel_bin and the
+// rank inside that bin to sh.sel_rank. Two levels: the warps sum groups of 32
+// consecutive bins (lanes read consecutive words), then warp 0 finds the group
+// and the bin inside it with warp scans. nbins: 1024, 2048 or 4096.
 template <int THREADS, class S>
 __device__ __forceinline__ void select_bin(S& sh, int nbins, uint32_t rank) {
-    const int per = (nbins + THREADS - 1) / THREADS;       // bins per thread
-    const int hi = nbins - 1 - (int)threadIdx.x * per;     // this thread's highest bin
-    uint32_t sum = 0;
-    for (int i = 0; i < per; ++i)
-        if (hi - i >= 0) sum += sh.hist[hi - i];
-    const uint32_t excl = block_excl_scan<THREADS>(sh, sum);
-    if (excl < rank && rank <= excl + sum) {   // exactly one thread
-        uint32_t acc = excl;
-        for (int i = 0; i < per; ++i) {
-            const uint32_t c = sh.hist[hi - i];
-            if (acc + c >= rank) {
-                sh.sel_bin = (uint32_t)(hi - i);
-                sh.sel_rank = rank - acc;
-                break;
+    constexpr int W = THREADS / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ngroups = nbins >> 5;
+    for (int g = warp; g < ngroups; g += W) {
+        uint32_t v = sh.hist[(g << 5) + lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) sh.super[g] = v;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // lane l owns groups top-per*l .. top-per*l-per+1 (from the highest)
+        const int per = ngroups >> 5;
+        const int top = ngroups - 1 - lane * per;
+        uint32_t sum = 0;
+        for (int i = 0; i < per; ++i) sum += sh.super[top - i];
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        const uint32_t excl = incl - sum;
+        const int src = __ffs(__ballot_sync(0xffffffffu, excl < rank && rank <= incl)) - 1;
+        int grp = 0;
+        uint32_t r = 0;
+        if (lane == src) {
+            uint32_t acc = excl;
+            for (int i = 0; i < per; ++i) {
+                const uint32_t c = sh.super[top - i];
+                if (acc + c >= rank) {
+                    grp = top - i;
+                    r = rank - acc;
+                    break;
+                }
+                acc += c;
             }
-            acc += c;
+        }
+        grp = __shfl_sync(0xffffffffu, grp, src);
+        r = __shfl_sync(0xffffffffu, r, src);
+        // inside the group: lane l holds bin grp*32 + 31 - l (from the highest)
+        const uint32_t c = sh.hist[(grp << 5) + 31 - lane];
+        uint32_t ci = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(0xffffffffu, ci, o);
+            if (lane >= o) ci += x;
+        }
+        const int l2 = __ffs(__ballot_sync(0xffffffffu, ci >= r)) - 1;
+        if (lane == l2) {
+            sh.sel_bin = (uint32_t)((grp << 5) + 31 - l2);
+            sh.sel_rank = r - (ci - c);
         }
     }
     __syncthreads();
@@ -139,12 +178,7 @@ __device__ __forceinline__ void zero(uint32_t* p, int64_t n) {
     for (int64_t i = threadIdx.x; i < n; i += THREADS) p[i] = 0;
 }
 
-// Order-preserving key of a score: a > b (numerically) iff fkey(a) > fkey(b).
-// Adding +0 turns -0 into +0 first, so the two zeros share one key.
-__device__ __forceinline__ uint32_t fkey(float x) {
-    const uint32_t u = __float_as_uint(__fadd_rn(x, 0.0f));
-    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
-}
+__device__ __forceinline__ uint32_t fkey(float x) { return score_key(x); }
 
 // Keys of the 4 scores of vector v (elements 4v..4v+3) of a row, from global.
 __device__ __forceinline__ uint4 gkeys(const float* row, int32_t v) {
@@ -484,6 +518,311 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Few long rows (decode): each row is split into slices handled by separate
+// blocks, so that T rows keep T x slices blocks busy instead of T. Three
+// kernels share per-row scratch in global memory: first-digit histogram
+// [4096], second-digit histogram of the candidates [1024], and the above /
+// tie / cand bitmaps.
+//   split_hist   per slice: first-digit histogram, added into the row's;
+//   split_mark   per slice: select b1 from the row histogram, write whole
+//                bitmap words (above b1, in b1), add the candidates' second
+//                digits into the row's second histogram;
+//   split_finish per row: digits 2 and 3 (the third over the candidates'
+//                keys, gathered from the row), mark, ordered emit.
+// ---------------------------------------------------------------------------
+constexpr int kSplitThreads = 256;
+constexpr int kSplitSlice = 4096;           // positions per block (multiple of 128)
+constexpr int kFinishThreads = 1024;
+constexpr int kFinishCand = 8192;           // candidates listed in (dynamic) shared memory
+constexpr int32_t kSplitMaxRows = 128;      // fewer rows than GB300 has SMs
+
+struct SplitScratch {
+    uint32_t* hist1;   // [T][4096]
+    uint32_t* hist2;   // [T][1024]
+    uint32_t* bits;    // [T][3][nw_cap]: above | tie | cand
+    int64_t nw_cap;
+};
+
+__host__ __device__ inline size_t split_hist_bytes(int32_t T) {
+    return (size_t)T * (4096 + 1024) * 4;
+}
+
+__device__ __forceinline__ SplitScratch split_scratch(uint32_t* base, int32_t T, int64_t nw_cap) {
+    SplitScratch sc;
+    sc.hist1 = base;
+    sc.hist2 = base + (size_t)T * 4096;
+    sc.bits = base + (size_t)T * 5120;
+    sc.nw_cap = nw_cap;
+    return sc;
+}
+
+// Row length when the row needs a selection (n > K and valid), else -1; no
+// side effects (the finishing kernel writes the other rows' output).
+__device__ __forceinline__ int64_t selecting_row(int t, const int32_t* __restrict__ n_valid,
+                                                 bool n_from_pos, int64_t max_len, int64_t ld, int K,
+                                                 const int32_t* __restrict__ cu_q,
+                                                 const int32_t* __restrict__ cu_k, int B) {
+    const int64_t n = (int64_t)__ldg(n_valid + t) + (n_from_pos ? 1 : 0);
+    bool bad = n < 0 || n > max_len || n > ld;
+    if (cu_q != nullptr) {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+        }
+        const int64_t len_k = (int64_t)__ldg(cu_k + lo + 1) - __ldg(cu_k + lo);
+        bad = bad || n < 1 || n > len_k;
+    }
+    return (bad || n <= K) ? -1 : n;
+}
+
+// Bits of the 4 positions held by each lane (4 consecutive positions per lane,
+// lanes in order) gathered into the 32-bit word of their 32-position group:
+// lanes 8j..8j+7 hold word j of the warp's 128 positions; returns that word
+// in every lane of the group.
+__device__ __forceinline__ uint32_t word_of_masks(uint32_t mask4) {
+    const int lane = threadIdx.x & 31;
+    uint32_t v = mask4 << ((lane & 7) * 4);
+    v |= __shfl_xor_sync(0xffffffffu, v, 1);
+    v |= __shfl_xor_sync(0xffffffffu, v, 2);
+    v |= __shfl_xor_sync(0xffffffffu, v, 4);
+    return v;
+}
+
+__global__ void __launch_bounds__(kSplitThreads)
+topk_split_hist_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
+                       bool n_from_pos, int64_t max_len, int K, const int32_t* __restrict__ cu_q,
+                       const int32_t* __restrict__ cu_k, int B, int slices, uint32_t* scratch,
+                       int32_t T, int64_t nw_cap) {
+    __shared__ uint32_t hist[4096];
+    const int t = blockIdx.x / slices, sl = blockIdx.x % slices;
+    const int64_t n64 = selecting_row(t, n_valid, n_from_pos, max_len, ld, K, cu_q, cu_k, B);
+    const int32_t p0 = sl * kSplitSlice;
+    if (n64 < 0 || p0 >= n64) return;                       // block-uniform
+    const int32_t p1 = (int32_t)(n64 < p0 + kSplitSlice ? n64 : p0 + kSplitSlice);
+    const SplitScratch sc = split_scratch(scratch, T, nw_cap);
+    zero<kSplitThreads>(hist, 4096);
+    __syncthreads();
+    const float* row = scores + (int64_t)t * ld;
+    const int32_t v0 = p0 >> 2, v1 = p1 >> 2;               // whole vectors, then the tail
+    for (int32_t vb = v0; vb < v1; vb += kUnroll * kSplitThreads) {
+        uint4 k[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int32_t v = vb + u * kSplitThreads + threadIdx.x;
+            if (v < v1) k[u] = gkeys(row, v);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (vb + u * kSplitThreads + threadIdx.x >= v1) break;
+            atomicAdd(&hist[k[u].x >> 20], 1u);
+            atomicAdd(&hist[k[u].y >> 20], 1u);
+            atomicAdd(&hist[k[u].z >> 20], 1u);
+            atomicAdd(&hist[k[u].w >> 20], 1u);
+        }
+    }
+    if (threadIdx.x < p1 - (v1 << 2)) atomicAdd(&hist[fkey(__ldg(row + (v1 << 2) + threadIdx.x)) >> 20], 1u);
+    __syncthreads();
+    uint32_t* g = sc.hist1 + (size_t)t * 4096;
+    for (int b = threadIdx.x; b < 4096; b += kSplitThreads)
+        if (hist[b]) atomicAdd(g + b, hist[b]);
+}
+
+__global__ void __launch_bounds__(kSplitThreads)
+topk_split_mark_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
+                       bool n_from_pos, int64_t max_len, int K, const int32_t* __restrict__ cu_q,
+                       const int32_t* __restrict__ cu_k, int B, int slices, uint32_t* scratch,
+                       int32_t T, int64_t nw_cap) {
+    using S = TopkSmem<kSplitThreads, 12>;
+    __shared__ S sh;
+    __shared__ uint32_t hist2[1024];
+    const int t = blockIdx.x / slices, sl = blockIdx.x % slices;
+    const int64_t n64 = selecting_row(t, n_valid, n_from_pos, max_len, ld, K, cu_q, cu_k, B);
+    const int32_t p0 = sl * kSplitSlice;
+    if (n64 < 0 || p0 >= n64) return;                       // block-uniform
+    const int32_t n = (int32_t)n64;
+    const int32_t p1 = n < p0 + kSplitSlice ? n : p0 + kSplitSlice;
+    const SplitScratch sc = split_scratch(scratch, T, nw_cap);
+    const uint32_t* g1 = sc.hist1 + (size_t)t * 4096;
+    for (int b = threadIdx.x; b < 4096; b += kSplitThreads) sh.hist[b] = g1[b];
+    zero<kSplitThreads>(hist2, 1024);
+    __syncthreads();
+    select_bin<kSplitThreads>(sh, 4096, (uint32_t)K);
+    const uint32_t b1 = sh.sel_bin;
+
+    uint32_t* above = sc.bits + (size_t)t * 3 * nw_cap;
+    uint32_t* tie = above + nw_cap;
+    uint32_t* cand = tie + nw_cap;
+    const float* row = scores + (int64_t)t * ld;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kSplitThreads / 32;
+    // each warp: 128 consecutive positions per step (4 per lane), 4 steps in flight
+    for (int32_t c0 = p0 + warp * 128; c0 < p1; c0 += kWarps * 128 * kUnroll) {
+        float4 x[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int32_t p = c0 + u * kWarps * 128 + 4 * lane;
+            x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p + 3 < p1) x[u] = __ldg(reinterpret_cast<const float4*>(row + p));
+            else if (p < p1) {
+                x[u].x = __ldg(row + p);
+                if (p + 1 < p1) x[u].y = __ldg(row + p + 1);
+                if (p + 2 < p1) x[u].z = __ldg(row + p + 2);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int32_t cb = c0 + u * kWarps * 128;          // warp-uniform
+            if (cb >= p1) break;
+            const int32_t p = cb + 4 * lane;
+            const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+            uint32_t ma = 0, mc = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (p + j >= p1) break;
+                const uint32_t kk = fkey(xs[j]);
+                const uint32_t d = kk >> 20;
+                ma |= (d > b1 ? 1u : 0u) << j;
+                if (d == b1) {
+                    mc |= 1u << j;
+                    atomicAdd(&hist2[(kk >> 10) & 1023u], 1u);
+                }
+            }
+            const uint32_t wa = word_of_masks(ma), wc = word_of_masks(mc);
+            if ((lane & 7) == 0) {
+                const int32_t w = (cb >> 5) + (lane >> 3);
+                if ((w << 5) < p1) {
+                    above[w] = wa;
+                    cand[w] = wc;
+                    tie[w] = 0u;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    uint32_t* g2 = sc.hist2 + (size_t)t * 1024;
+    for (int b = threadIdx.x; b < 1024; b += kSplitThreads)
+        if (hist2[b]) atomicAdd(g2 + b, hist2[b]);
+}
+
+__global__ void __launch_bounds__(kFinishThreads)
+topk_split_finish_kernel(const float* __restrict__ scores, int64_t ld,
+                         const int32_t* __restrict__ n_valid, bool n_from_pos, int T,
+                         int64_t max_len, int K, int32_t* __restrict__ idx,
+                         int32_t* __restrict__ cnt, DeviceStatus* status,
+                         const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B,
+                         uint32_t* scratch, int64_t nw_cap) {
+    using S = TopkSmem<kFinishThreads, 12>;
+    __shared__ S sh;
+    extern __shared__ __align__(16) uint32_t dyn_list[];   // [kFinishCand] keys, positions
+    uint32_t* cand_key = dyn_list;
+    int32_t* cand_pos = reinterpret_cast<int32_t*>(dyn_list + kFinishCand);
+    const int t = blockIdx.x;
+    int32_t* out = idx + (int64_t)t * K;
+    const int64_t n64 = row_prologue<kFinishThreads>(t, n_valid, n_from_pos, max_len, ld, K, out,
+                                                     cnt, status, cu_q, cu_k, B);
+    if (n64 < 0) return;
+    const int32_t n = (int32_t)n64;
+    const int32_t nw = (n + 31) >> 5;
+    const SplitScratch sc = split_scratch(scratch, T, nw_cap);
+    const float* row = scores + (int64_t)t * ld;
+    uint32_t* above = sc.bits + (size_t)t * 3 * nw_cap;
+    uint32_t* tie = above + nw_cap;
+    const uint32_t* cand = tie + nw_cap;
+
+    // digit 1 and digit 2 from the row histograms
+    const uint32_t* g1 = sc.hist1 + (size_t)t * 4096;
+    for (int b = threadIdx.x; b < 4096; b += kFinishThreads) sh.hist[b] = g1[b];
+    __syncthreads();
+    select_bin<kFinishThreads>(sh, 4096, (uint32_t)K);
+    uint32_t prefix = sh.sel_bin << 20;
+    uint32_t rank = sh.sel_rank;
+    const uint32_t* g2 = sc.hist2 + (size_t)t * 1024;
+    for (int b = threadIdx.x; b < 1024; b += kFinishThreads) sh.hist[b] = g2[b];
+    __syncthreads();
+    select_bin<kFinishThreads>(sh, 1024, rank);
+    prefix |= sh.sel_bin << 10;
+    rank = sh.sel_rank;
+
+    // list the candidates' positions in shared memory (block scan of counts)
+    const int32_t per = (nw + kFinishThreads - 1) / kFinishThreads;
+    const int32_t w0 = threadIdx.x * per, w1 = w0 + per < nw ? w0 + per : nw;
+    uint32_t mine = 0;
+    for (int32_t w = w0; w < w1; ++w) mine += __popc(cand[w]);
+    const uint32_t off = block_excl_scan<kFinishThreads>(sh, mine);
+    if (threadIdx.x == kFinishThreads - 1) sh.cand_count = off + mine;
+    __syncthreads();
+    const uint32_t n_cand = sh.cand_count;
+    const bool listed = n_cand <= (uint32_t)kFinishCand;
+    if (listed) {
+        uint32_t slot = off;
+        for (int32_t w = w0; w < w1; ++w)
+            for (uint32_t m = cand[w]; m; m &= m - 1u) cand_pos[slot++] = (w << 5) + (__ffs(m) - 1);
+    }
+    __syncthreads();
+    // their keys, loads batched; digit 3 over them
+    zero<kFinishThreads>(sh.hist, 1024);
+    __syncthreads();
+    if (listed) {
+        for (uint32_t i0 = threadIdx.x; i0 < n_cand; i0 += 4 * kFinishThreads) {
+            float x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t i = i0 + u * kFinishThreads;
+                x[u] = i < n_cand ? __ldg(row + cand_pos[i]) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t i = i0 + u * kFinishThreads;
+                if (i >= n_cand) break;
+                const uint32_t kk = fkey(x[u]);
+                cand_key[i] = kk;
+                if ((kk & 0xFFFFFC00u) == prefix) atomicAdd(&sh.hist[kk & 1023u], 1u);
+            }
+        }
+    } else {   // very many candidates: walk the bitmap, gathering per word
+        for (int32_t w = threadIdx.x; w < nw; w += kFinishThreads) {
+            for (uint32_t m = cand[w]; m; m &= m - 1u) {
+                const uint32_t kk = fkey(__ldg(row + (w << 5) + (__ffs(m) - 1)));
+                if ((kk & 0xFFFFFC00u) == prefix) atomicAdd(&sh.hist[kk & 1023u], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    select_bin<kFinishThreads>(sh, 1024, rank);
+    const uint32_t tau = prefix | sh.sel_bin;
+    const uint32_t need = sh.sel_rank;
+    const uint32_t n_above = (uint32_t)K - need;
+
+    // mark candidates above tau (above bits) and equal to tau (tie bits), then emit
+    if (listed) {
+        for (uint32_t i = threadIdx.x; i < n_cand; i += kFinishThreads) {
+            const uint32_t kk = cand_key[i];
+            if (kk > tau) set_bit(above, cand_pos[i]);
+            else if (kk == tau) set_bit(tie, cand_pos[i]);
+        }
+    } else {   // this thread owns word w
+        for (int32_t w = threadIdx.x; w < nw; w += kFinishThreads) {
+            uint32_t m = cand[w];
+            if (!m) continue;
+            uint32_t a = 0, e = 0;
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1u;
+                const uint32_t kk = fkey(__ldg(row + (w << 5) + b));
+                a |= (kk > tau ? 1u : 0u) << b;
+                e |= (kk == tau ? 1u : 0u) << b;
+            }
+            above[w] |= a;
+            tie[w] = e;
+        }
+    }
+    __syncthreads();
+    emit_ordered<kFinishThreads>(sh, above, tie, nw, out, n_above, need);
+    if (cnt && threadIdx.x == 0) cnt[t] = K;
+}
+
 // Shared memory a block may use in total (GB300 opt-in limit, 227 KB), and a
 // bound on the streamed kernel's static part (histogram, scans, counters, with
 // alignment padding).
@@ -497,9 +836,26 @@ bool bitmaps_fit_in_smem(int64_t row_cap) {
 
 }  // namespace
 
+static bool uses_split(const TopkArgs& a) {
+    const int64_t row_cap = a.max_len < a.ld ? a.max_len : a.ld;
+    return a.T > 0 && a.T <= kSplitMaxRows && row_cap > kStageCap && a.bits_scratch != nullptr;
+}
+
+uint32_t* topk_split_row_hist(const TopkArgs& a) { return uses_split(a) ? a.bits_scratch : nullptr; }
+
+cudaError_t topk_prepare(TopkArgs* a, cudaStream_t stream) {
+    if (!uses_split(*a) || a->hist_state != 0) return cudaSuccess;
+    cudaError_t e = cudaMemsetAsync(a->bits_scratch, 0, split_hist_bytes(a->T), stream);
+    if (e == cudaSuccess) a->hist_state = 1;
+    return e;
+}
+
 size_t topk_scratch_bytes(int32_t T, int64_t max_len) {
-    if (T <= 0 || max_len <= kStageCap || bitmaps_fit_in_smem(max_len)) return 0;
-    return (size_t)kScratchBlocks * 3 * (size_t)((max_len + 31) / 32) * 4;
+    if (T <= 0 || max_len <= kStageCap) return 0;
+    const size_t nw_cap = (size_t)((max_len + 31) / 32);
+    if (T <= kSplitMaxRows) return split_hist_bytes(T) + (size_t)T * 3 * nw_cap * 4;
+    if (bitmaps_fit_in_smem(max_len)) return 0;
+    return (size_t)kScratchBlocks * 3 * nw_cap * 4;
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
@@ -517,6 +873,31 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
         kern<<<grid, kStagedThreads, smem, stream>>>(a.scores, a.ld, a.n_valid, a.n_from_pos, a.T,
                                                      a.max_len, a.topk, a.idx, a.cnt, a.status,
                                                      a.cu_q, a.cu_k, a.B, stage);
+    } else if (a.T <= kSplitMaxRows) {
+        if (a.bits_scratch == nullptr) return cudaErrorInvalidValue;
+        if (a.hist_state == 0) {
+            cudaError_t e = cudaMemsetAsync(a.bits_scratch, 0, split_hist_bytes(a.T), stream);
+            if (e != cudaSuccess) return e;
+        }
+        const int slices = (int)((row_cap + kSplitSlice - 1) / kSplitSlice);
+        const int64_t blocks = (int64_t)a.T * slices;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+        if (a.hist_state != 2) {   // the scorer did not histogram the rows
+            topk_split_hist_kernel<<<(unsigned)blocks, kSplitThreads, 0, stream>>>(
+                a.scores, a.ld, a.n_valid, a.n_from_pos, a.max_len, a.topk, a.cu_q, a.cu_k, a.B,
+                slices, a.bits_scratch, a.T, nw_cap);
+            count_launch();
+        }
+        topk_split_mark_kernel<<<(unsigned)blocks, kSplitThreads, 0, stream>>>(
+            a.scores, a.ld, a.n_valid, a.n_from_pos, a.max_len, a.topk, a.cu_q, a.cu_k, a.B, slices,
+            a.bits_scratch, a.T, nw_cap);
+        const int64_t list_bytes = (int64_t)kFinishCand * 8;
+        cudaError_t e2 = ensure_smem_optin((const void*)topk_split_finish_kernel, list_bytes);
+        if (e2 != cudaSuccess) return e2;
+        topk_split_finish_kernel<<<a.T, kFinishThreads, (size_t)list_bytes, stream>>>(
+            a.scores, a.ld, a.n_valid, a.n_from_pos, a.T, a.max_len, a.topk, a.idx, a.cnt, a.status,
+            a.cu_q, a.cu_k, a.B, a.bits_scratch, nw_cap);
+        count_launch();
     } else {
         const bool in_smem = bitmaps_fit_in_smem(row_cap);
         if (!in_smem && a.bits_scratch == nullptr) return cudaErrorInvalidValue;

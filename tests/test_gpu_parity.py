@@ -285,6 +285,13 @@ def test_indexer_history_lengths_around_tiles_and_budget(B, L):
     _check_exact(B, w)
 
 
+def test_indexer_few_chunk_queries_with_long_histories(B):
+    # many queries per sequence (tensor-core prefill tiles) but few rows in all:
+    # the few-rows selection path, with its own histogram pass
+    w = wl.custom(401, q_counts=[60, 40], k_lens=[20000, 15000], kind="int2")
+    _check_exact(B, w)
+
+
 def test_indexer_batch_with_empty_sequences(B):
     w = wl.custom(301, q_counts=[0, 4, 0, 2, 0], k_lens=[0, 2500, 10, 3000, 0], kind="int2")
     _check_exact(B, w)

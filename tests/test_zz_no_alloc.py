@@ -59,8 +59,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(L):
     # call 1: integer inputs with heavy ties (bit-exact bar); call 2: a different,
     # smaller real-valued batch that reuses the shared scratch after call 1.
     w1 = wl.custom(901, q_counts=[40, 3], k_lens=[3000, 2600], kind="int2")
-    w2 = wl.custom(902, q_counts=[1, 1, 1, 5], k_lens=[5000, 2049, 7, 4100], kind="normal",
-                   positions="random")
+    # (call 2 is decode-shaped: few queries with long histories)
+    w2 = wl.custom(902, q_counts=[1, 1, 1, 2], k_lens=[20000, 2049, 7, 14000], kind="normal")
     for w in (w1, w2):
         d = to_device(w)
         idx_a, cnt_a = _noalloc(L, d, w.T, w.B, w.max_len, w.topk)
