@@ -108,6 +108,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+def dram_traffic(workload: int, kernel: str):
+    """DRAM bytes per launch of `kernel` from the ncu capture recorded in
+    profiles/dram_traffic.json, or None when there is none or when the kernel's
+    source file changed since the capture (sha256 recorded with it)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(wl.NAMES[workload], {}).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "sparse_attention_key_gb300", "csrc", rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["sha256"]:
+        return None
+    return rec["bytes_per_launch"]
+
+
 # ---------------------------------------------------------------------------
 # algorithmic work per launch
 # ---------------------------------------------------------------------------
@@ -120,7 +137,8 @@ def algorithmic(w: wl.Workload):
         if q1 > q0:
             unique_keys += int(w.q_pos[q0:q1].max()) + 1
     score_bytes = unique_keys * 256 + w.T * (32 * 128 * 2 + 32 * 4)
-    topk_bytes = w.T * w.topk * 4 + w.T * 4
+    # the selection's own minimum: one read of its fp32 score rows, its outputs
+    topk_bytes = 4 * w.pairs + w.T * w.topk * 4 + w.T * 4
     ln_bytes = (w.k_raw.shape[0] * 512 + 2 * 128 * 2) if (w.k is None and w.k_raw is not None) else 0
     return {"flops": 8192.0 * w.pairs, "score_bytes": score_bytes, "topk_bytes": topk_bytes,
             "ln_bytes": ln_bytes, "unique_keys": unique_keys}
@@ -286,18 +304,26 @@ def run_ours(args, rank, world, local_rank):
         "score": {"ms": score_ms, "bytes": alg["score_bytes"], "flops": alg["flops"]},
         "topk": {"ms": topk_ms, "bytes": alg["topk_bytes"]},
     }
-    dominant = max((k_ for k_ in kernels if kernels[k_]["ms"] > 0), key=lambda k_: kernels[k_]["ms"])
     tensor_bound = w.T > w.B * 4   # many queries per sequence: the contraction dominates
-    if dominant == "score" and tensor_bound:
-        ach = alg["flops"] / (score_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_tflops"]}
-    else:
-        by = kernels[dominant]["bytes"]
-        ach = by / (kernels[dominant]["ms"] / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / pk["hbm_gbs"]}
-    roof.update({"kernel": dominant, "traffic": None, "peak_source": pk["source"]})
+
+    def roofline_of(name):
+        kv = kernels[name]
+        if kv["ms"] <= 0:
+            return None
+        if name == "score" and tensor_bound:
+            ach = alg["flops"] / (kv["ms"] / 1e3) / 1e12
+            return {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "ms": kv["ms"]}
+        ach = kv["bytes"] / (kv["ms"] / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"], "ms": kv["ms"]}
+
+    per_kernel = {k_: roofline_of(k_) for k_ in kernels if kernels[k_]["ms"] > 0}
+    dominant = max(per_kernel, key=lambda k_: per_kernel[k_]["ms"])
+    roof = dict(per_kernel[dominant])
+    roof.pop("ms")
+    roof.update({"kernel": dominant, "traffic": dram_traffic(args.workload, dominant),
+                 "peak_source": pk["source"]})
 
     ck = clocks.summary(t_wall0, t_wall2)
     line = {
@@ -314,6 +340,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "kernels_ms": {k_: v["ms"] for k_, v in kernels.items()},
         "roofline": roof,
+        "kernel_rooflines": per_kernel,
         "clocks": ck,
     }
     if args.cpu_baseline:

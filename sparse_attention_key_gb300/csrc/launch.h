@@ -54,9 +54,6 @@ struct ScoreArgs {
     uint32_t* row_hist = nullptr;
 };
 
-// CUDA-core scorer: one thread per key, streams K with 16-byte loads.
-cudaError_t launch_score_simt(const ScoreArgs& a, cudaStream_t stream);
-
 // Tensor-core scorer (tcgen05/TMEM/TMA): a plan kernel, then the persistent
 // scorer. `plan_ws` holds tc_plan_bytes(B, T) bytes of device scratch.
 size_t tc_plan_bytes(int32_t B, int32_t T);
