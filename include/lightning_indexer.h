@@ -195,6 +195,19 @@ IDX_API int32_t idx_version(void);
  */
 IDX_API uint64_t idx_kernel_launches(void);
 
+/*
+ * Test hook for failure detection: sets the bound, in nanoseconds, of every
+ * wait inside the tensor-core scorer (default 2,000,000,000) for launches
+ * enqueued from now on, and returns the previous bound. When a wait runs out
+ * the kernel records IDX_ERR_TIMEOUT in the status word, stops all its roles,
+ * lets copies and tensor-core work already issued finish (within 100 ms),
+ * frees its tensor memory and returns, leaving the CUDA context usable. The
+ * call's later kernels still run on the partly written scores: idx and cnt are
+ * then meaningless, but every write stays inside its buffer. A bound of 0 makes
+ * the first wait that is not already satisfied give up.
+ */
+IDX_API uint64_t idx_set_wait_limit_ns(uint64_t limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

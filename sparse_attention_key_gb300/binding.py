@@ -33,7 +33,7 @@ _lock = threading.Lock()
 EXPORTS = ("idx_key_layernorm", "idx_score", "idx_score_workspace_size", "idx_topk",
            "idx_topk_workspace_size", "idx_score_topk", "idx_score_topk_workspace_size",
            "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches",
-           "idx_score_topk_noalloc")
+           "idx_score_topk_noalloc", "idx_set_wait_limit_ns")
 
 
 class IndexerError(RuntimeError):
@@ -277,3 +277,11 @@ def score_topk_noalloc(q, k, w, q_pos, cu_q, cu_k, max_len: int, topk: int = TOP
     _check(fn(_ptr(q), _ptr(k), _ptr(w), _ptr(q_pos), _ptr(cu_q), _ptr(cu_k), B, T, k.shape[0],
               max_len, topk, _ptr(idx), _ptr(cnt), _stream()), "idx_score_topk_noalloc")
     return idx, cnt
+
+
+def set_wait_limit_ns(limit_ns: int) -> int:
+    """Test hook: bound (ns) of every wait in the tensor-core scorer; returns the old one."""
+    fn = lib().idx_set_wait_limit_ns
+    fn.argtypes = [ctypes.c_uint64]
+    fn.restype = ctypes.c_uint64
+    return int(fn(int(limit_ns)))

@@ -162,6 +162,8 @@ const char* idx_last_error(void) { return g_last_error; }
 
 uint64_t idx_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+uint64_t idx_set_wait_limit_ns(uint64_t limit_ns) { return set_wait_limit_ns(limit_ns); }
+
 idx_status idx_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
                              int ln_dtype, float eps, uint16_t* k_out, int64_t n_rows,
                              void* stream) {

@@ -33,6 +33,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -230,7 +231,12 @@ struct TcCfg {
     static_assert(QROWS % Q_BOX_ROWS == 0, "Q box");
 };
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: no legitimate wait comes close
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s: no legitimate wait comes close
+
+// Bound of every wait in the scorer (idx_set_wait_limit_ns changes it for tests).
+static std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+
+uint64_t set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms to drain after an abort
 
 // Walks the steps [beg, end) of a CTA: which group, which key tile.
@@ -270,7 +276,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                 const float* __restrict__ w, const int32_t* __restrict__ q_pos,
                 const int32_t* __restrict__ cu_k, int64_t max_len, float* __restrict__ scores,
-                int64_t ld, TcPlan plan, DeviceStatus* status, uint32_t* __restrict__ row_hist) {
+                int64_t ld, TcPlan plan, DeviceStatus* status, uint32_t* __restrict__ row_hist,
+                uint64_t wait_ns) {
     using namespace ptx;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_addr(smem_raw) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
@@ -355,7 +362,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
             for (int32_t s = beg; s < end; ++s) {
                 if (s > beg) new_group = cur.advance(s, plan);
                 if (new_group) {
-                    if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, abort_flag, kWaitLimitNs)) {
+                    if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, abort_flag, wait_ns)) {
                         give_up(1);
                         break;
                     }
@@ -369,7 +376,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                                         q_full, half * 64, qrow0 + r);
                     ++q_loads;
                 }
-                if (!mbar_wait(k_empty + stage, phase ^ 1, abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait(k_empty + stage, phase ^ 1, abort_flag, wait_ns)) {
                     give_up(2);
                     break;
                 }
@@ -384,7 +391,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                     phase ^= 1;
                 }
             }
-            if (aborted || *abort_flag) {  // let every copy already issued land
+            // Let every copy this lane issued land before the CTA may exit.
+            // Normally the MMA warp has consumed them all already; after an
+            // abort (here or, later, in another role) some may be in flight.
+            {
                 for (int s = 0; s < C::STAGES; ++s)
                     if (issued[s] > 0) mbar_wait(k_full + s, (issued[s] - 1) & 1, nullptr, kDrainLimitNs);
                 if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, nullptr, kDrainLimitNs);
@@ -403,13 +413,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
             for (int32_t s = beg; s < end && !aborted; ++s) {
                 if (s > beg) new_group = cur.advance(s, plan);
                 if (new_group) {
-                    if (!mbar_wait(q_full, q_uses & 1, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait(q_full, q_uses & 1, abort_flag, wait_ns)) {
                         give_up(3);
                         break;
                     }
                     ++q_uses;
                 }
-                if (!mbar_wait(k_full + stage, phase, abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait(k_full + stage, phase, abort_flag, wait_ns)) {
                     give_up(4);
                     break;
                 }
@@ -417,7 +427,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                 const uint32_t k_addr = k_base + stage * C::K_STAGE;
 #pragma unroll 1
                 for (int sub = 0; sub < C::NSUB; ++sub) {
-                    if (!mbar_wait(acc_empty + acc, aphase ^ 1, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait(acc_empty + acc, aphase ^ 1, abort_flag, wait_ns)) {
                         give_up(5);
                         break;
                     }
@@ -465,7 +475,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         auto epi_sync = [&]() -> bool {
             __syncwarp();
             if (lane == 0) mbar_arrive(epi_bar);
-            const bool ok = mbar_wait(epi_bar, ephase, abort_flag, kWaitLimitNs);
+            const bool ok = mbar_wait(epi_bar, ephase, abort_flag, wait_ns);
             ephase ^= 1;
             if (!ok) give_up(7);
             return ok;
@@ -516,7 +526,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                 const int32_t key = cur.j * 128 + quarter * 32 + lane;
 #pragma unroll 1
                 for (int sub = 0; sub < C::NSUB; ++sub) {
-                    if (!mbar_wait(acc_full + acc, aphase, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait(acc_full + acc, aphase, abort_flag, wait_ns)) {
                         give_up(6);
                         break;
                     }
@@ -628,7 +638,8 @@ static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream
     if (e != cudaSuccess) return e;
     const DeviceInfo& dev = device_info();
     score_tc_kernel<C><<<dev.sm_count, C::THREADS, C::SMEM, stream>>>(
-        tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan, a.status, row_hist);
+        tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan, a.status, row_hist,
+        g_wait_limit_ns.load());
     count_launch();
     return cudaGetLastError();
 }

@@ -195,13 +195,17 @@ __device__ __forceinline__ void set_bit(uint32_t* bits, int64_t pos) {
 }
 
 // Ordered output from the two bitmaps: the set positions of `above` in
-// increasing order to out[0..n_above), then the first `need` set positions of
-// `tie` in increasing order to out[n_above..). Each thread owns a contiguous
+// increasing order to out[0..K-need), then the first `need` set positions of
+// `tie` in increasing order to out[K-need..K). Each thread owns a contiguous
 // range of words; one block scan of packed (above, tie) counts gives offsets.
+// Writes stay inside out[0..K) even when the bitmaps disagree with the counts
+// (scores that an aborted scorer left half-written): surplus positions are
+// dropped.
 template <int THREADS, class S>
 __device__ __forceinline__ void emit_ordered(S& sh, const uint32_t* above, const uint32_t* tie,
-                                             int32_t nw, int32_t* out, uint32_t n_above,
-                                             uint32_t need) {
+                                             int32_t nw, int32_t* out, uint32_t K, uint32_t need) {
+    need = need < K ? need : K;
+    const uint32_t n_above = K - need;
     const int32_t per = (nw + THREADS - 1) / THREADS;
     const int32_t w0 = threadIdx.x * per;
     const int32_t w1 = w0 + per < nw ? w0 + per : nw;
@@ -215,7 +219,7 @@ __device__ __forceinline__ void emit_ordered(S& sh, const uint32_t* above, const
     uint32_t pa = (uint32_t)off, pt = (uint32_t)(off >> 32);
     for (int32_t w = w0; w < w1; ++w) {
         uint32_t m = above[w];
-        while (m) {
+        while (m && pa < n_above) {
             out[pa++] = w * 32 + (__ffs(m) - 1);
             m &= m - 1u;
         }
@@ -350,8 +354,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
             rank = sh.sel_rank;
         }
         const uint32_t tau = prefix;
-        const uint32_t need = rank;                   // tau-valued keys kept
-        const uint32_t n_above = (uint32_t)K - need;  // every key above tau is kept
+        const uint32_t need = rank;   // tau-valued keys kept; every key above tau is kept
 
         // ---- mark: one thread per 32-position word, no atomics
         for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
@@ -369,7 +372,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         __syncthreads();
 
         // ---- emit: above positions ascending, then the first `need` ties ascending
-        emit_ordered<THREADS>(sh, above, tie, nw, out, n_above, need);
+        emit_ordered<THREADS>(sh, above, tie, nw, out, (uint32_t)K, need);
         if (cnt && threadIdx.x == 0) cnt[t] = K;
     }
 }
@@ -492,8 +495,7 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
             rank = sh.sel_rank;
         }
         const uint32_t tau = prefix;
-        const uint32_t need = rank;                   // tau-valued keys kept
-        const uint32_t n_above = (uint32_t)K - need;  // every key above tau is kept
+        const uint32_t need = rank;   // tau-valued keys kept; every key above tau is kept
 
         // ---- mark: candidates above tau -> above bits, equal -> tie bits
         for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
@@ -513,7 +515,7 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         __syncthreads();
 
         // ---- emit
-        emit_ordered<THREADS>(sh, above, tie, nw, out, n_above, need);
+        emit_ordered<THREADS>(sh, above, tie, nw, out, (uint32_t)K, need);
         if (cnt && threadIdx.x == 0) cnt[t] = K;
     }
 }
@@ -793,7 +795,6 @@ topk_split_finish_kernel(const float* __restrict__ scores, int64_t ld,
     select_bin<kFinishThreads>(sh, 1024, rank);
     const uint32_t tau = prefix | sh.sel_bin;
     const uint32_t need = sh.sel_rank;
-    const uint32_t n_above = (uint32_t)K - need;
 
     // mark candidates above tau (above bits) and equal to tau (tie bits), then emit
     if (listed) {
@@ -819,7 +820,7 @@ topk_split_finish_kernel(const float* __restrict__ scores, int64_t ld,
         }
     }
     __syncthreads();
-    emit_ordered<kFinishThreads>(sh, above, tie, nw, out, n_above, need);
+    emit_ordered<kFinishThreads>(sh, above, tie, nw, out, (uint32_t)K, need);
     if (cnt && threadIdx.x == 0) cnt[t] = K;
 }
 

@@ -1,0 +1,54 @@
+"""Failure detection on the GPU without a fault: the scorer's bounded waits.
+
+Every wait inside the tensor-core scorer has a time bound. This test lowers
+the bound to zero through the library's test hook, so the first wait that is
+not already satisfied gives up: the kernel must record IDX_ERR_TIMEOUT in the
+status word, drain its copies and tensor-core work, free its tensor memory and
+return. The test then restores the bound and checks that the same CUDA context
+still computes correct results. No GPU is faulted, trapped or hung.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_key_gb300 import workloads as wl
+from tests._util import to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+IDX_ERR_TIMEOUT = 5
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_attention_key_gb300 import build
+    build.build()
+    from sparse_attention_key_gb300 import binding
+    return binding
+
+
+@pytest.mark.parametrize("shape", ["decode", "prefill"])
+def test_zero_wait_bound_reports_timeout_and_context_survives(B, shape):
+    if shape == "decode":
+        w = wl.custom(701, q_counts=[1, 1, 1], k_lens=[30000, 9000, 20000], kind="int2")
+    else:
+        w = wl.custom(702, q_counts=[300], k_lens=[3000], kind="int2")
+    d = to_device(w)
+    ws = B.workspace(B.score_topk_workspace_size(w.B, w.T, w.max_len), "cuda")
+    old = B.set_wait_limit_ns(0)
+    try:
+        B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len, ws=ws)
+        code, _ = B.get_status(ws)          # synchronises: the kernel returned
+    finally:
+        B.set_wait_limit_ns(old)
+    assert code == IDX_ERR_TIMEOUT
+    # same context, normal bound: a correct result again
+    idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len,
+                            ws=ws)
+    assert B.get_status(ws) == (0, 0)
+    ridx, rcnt, _ = oracle.score_topk(w.q, w.k, w.w, w.q_pos, w.cu_q, w.cu_k, K=2048, threads=8)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt)
