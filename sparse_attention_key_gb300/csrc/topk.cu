@@ -31,10 +31,14 @@
 // A; every later step reads that copy. Long rows (streamed kernel) are read
 // twice from global memory (pass A and the split); the candidates' keys are
 // gathered from global memory again where needed. No block waits on another.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace lidx {
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -824,6 +828,390 @@ topk_split_finish_kernel(const float* __restrict__ scores, int64_t ld,
     if (cnt && threadIdx.x == 0) cnt[t] = K;
 }
 
+// ---------------------------------------------------------------------------
+// Few long rows: one cluster of C CTAs per row (C = 8, 4 or 2, chosen so that
+// all rows fit in one wave). CTA r owns the slice [r*sl, (r+1)*sl) of the row
+// (sl = ceil(n/C) rounded up to 128) and keeps that slice's above / tie / cand
+// bitmaps and candidate list in its own shared memory.
+//   digit 1  from hist1[t] (the scorer's epilogue histogram), or counted over
+//            the slices and summed in the leader CTA (rank 0) through
+//            distributed shared memory (DSMEM).
+//   split    one pass over the slice. Lane l of a warp takes positions
+//            cb + l + 32j of a 128-position chunk, so the warp's ballot of a
+//            predicate is directly the bitmap word of positions
+//            cb + 32j .. cb + 32j + 31. Scores are compared with the float
+//            bounds of bin b1 (no key arithmetic for non-candidates).
+//            Candidates (keys, positions) go to the CTA's list.
+//   select   normally the leader gathers every CTA's candidate keys through
+//            DSMEM, finds digits 2 and 3 alone, counts per CTA the candidates
+//            above and equal to tau, and writes tau, need and each CTA's
+//            output offsets into that CTA's shared memory. When a list
+//            overflows (a large tie group), the CTAs instead sum their digit
+//            counts in the leader and each walks its own cand bitmap.
+//   emit     each CTA marks its candidates and writes its own positions at
+//            its offsets: above positions first, then the first `need` tie
+//            positions, both in increasing order across the cluster.
+// ---------------------------------------------------------------------------
+constexpr int kClusterMax = 8;
+constexpr int kClThreads = 512;
+constexpr int kClCand = 2048;            // candidates listed per CTA
+constexpr int kClGather = 8192;          // candidate keys the leader gathers
+constexpr int64_t kClSliceCap = 262144;  // longest slice (bitmaps in shared memory)
+constexpr int64_t kClusterRowCap = kClusterMax * kClSliceCap;   // longest row of the cluster kernel
+
+struct ClusterTopkSmem : TopkSmem<kClThreads, 12> {
+    uint32_t h2[1024];                 // this CTA's candidates: second-digit counts
+    uint32_t h3[1024];                 // this CTA's candidates: third-digit counts
+    uint32_t m2[1024];                 // leader: the cluster's second-digit counts
+    uint32_t m3[1024];                 // leader: the cluster's third-digit counts
+    uint32_t n_above_b1;               // positions of this slice above bin b1
+    uint32_t cta_cand[kClusterMax];    // every CTA's candidate count
+    uint32_t cta_above[kClusterMax];   // every CTA's count above b1
+    uint32_t ext_above[kClusterMax];   // leader: candidates above tau per CTA
+    uint32_t ext_tie[kClusterMax];     // leader: candidates equal to tau per CTA
+    uint32_t n_above[kClusterMax];     // leader (overflow path): marked positions per CTA
+    uint32_t n_tie[kClusterMax];
+    uint32_t tau, need, a_off, t_off;  // written by the leader
+};
+
+// Smallest non-NaN float whose order key is >= z (keys are monotone in the
+// value, with -0 == +0): every float if z is at or below the key of -inf; no
+// float (NaN, so that every comparison is false) if z is above the key of
+// +inf. Otherwise the float whose key is exactly z: positive for
+// z >= 0x80000000, negative below (z is never 0x7FFFFFFF, the key -0 would
+// have before folding). For non-NaN x: fkey(x) >= z  <=>  x >= key_floor(z),
+// denormals included (no flush to zero in this library).
+__device__ __forceinline__ float key_floor(uint64_t z) {
+    if (z <= 0x007FFFFFull) return -__int_as_float(0x7f800000);
+    if (z > 0xFF800000ull) return __int_as_float(0x7fffffff);
+    const uint32_t zz = (uint32_t)z;
+    return __uint_as_float(zz >= 0x80000000u ? (zz ^ 0x80000000u) : ~zz);
+}
+
+__global__ void __launch_bounds__(kClThreads)
+topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
+                    const int32_t* __restrict__ n_valid, bool n_from_pos, int64_t max_len, int K,
+                    int32_t* __restrict__ idx, int32_t* __restrict__ cnt, DeviceStatus* status,
+                    const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B,
+                    const uint32_t* __restrict__ hist1, int32_t nw_slice_cap) {
+    __shared__ ClusterTopkSmem sh;
+    extern __shared__ __align__(16) uint32_t dyn_cl[];
+    uint32_t* cand_key = dyn_cl;
+    int32_t* cand_pos = reinterpret_cast<int32_t*>(dyn_cl + kClCand);
+    uint32_t* g_key = dyn_cl + 2 * kClCand;          // leader: gathered keys
+    uint32_t* above = g_key + kClGather;
+    uint32_t* tie = above + nw_slice_cap;
+    uint32_t* cand = tie + nw_slice_cap;
+    cg::cluster_group cl = cg::this_cluster();
+    const int C = (int)cl.num_blocks();
+    const int r = (int)cl.block_rank();
+    const int t = blockIdx.x / C;
+    int32_t* out = idx + (int64_t)t * K;
+    // every CTA of the cluster takes the same decision; only the leader writes
+    // the output of a bad or dormant row
+    const int64_t n64 = r == 0 ? row_prologue<kClThreads>(t, n_valid, n_from_pos, max_len, ld, K,
+                                                          out, cnt, status, cu_q, cu_k, B)
+                               : selecting_row(t, n_valid, n_from_pos, max_len, ld, K, cu_q, cu_k, B);
+    if (n64 < 0) return;   // the whole cluster returns, before any cluster barrier
+    const int32_t n = (int32_t)n64;
+    const int32_t sl = (int32_t)((((int64_t)n + C - 1) / C + 127) / 128 * 128);
+    const int32_t p0 = (int32_t)((int64_t)r * sl < n ? (int64_t)r * sl : n);
+    const int32_t p1 = (int32_t)((int64_t)p0 + sl < n ? (int64_t)p0 + sl : n);
+    const int32_t nwl = (p1 - p0 + 31) >> 5;          // this slice's bitmap words
+    const float* row = scores + (int64_t)t * ld;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kClThreads / 32;
+    ClusterTopkSmem* lead = cl.map_shared_rank(&sh, 0);
+
+    zero<kClThreads>(sh.h2, 1024);
+    zero<kClThreads>(sh.h3, 1024);
+    zero<kClThreads>(sh.m2, 1024);
+    zero<kClThreads>(sh.m3, 1024);
+    if (threadIdx.x < kClusterMax) {
+        sh.ext_above[threadIdx.x] = 0;
+        sh.ext_tie[threadIdx.x] = 0;
+        sh.n_above[threadIdx.x] = 0;
+        sh.n_tie[threadIdx.x] = 0;
+    }
+    if (threadIdx.x == 0) {
+        sh.cand_count = 0;
+        sh.n_above_b1 = 0;
+    }
+    if (hist1 != nullptr) {
+        const uint32_t* g1 = hist1 + (size_t)t * 4096;
+        for (int b = threadIdx.x; b < 4096; b += kClThreads) sh.hist[b] = g1[b];
+    } else {
+        zero<kClThreads>(sh.hist, 4096);
+    }
+    __syncthreads();
+    cl.sync();   // every CTA has started and zeroed what the others add into
+
+    if (hist1 == nullptr) {   // digit 1: count the slice, sum in the leader
+        // a non-empty slice starts at a multiple of 128; an empty one (p0 == n)
+        // must not round p0 down into the previous slice
+        const int32_t v_end = p0 < p1 ? (p1 + 3) >> 2 : (p0 >> 2);
+        for (int32_t v = (p0 >> 2) + threadIdx.x; v < v_end; v += kClThreads) {
+            const int32_t p = v << 2;
+            if (p + 3 < p1) {
+                const uint4 k = gkeys(row, v);
+                atomicAdd(&sh.hist[k.x >> 20], 1u);
+                atomicAdd(&sh.hist[k.y >> 20], 1u);
+                atomicAdd(&sh.hist[k.z >> 20], 1u);
+                atomicAdd(&sh.hist[k.w >> 20], 1u);
+            } else {
+                for (int32_t q = p; q < p1; ++q) atomicAdd(&sh.hist[fkey(__ldg(row + q)) >> 20], 1u);
+            }
+        }
+        __syncthreads();
+        if (r != 0)
+            for (int b = threadIdx.x; b < 4096; b += kClThreads)
+                if (sh.hist[b]) atomicAdd(&lead->hist[b], sh.hist[b]);
+        cl.sync();
+        if (r != 0)
+            for (int b = threadIdx.x; b < 4096; b += kClThreads) sh.hist[b] = lead->hist[b];
+        __syncthreads();
+    }
+    select_bin<kClThreads>(sh, 4096, (uint32_t)K);
+    const uint32_t b1 = sh.sel_bin;
+    uint32_t rank = sh.sel_rank;
+    const float f_lo = key_floor((uint64_t)b1 << 20);          // bin b1 or above
+    const float f_hi = key_floor((uint64_t)(b1 + 1) << 20);    // above bin b1
+
+    // ---- split: one pass over the slice
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    uint32_t my_above = 0;   // lane 0: above-b1 positions seen by this warp
+    for (int32_t c0 = p0 + warp * 128; c0 < p1; c0 += kWarps * 128 * kUnroll) {
+        float x[kUnroll][4];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int32_t p = c0 + u * kWarps * 128 + 32 * j + lane;
+                x[u][j] = p < p1 ? __ldg(row + p) : __int_as_float(0x7fffffff);   // NaN: never kept
+            }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int32_t cb = c0 + u * kWarps * 128;          // warp-uniform
+            if (cb >= p1) break;
+            uint32_t ba[4], bc[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool a = x[u][j] >= f_hi;
+                ba[j] = __ballot_sync(0xffffffffu, a);
+                bc[j] = __ballot_sync(0xffffffffu, !a && x[u][j] >= f_lo);
+            }
+            const int32_t w = (cb - p0) >> 5;                   // p0 is a multiple of 128
+            if (lane < 4 && w + lane < nwl) {
+                above[w + lane] = lane == 0 ? ba[0] : lane == 1 ? ba[1] : lane == 2 ? ba[2] : ba[3];
+                cand[w + lane] = lane == 0 ? bc[0] : lane == 1 ? bc[1] : lane == 2 ? bc[2] : bc[3];
+                tie[w + lane] = 0u;
+            }
+            if (lane == 0) my_above += __popc(ba[0]) + __popc(ba[1]) + __popc(ba[2]) + __popc(ba[3]);
+            if ((bc[0] | bc[1] | bc[2] | bc[3]) != 0u) {      // warp-uniform
+                const uint32_t tot = __popc(bc[0]) + __popc(bc[1]) + __popc(bc[2]) + __popc(bc[3]);
+                uint32_t base = 0;
+                if (lane == 0) base = atomicAdd(&sh.cand_count, tot);
+                base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if ((bc[j] >> lane) & 1u) {
+                        const uint32_t slot = base + __popc(bc[j] & lt_mask);
+                        const uint32_t kk = fkey(x[u][j]);
+                        if (slot < (uint32_t)kClCand) {
+                            cand_key[slot] = kk;
+                            cand_pos[slot] = cb + 32 * j + lane;
+                        }
+                        atomicAdd(&sh.h2[(kk >> 10) & 1023u], 1u);
+                    }
+                    base += __popc(bc[j]);
+                }
+            }
+        }
+    }
+    if (lane == 0 && my_above) atomicAdd(&sh.n_above_b1, my_above);
+    __syncthreads();
+    cl.sync();   // every CTA's bitmaps, list and counts are complete
+
+    if (warp == 0 && lane < C) {
+        const ClusterTopkSmem* rs = cl.map_shared_rank(&sh, lane);
+        sh.cta_cand[lane] = rs->cand_count;
+        sh.cta_above[lane] = rs->n_above_b1;
+    }
+    __syncthreads();
+    uint32_t total_cand = 0;
+    bool fits = true;
+    for (int i = 0; i < C; ++i) {
+        total_cand += sh.cta_cand[i];
+        fits = fits && sh.cta_cand[i] <= (uint32_t)kClCand;
+    }
+    const bool gathered = fits && total_cand <= (uint32_t)kClGather;   // same in every CTA
+    const uint32_t n_cand = sh.cand_count;
+    const bool listed = n_cand <= (uint32_t)kClCand;
+
+    uint32_t tau, need, a_base, t_base;
+    if (gathered) {
+        if (r == 0) {
+            // the cluster's candidate keys, CTA by CTA
+            uint32_t seg[kClusterMax + 1];
+            seg[0] = 0;
+            for (int i = 0; i < C; ++i) seg[i + 1] = seg[i] + sh.cta_cand[i];
+            for (int i = 0; i < C; ++i) {
+                const uint32_t* rk = cl.map_shared_rank(cand_key, i);
+                for (uint32_t e = threadIdx.x; e < sh.cta_cand[i]; e += kClThreads)
+                    g_key[seg[i] + e] = rk[e];
+            }
+            zero<kClThreads>(sh.hist, 1024);
+            __syncthreads();
+            for (uint32_t e = threadIdx.x; e < total_cand; e += kClThreads)
+                atomicAdd(&sh.hist[(g_key[e] >> 10) & 1023u], 1u);
+            __syncthreads();
+            select_bin<kClThreads>(sh, 1024, rank);
+            const uint32_t prefix = (b1 << 20) | (sh.sel_bin << 10);
+            const uint32_t rank3 = sh.sel_rank;
+            __syncthreads();
+            zero<kClThreads>(sh.hist, 1024);
+            __syncthreads();
+            for (uint32_t e = threadIdx.x; e < total_cand; e += kClThreads) {
+                const uint32_t kk = g_key[e];
+                if ((kk & 0xFFFFFC00u) == prefix) atomicAdd(&sh.hist[kk & 1023u], 1u);
+            }
+            __syncthreads();
+            select_bin<kClThreads>(sh, 1024, rank3);
+            const uint32_t tau0 = prefix | sh.sel_bin;
+            const uint32_t need0 = sh.sel_rank < (uint32_t)K ? sh.sel_rank : (uint32_t)K;
+            for (uint32_t e = threadIdx.x; e < total_cand; e += kClThreads) {
+                const uint32_t kk = g_key[e];
+                if (kk < tau0) continue;
+                int i = 0;
+                while (i + 1 < C && e >= seg[i + 1]) ++i;
+                atomicAdd(kk > tau0 ? &sh.ext_above[i] : &sh.ext_tie[i], 1u);
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                uint32_t a = 0, e = 0;
+                for (int i = 0; i < C; ++i) {
+                    ClusterTopkSmem* rs = cl.map_shared_rank(&sh, i);
+                    rs->tau = tau0;
+                    rs->need = need0;
+                    rs->a_off = a;
+                    rs->t_off = e;
+                    a += sh.cta_above[i] + sh.ext_above[i];
+                    e += sh.ext_tie[i];
+                }
+            }
+        }
+        cl.sync();   // tau, need and offsets are in every CTA; no DSMEM access after this
+        tau = sh.tau;
+        need = sh.need;
+        a_base = sh.a_off;
+        t_base = sh.t_off;
+        for (uint32_t i = threadIdx.x; i < n_cand; i += kClThreads) {
+            const uint32_t kk = cand_key[i];
+            if (kk > tau) set_bit(above, cand_pos[i] - p0);
+            else if (kk == tau) set_bit(tie, cand_pos[i] - p0);
+        }
+    } else {
+        // digit 2 from the cluster's summed counts
+        for (int b = threadIdx.x; b < 1024; b += kClThreads)
+            if (sh.h2[b]) atomicAdd(&lead->m2[b], sh.h2[b]);
+        cl.sync();
+        for (int b = threadIdx.x; b < 1024; b += kClThreads) sh.hist[b] = lead->m2[b];
+        __syncthreads();
+        select_bin<kClThreads>(sh, 1024, rank);
+        const uint32_t prefix = (b1 << 20) | (sh.sel_bin << 10);
+        rank = sh.sel_rank;
+        // digit 3 over this slice's candidates that share the first two digits
+        if (listed) {
+            for (uint32_t i = threadIdx.x; i < n_cand; i += kClThreads) {
+                const uint32_t kk = cand_key[i];
+                if ((kk & 0xFFFFFC00u) == prefix) atomicAdd(&sh.h3[kk & 1023u], 1u);
+            }
+        } else {
+            for (int32_t w = threadIdx.x; w < nwl; w += kClThreads)
+                for (uint32_t m = cand[w]; m; m &= m - 1u) {
+                    const uint32_t kk = fkey(__ldg(row + p0 + (w << 5) + (__ffs(m) - 1)));
+                    if ((kk & 0xFFFFFC00u) == prefix) atomicAdd(&sh.h3[kk & 1023u], 1u);
+                }
+        }
+        __syncthreads();
+        for (int b = threadIdx.x; b < 1024; b += kClThreads)
+            if (sh.h3[b]) atomicAdd(&lead->m3[b], sh.h3[b]);
+        cl.sync();
+        for (int b = threadIdx.x; b < 1024; b += kClThreads) sh.hist[b] = lead->m3[b];
+        __syncthreads();
+        select_bin<kClThreads>(sh, 1024, rank);
+        tau = prefix | sh.sel_bin;
+        need = sh.sel_rank < (uint32_t)K ? sh.sel_rank : (uint32_t)K;
+        // mark this slice's candidates
+        if (listed) {
+            for (uint32_t i = threadIdx.x; i < n_cand; i += kClThreads) {
+                const uint32_t kk = cand_key[i];
+                if (kk > tau) set_bit(above, cand_pos[i] - p0);
+                else if (kk == tau) set_bit(tie, cand_pos[i] - p0);
+            }
+        } else {   // this thread owns word w
+            for (int32_t w = threadIdx.x; w < nwl; w += kClThreads) {
+                uint32_t m = cand[w];
+                if (!m) continue;
+                uint32_t a = 0, e = 0;
+                while (m) {
+                    const int b = __ffs(m) - 1;
+                    m &= m - 1u;
+                    const uint32_t kk = fkey(__ldg(row + p0 + (w << 5) + b));
+                    a |= (kk > tau ? 1u : 0u) << b;
+                    e |= (kk == tau ? 1u : 0u) << b;
+                }
+                above[w] |= a;
+                tie[w] = e;
+            }
+        }
+        // per-CTA totals of marked positions, summed in the leader
+        __syncthreads();
+        uint32_t ca = 0, ct = 0;
+        for (int32_t w = threadIdx.x; w < nwl; w += kClThreads) {
+            ca += __popc(above[w]);
+            ct += __popc(tie[w]);
+        }
+        if (ca) atomicAdd(&lead->n_above[r], ca);
+        if (ct) atomicAdd(&lead->n_tie[r], ct);
+        cl.sync();
+        a_base = 0;
+        t_base = 0;
+        for (int i = 0; i < r; ++i) {
+            a_base += lead->n_above[i];
+            t_base += lead->n_tie[i];
+        }
+    }
+    __syncthreads();
+
+    // ---- emit: offsets inside the CTA from a block scan of packed counts
+    const uint32_t n_above_all = (uint32_t)K - need;
+    const int32_t per = (nwl + kClThreads - 1) / kClThreads;
+    const int32_t w0 = threadIdx.x * per < nwl ? threadIdx.x * per : nwl;
+    const int32_t w1 = w0 + per < nwl ? w0 + per : nwl;
+    uint32_t ca = 0, ct = 0;
+    for (int32_t w = w0; w < w1; ++w) {
+        ca += __popc(above[w]);
+        ct += __popc(tie[w]);
+    }
+    const uint64_t off = block_excl_scan64<kClThreads>(sh, (uint64_t)ca | ((uint64_t)ct << 32));
+    uint32_t pa = a_base + (uint32_t)off, pt = t_base + (uint32_t)(off >> 32);
+    for (int32_t w = w0; w < w1; ++w) {
+        uint32_t m = above[w];
+        while (m && pa < n_above_all) {
+            out[pa++] = p0 + w * 32 + (__ffs(m) - 1);
+            m &= m - 1u;
+        }
+        m = tie[w];
+        while (m && pt < need) {
+            out[n_above_all + pt++] = p0 + w * 32 + (__ffs(m) - 1);
+            m &= m - 1u;
+        }
+    }
+    if (r == 0 && cnt && threadIdx.x == 0) cnt[t] = K;
+    if (!gathered) cl.sync();   // the leader's counters were read until here
+}
+
 // Shared memory a block may use in total (GB300 opt-in limit, 227 KB), and a
 // bound on the streamed kernel's static part (histogram, scans, counters, with
 // alignment padding).
@@ -836,6 +1224,16 @@ bool bitmaps_fit_in_smem(int64_t row_cap) {
 }
 
 }  // namespace
+
+// CTAs per row for the cluster kernel: the largest of 8, 4, 2 that keeps all
+// T rows in one wave at two CTAs per SM, raised again (up to 8) while a slice
+// would exceed kClSliceCap positions. Rows up to kClusterRowCap always fit.
+static int cluster_ctas(int32_t T, int64_t row_cap) {
+    const int64_t slots = 2 * (int64_t)(device_info().sm_count > 0 ? device_info().sm_count : 1);
+    int c = (int64_t)T * 8 <= slots ? 8 : (int64_t)T * 4 <= slots ? 4 : 2;
+    while (c < kClusterMax && ((row_cap + c - 1) / c + 127) / 128 * 128 > kClSliceCap) c *= 2;
+    return c;
+}
 
 static bool uses_split(const TopkArgs& a) {
     const int64_t row_cap = a.max_len < a.ld ? a.max_len : a.ld;
@@ -854,7 +1252,8 @@ cudaError_t topk_prepare(TopkArgs* a, cudaStream_t stream) {
 size_t topk_scratch_bytes(int32_t T, int64_t max_len) {
     if (T <= 0 || max_len <= kStageCap) return 0;
     const size_t nw_cap = (size_t)((max_len + 31) / 32);
-    if (T <= kSplitMaxRows) return split_hist_bytes(T) + (size_t)T * 3 * nw_cap * 4;
+    if (T <= kSplitMaxRows)
+        return split_hist_bytes(T) + (max_len <= kClusterRowCap ? 0 : (size_t)T * 3 * nw_cap * 4);
     if (bitmaps_fit_in_smem(max_len)) return 0;
     return (size_t)kScratchBlocks * 3 * nw_cap * 4;
 }
@@ -874,6 +1273,31 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
         kern<<<grid, kStagedThreads, smem, stream>>>(a.scores, a.ld, a.n_valid, a.n_from_pos, a.T,
                                                      a.max_len, a.topk, a.idx, a.cnt, a.status,
                                                      a.cu_q, a.cu_k, a.B, stage);
+    } else if (a.T <= kSplitMaxRows && row_cap <= kClusterRowCap) {
+        const int C = cluster_ctas(a.T, row_cap);
+        const int64_t sl_cap = ((row_cap + C - 1) / C + 127) / 128 * 128;
+        const int32_t nw_slice_cap = (int32_t)(sl_cap / 32);
+        const size_t smem = ((size_t)2 * kClCand + kClGather + 3 * (size_t)nw_slice_cap) * 4;
+        cudaError_t e = ensure_smem_optin((const void*)topk_cluster_kernel,
+                                          ((int64_t)2 * kClCand + kClGather + 3 * (kClSliceCap / 32)) * 4);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(a.T * C));
+        cfg.blockDim = dim3(kClThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const uint32_t* h1 = a.hist_state == 2 ? a.bits_scratch : nullptr;
+        e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a.scores, a.ld, a.n_valid, a.n_from_pos,
+                               a.max_len, a.topk, a.idx, a.cnt, a.status, a.cu_q, a.cu_k, a.B, h1,
+                               nw_slice_cap);
+        if (e != cudaSuccess) return e;
     } else if (a.T <= kSplitMaxRows) {
         if (a.bits_scratch == nullptr) return cudaErrorInvalidValue;
         if (a.hist_state == 0) {

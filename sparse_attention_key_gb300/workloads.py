@@ -238,7 +238,8 @@ def score_rows(seed: int, T: int, n_valid, ld: int, kind: str = "ties") -> np.nd
 
     kind: "ties" (small integers: large tie groups at the boundary), "normal"
     (continuous, mostly distinct), "mixed" (relu-like: ~half exact zeros, the
-    rest continuous, some -0.0), "const" (all equal).
+    rest continuous, some -0.0), "const" (all equal), "tiny" (+-0, +-denormals
+    and the smallest normals, with repeats).
     """
     rng = np.random.default_rng(seed)
     n_valid = np.asarray(n_valid, dtype=np.int64)
@@ -256,6 +257,15 @@ def score_rows(seed: int, T: int, n_valid, ld: int, kind: str = "ties") -> np.nd
             v[neg0 & (v == 0)] = -0.0
         elif kind == "const":
             v = np.full(n, 1.5, dtype=np.float32)
+        elif kind == "tiny":
+            # values around zero: +-0, +-denormals, the smallest normals and a
+            # few ordinary values; many exact repeats
+            pool = np.array([0.0, -0.0, 1e-45, -1e-45, 3e-42, -3e-42, 1.1754942e-38,
+                             -1.1754942e-38, 1.1754944e-38, 2.5e-39, 1.0, -1.0, 5e-40],
+                            dtype=np.float32)
+            v = pool[rng.integers(0, pool.size, size=n)]
+            m = rng.random(n) < 0.3
+            v[m] = (rng.standard_normal(int(m.sum())) * 1e-38).astype(np.float32)
         else:
             raise ValueError(kind)
         S[t, :n] = v

@@ -149,9 +149,9 @@ def test_scores_real_inputs_within_tolerance(B):
 # stand-alone top-K on given fp32 rows: bit-exact
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("kind", ["ties", "normal", "mixed", "const"])
+@pytest.mark.parametrize("kind", ["ties", "normal", "mixed", "const", "tiny"])
 @pytest.mark.parametrize("K", [1, 7, 2048])
-@pytest.mark.parametrize("lens", ["short", "mid", "long"])
+@pytest.mark.parametrize("lens", ["short", "mid", "long", "cap", "over_cap"])
 def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
     rng = np.random.default_rng(zlib.crc32(f"{kind}/{K}/{lens}".encode()))
     if lens == "short":
@@ -160,10 +160,14 @@ def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
     elif lens == "mid":   # many rows of 16K..32K positions: clusters of 2 CTAs
         n_valid = rng.integers(16_000, 30_001, size=400).astype(np.int32)
         n_valid[:3] = [30_000, 16_385, K + 1]
-    else:   # up to 8 x 16K positions (clusters of 8); one row beyond: streamed path
+    elif lens == "long":   # few long rows
         n_valid = np.array([70_000, 131_072, 65_537, K + 3, 100_001], np.int32)
         if kind in ("normal", "ties"):
             n_valid = np.append(n_valid, np.int32(700_001))
+    elif lens == "cap":   # few rows up to exactly 2^21 positions: one cluster per row
+        n_valid = np.array([2_097_152, 12_289, K + 1, 262_145, 131_071], np.int32)
+    else:                 # one position beyond it: the slice-parallel kernels
+        n_valid = np.array([2_097_153, 12_289, 40_000], np.int32)
     max_len = int(n_valid.max())
     ld = (max_len + 3) // 4 * 4
     S = wl.score_rows(int(rng.integers(1 << 30)), n_valid.size, n_valid, ld, kind=kind)
@@ -289,6 +293,13 @@ def test_indexer_few_chunk_queries_with_long_histories(B):
     # many queries per sequence (tensor-core prefill tiles) but few rows in all:
     # the few-rows selection path, with its own histogram pass
     w = wl.custom(401, q_counts=[60, 40], k_lens=[20000, 15000], kind="int2")
+    _check_exact(B, w)
+
+
+def test_indexer_decode_integer_ties_long_histories(B):
+    # one query per sequence (the scorer histograms the first digit itself) on
+    # integer inputs: tie groups far larger than the selection's candidate list
+    w = wl.custom(402, q_counts=[1, 1, 1, 1], k_lens=[40000, 13000, 30000, 12289], kind="int2")
     _check_exact(B, w)
 
 
