@@ -200,9 +200,9 @@ idx_status idx_score(const uint16_t* q, const uint16_t* k, const float* w, const
     if (idx_status st = check_ws(ws, ws_bytes, idx_score_workspace_size(B, T, max_len))) return st;
     if (idx_status st = check_device()) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    if (idx_status st = clear_status(ws, s)) return st;
-    if (T == 0) return IDX_OK;
+    if (T == 0) return clear_status(ws, s);
     ScoreArgs a{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, (DeviceStatus*)ws};
+    a.zero_status = true;   // the plan kernel, first of the call, clears the status word
     cudaError_t e = launch_score_tc(a, (char*)ws + kWsHeader, s);
     return e == cudaSuccess ? IDX_OK : cuda_fail(e, "score launch");
 }
@@ -258,8 +258,7 @@ idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
         return st;
     if (idx_status st = check_device()) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    if (idx_status st = clear_status(ws, s)) return st;
-    if (T == 0) return IDX_OK;
+    if (T == 0) return clear_status(ws, s);
     const int64_t ld = staged_ld(max_len);
     char* base = (char*)ws + kWsHeader + align_up(score_plan_bytes(B, T), 256);
     float* scores = (float*)base;
@@ -268,13 +267,14 @@ idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
     if (topk_scratch_bytes(T, max_len))
         ta.bits_scratch = (uint32_t*)((char*)scores +
                                       align_up((size_t)T * (size_t)ld * sizeof(float), 256));
-    // few long rows: the scorer also histograms the rows for the selection
-    cudaError_t e = topk_prepare(&ta, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(selection histograms)");
     ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, status};
+    // The plan kernel, first of the call, clears the status word and the few-
+    // rows selection histograms (which the scorer's epilogue may fill).
+    sa.zero_status = true;
+    topk_prepare(&ta, &sa.zero_ptr, &sa.zero_bytes);
     sa.row_hist = topk_split_row_hist(ta);
     bool hist_filled = false;
-    e = launch_score_tc(sa, (char*)ws + kWsHeader, s, &hist_filled);
+    cudaError_t e = launch_score_tc(sa, (char*)ws + kWsHeader, s, &hist_filled);
     if (e != cudaSuccess) return cuda_fail(e, "score launch");
     if (hist_filled) ta.hist_state = 2;
     e = launch_topk(ta, s);

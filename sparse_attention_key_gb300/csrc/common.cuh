@@ -37,6 +37,27 @@ __device__ inline void report_error(DeviceStatus* st, int32_t code, int32_t deta
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
 
+// Programmatic dependent launch. Every kernel of this library is launched so
+// that it may start while the previous kernel on the stream is finishing; it
+// calls pdl_wait() before it reads or writes any global data (this returns
+// once every grid it depends on has completed and its writes are visible; at
+// once when there is none), then pdl_launch_dependents() so that the next
+// kernel may be scheduled in turn. Because each kernel waits before it lets
+// the next one start, a kernel's completion implies that of all kernels
+// before it on the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Two fp32 -> packed bf16x2 (lo in bits 0..15), round to nearest even: one
+// hardware conversion (equal to f32_to_bf16_rn on finite inputs).
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2_rn(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 // fp32 -> bf16 bits, round to nearest even (finite inputs).
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
     uint32_t u = __float_as_uint(x);

@@ -31,6 +31,36 @@ cudaError_t ensure_smem_optin(const void* kernel, int64_t bytes);
 // Static shared memory of `kernel` as compiled (bytes), or -1.
 int64_t kernel_static_smem(const void* kernel);
 
+// Launch `kernel` on `stream` as a programmatic dependent launch (it may be
+// scheduled while the previous kernel finishes; the kernel itself waits with
+// pdl_wait() before touching global data), optionally as clusters of
+// `cluster` CTAs along x. Counts the launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, int cluster, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
                                  bool f32_params, float eps, uint16_t* k_out, int64_t n_rows,
                                  cudaStream_t stream);
@@ -50,8 +80,14 @@ struct ScoreArgs {
     int64_t ld;
     DeviceStatus* status;
     // Optional [T][kTopkDigit1Bins] first-digit histograms of the written
-    // scores (zeroed by the caller), filled by scorers that support it.
+    // scores (zeroed before the scorer runs), filled by scorers that support it.
     uint32_t* row_hist = nullptr;
+    // Device memory the plan kernel clears before anything else of the call
+    // runs: the status word (when zero_status) and zero_bytes (a multiple of
+    // 16) at zero_ptr (16-byte aligned; may be NULL).
+    bool zero_status = false;
+    void* zero_ptr = nullptr;
+    size_t zero_bytes = 0;
 };
 
 // Tensor-core scorer (tcgen05/TMEM/TMA): a plan kernel, then the persistent
@@ -94,8 +130,9 @@ size_t topk_scratch_bytes(int32_t T, int64_t max_len);
 // Split path (few long rows): its [T][kTopkDigit1Bins] first-digit row
 // histograms inside bits_scratch, or NULL when the call does not take it.
 uint32_t* topk_split_row_hist(const TopkArgs& a);
-// Zero the split path's row histograms (sets a->hist_state = 1); no-op otherwise.
-cudaError_t topk_prepare(TopkArgs* a, cudaStream_t stream);
+// The split path's row histograms must start at zero: returns the region to
+// clear (and sets a->hist_state = 1), or sets *bytes = 0 when there is none.
+void topk_prepare(TopkArgs* a, void** ptr, size_t* bytes);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
 }  // namespace lidx

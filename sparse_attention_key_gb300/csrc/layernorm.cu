@@ -9,7 +9,10 @@
 // of its 16 lanes owns 8 consecutive features (one 16-byte load and store), and
 // a warp keeps 4 row pairs in flight (64 bytes per lane outstanding) before
 // reducing. Mean and variance are half-warp shuffle reductions (two passes over
-// registers). The grid is persistent: 4 blocks of 8 warps per SM.
+// registers). The grid is persistent: 4 blocks of 8 warps per SM. The
+// arithmetic runs on packed fp32 pairs (FADD2 / FMUL2 / FFMA2), with a hardware
+// rsqrt and packed bf16x2 conversion, to keep the instruction count per row
+// low enough that the kernel is bound by memory rather than issue.
 #include "common.cuh"
 #include "launch.h"
 
@@ -22,19 +25,23 @@ template <bool kF32Params>
 __global__ void __launch_bounds__(kLnWarpsPerBlock * 32)
 key_layernorm_kernel(const uint4* x, const void* __restrict__ ln_w, const void* __restrict__ ln_b,
                      float eps, uint4* y, int64_t n_rows) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;          // which row of the pair
     const int hl = lane & 15;            // lane within the half-warp: features 8*hl .. 8*hl+7
-    float g[8], b[8];
+    float2 g[4], b[4];   // features 8*hl + 2k, 8*hl + 2k + 1
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int d = hl * 8 + j;
+    for (int k = 0; k < 4; ++k) {
+        const int d = hl * 8 + 2 * k;
         if (kF32Params) {
-            g[j] = static_cast<const float*>(ln_w)[d];
-            b[j] = static_cast<const float*>(ln_b)[d];
+            g[k] = make_float2(static_cast<const float*>(ln_w)[d], static_cast<const float*>(ln_w)[d + 1]);
+            b[k] = make_float2(static_cast<const float*>(ln_b)[d], static_cast<const float*>(ln_b)[d + 1]);
         } else {
-            g[j] = __uint_as_float(uint32_t(static_cast<const uint16_t*>(ln_w)[d]) << 16);
-            b[j] = __uint_as_float(uint32_t(static_cast<const uint16_t*>(ln_b)[d]) << 16);
+            const uint16_t* w16 = static_cast<const uint16_t*>(ln_w);
+            const uint16_t* b16 = static_cast<const uint16_t*>(ln_b);
+            g[k] = make_float2(__uint_as_float(uint32_t(w16[d]) << 16), __uint_as_float(uint32_t(w16[d + 1]) << 16));
+            b[k] = make_float2(__uint_as_float(uint32_t(b16[d]) << 16), __uint_as_float(uint32_t(b16[d + 1]) << 16));
         }
     }
     const int64_t warp_id = (int64_t)blockIdx.x * kLnWarpsPerBlock + (threadIdx.x >> 5);
@@ -50,27 +57,36 @@ key_layernorm_kernel(const uint4* x, const void* __restrict__ ln_w, const void* 
 #pragma unroll
         for (int i = 0; i < kLnRowsInFlight; ++i) {
             const int64_t row = r0 + 2 * i + half;
-            float f[8] = {bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y),
-                          bf16_lo(v[i].z), bf16_hi(v[i].z), bf16_lo(v[i].w), bf16_hi(v[i].w)};
-            float s = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+            // packed pairs of features (2k, 2k+1): the two bf16 halves of one word
+            const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            float2 f[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) f[k] = make_float2(bf16_lo(wv[k]), bf16_hi(wv[k]));
+            const float2 s2 = __fadd2_rn(__fadd2_rn(f[0], f[1]), __fadd2_rn(f[2], f[3]));
+            float s = s2.x + s2.y;
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             const float mean = s * (1.0f / kDim);
-            float c[8], ss = 0.f;
+            const float2 nm = make_float2(-mean, -mean);
+            float2 c[4];
+            float2 q = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c[j] = f[j] - mean;
-                ss = fmaf(c[j], c[j], ss);
+            for (int k = 0; k < 4; ++k) {
+                c[k] = __fadd2_rn(f[k], nm);
+                q = __ffma2_rn(c[k], c[k], q);
             }
+            float ss = q.x + q.y;
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float inv = 1.0f / sqrtf(ss * (1.0f / kDim) + eps);
-            uint32_t o16[8];
+            const float inv = rsqrtf(fmaf(ss, 1.0f / kDim, eps));
+            const float2 inv2 = make_float2(inv, inv);
+            uint32_t o16[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o16[j] = f32_to_bf16_rn(fmaf(c[j] * inv, g[j], b[j]));
-            if (row < n_rows)
-                y[row * 16 + hl] = make_uint4(o16[0] | (o16[1] << 16), o16[2] | (o16[3] << 16),
-                                              o16[4] | (o16[5] << 16), o16[6] | (o16[7] << 16));
+            for (int k = 0; k < 4; ++k) {
+                const float2 o = __ffma2_rn(__fmul2_rn(c[k], inv2), g[k], b[k]);
+                o16[k] = f32x2_to_bf16x2_rn(o.x, o.y);
+            }
+            if (row < n_rows) y[row * 16 + hl] = make_uint4(o16[0], o16[1], o16[2], o16[3]);
         }
     }
 }
@@ -85,14 +101,9 @@ cudaError_t launch_key_layernorm(const uint16_t* k_raw, const void* ln_w, const 
     const int grid = (int)(blocks_needed < cap ? blocks_needed : cap);
     const uint4* x = reinterpret_cast<const uint4*>(k_raw);
     uint4* y = reinterpret_cast<uint4*>(k_out);
-    if (f32_params)
-        key_layernorm_kernel<true><<<grid, kLnWarpsPerBlock * 32, 0, stream>>>(x, ln_w, ln_b, eps, y,
-                                                                              n_rows);
-    else
-        key_layernorm_kernel<false><<<grid, kLnWarpsPerBlock * 32, 0, stream>>>(x, ln_w, ln_b, eps, y,
-                                                                               n_rows);
-    count_launch();
-    return cudaGetLastError();
+    return launch_kernel(f32_params ? key_layernorm_kernel<true> : key_layernorm_kernel<false>,
+                         dim3(grid), dim3(kLnWarpsPerBlock * 32), 0, stream, 1, x, ln_w, ln_b, eps, y,
+                         n_rows);
 }
 
 }  // namespace lidx

@@ -124,20 +124,19 @@ extern "C" IDX_API idx_status idx_score_topk_noalloc(
     if (!scratch) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
     cudaStream_t s = (cudaStream_t)stream;
     if (T == 0) return IDX_OK;
-    // Only the status word must start at zero; every staged score is written
-    // before it is read within the same call.
+    // Only the status word and the selection histograms must start at zero
+    // (the plan kernel, first of the call, clears them); every staged score is
+    // written before it is read within the same call.
     DeviceStatus* status = reinterpret_cast<DeviceStatus*>(scratch);
-    e = cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s);
-    if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
     void* plan = scratch + kWsHeader;
     float* scores = reinterpret_cast<float*>(scratch + kWsHeader + kNoAllocPlanBytes);
     TopkArgs ta{scores, ld, q_pos, true, T, max_len, topk, idx, cnt, status, cu_q, cu_k, B};
     if (topk_scratch_bytes(T, max_len))
         ta.bits_scratch = reinterpret_cast<uint32_t*>(scratch + kWsHeader + kNoAllocPlanBytes +
                                                       kNoAllocScoreBytes);
-    e = topk_prepare(&ta, s);   // zeroes the selection histograms when used
-    if (e != cudaSuccess) return noalloc_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
     ScoreArgs sa{q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len, scores, ld, status};
+    sa.zero_status = true;
+    topk_prepare(&ta, &sa.zero_ptr, &sa.zero_bytes);
     sa.row_hist = topk_split_row_hist(ta);
     bool hist_filled = false;
     e = launch_score_tc(sa, plan, s, &hist_filled);

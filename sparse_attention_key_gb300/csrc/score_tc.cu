@@ -106,11 +106,27 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int* warp_sums, int* t
     return res;
 }
 
+// Block 0 builds the plan (after clearing the status word when asked); any
+// further blocks clear `zero_bytes` at `zero_ptr` (the selection histograms
+// that the scorer's epilogue adds into).
 template <int GQ>
 __global__ void __launch_bounds__(kPlanThreads)
 tc_plan_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu_q,
                const int32_t* __restrict__ cu_k, int B, int T, int64_t n_keys, int64_t max_len,
-               TcPlan plan, DeviceStatus* status) {
+               TcPlan plan, DeviceStatus* status, bool zero_status, uint4* zero_ptr,
+               int64_t zero_vec) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x > 0) {
+        for (int64_t i = (int64_t)(blockIdx.x - 1) * kPlanThreads + threadIdx.x; i < zero_vec;
+             i += (int64_t)(gridDim.x - 1) * kPlanThreads)
+            zero_ptr[i] = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    if (zero_status && threadIdx.x == 0) {
+        status->code = 0;
+        status->detail = 0;
+    }
     __shared__ int warp_sums[33];
     __shared__ int overflow;
     if (threadIdx.x == 0) overflow = 0;
@@ -281,6 +297,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
     using namespace ptx;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_addr(smem_raw) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
+        pdl_wait();
         if (threadIdx.x == 0) report_error(status, IDX_ERR_UNSUPPORTED, 1024);
         return;
     }
@@ -334,6 +351,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Set-up above touches only this CTA's shared and tensor memory; the plan,
+    // the inputs and the outputs are used after the previous kernel completes.
+    pdl_wait();
+    pdl_launch_dependents();
 
     const int n_groups = plan.hdr->n_groups;
     const int64_t total = plan.hdr->total_steps;
@@ -629,19 +650,20 @@ static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream
     CUtensorMap tk, tq;
     if (!make_tmap(&tk, a.k, a.n_keys, 128) || !make_tmap(&tq, a.q, (int64_t)a.T * 32, C::Q_BOX_ROWS))
         return cudaErrorInvalidValue;
-    tc_plan_kernel<C::GQ><<<1, kPlanThreads, 0, stream>>>(a.q_pos, a.cu_q, a.cu_k, a.B, a.T,
-                                                          a.n_keys, a.max_len, plan, a.status);
-    count_launch();
-    cudaError_t e = cudaGetLastError();
+    const int64_t zero_vec = a.zero_ptr != nullptr ? (int64_t)(a.zero_bytes / 16) : 0;
+    const int64_t zero_blocks = zero_vec > 0 ? (zero_vec + 4 * kPlanThreads - 1) / (4 * kPlanThreads) : 0;
+    const int plan_grid = 1 + (int)(zero_blocks < 64 ? zero_blocks : 64);
+    cudaError_t e = launch_kernel(tc_plan_kernel<C::GQ>, dim3(plan_grid), dim3(kPlanThreads), 0, stream,
+                                  1, a.q_pos, a.cu_q, a.cu_k, a.B, a.T, a.n_keys, a.max_len, plan,
+                                  a.status, a.zero_status, reinterpret_cast<uint4*>(a.zero_ptr),
+                                  zero_vec);
     if (e != cudaSuccess) return e;
     e = ensure_smem_optin((const void*)score_tc_kernel<C>, C::SMEM);
     if (e != cudaSuccess) return e;
     const DeviceInfo& dev = device_info();
-    score_tc_kernel<C><<<dev.sm_count, C::THREADS, C::SMEM, stream>>>(
-        tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan, a.status, row_hist,
-        g_wait_limit_ns.load());
-    count_launch();
-    return cudaGetLastError();
+    return launch_kernel(score_tc_kernel<C>, dim3(dev.sm_count), dim3(C::THREADS), (size_t)C::SMEM,
+                         stream, 1, tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan,
+                         a.status, row_hist, g_wait_limit_ns.load());
 }
 
 cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream,

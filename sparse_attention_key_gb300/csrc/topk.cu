@@ -279,6 +279,8 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
                    bool n_from_pos, int T, int64_t max_len, int K, int32_t* __restrict__ idx,
                    int32_t* __restrict__ cnt, DeviceStatus* status, const int32_t* __restrict__ cu_q,
                    const int32_t* __restrict__ cu_k, int B, int32_t stage_cap) {
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int D1 = 11;                      // digits: bits 31..21, 20..10, 9..0
     constexpr int kD1Shift = 32 - D1;
     using S = TopkSmem<THREADS, D1>;
@@ -392,6 +394,8 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
                    int32_t* __restrict__ cnt, DeviceStatus* status, const int32_t* __restrict__ cu_q,
                    const int32_t* __restrict__ cu_k, int B, int64_t nw_cap,
                    uint32_t* __restrict__ gbits) {
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int D1 = 12;                      // digits: bits 31..20, 19..10, 9..0
     constexpr int kD1Shift = 32 - D1;
     using S = TopkSmem<THREADS, D1>;
@@ -601,6 +605,8 @@ topk_split_hist_kernel(const float* __restrict__ scores, int64_t ld, const int32
                        bool n_from_pos, int64_t max_len, int K, const int32_t* __restrict__ cu_q,
                        const int32_t* __restrict__ cu_k, int B, int slices, uint32_t* scratch,
                        int32_t T, int64_t nw_cap) {
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ uint32_t hist[4096];
     const int t = blockIdx.x / slices, sl = blockIdx.x % slices;
     const int64_t n64 = selecting_row(t, n_valid, n_from_pos, max_len, ld, K, cu_q, cu_k, B);
@@ -640,6 +646,8 @@ topk_split_mark_kernel(const float* __restrict__ scores, int64_t ld, const int32
                        bool n_from_pos, int64_t max_len, int K, const int32_t* __restrict__ cu_q,
                        const int32_t* __restrict__ cu_k, int B, int slices, uint32_t* scratch,
                        int32_t T, int64_t nw_cap) {
+    pdl_wait();
+    pdl_launch_dependents();
     using S = TopkSmem<kSplitThreads, 12>;
     __shared__ S sh;
     __shared__ uint32_t hist2[1024];
@@ -719,6 +727,8 @@ topk_split_finish_kernel(const float* __restrict__ scores, int64_t ld,
                          int32_t* __restrict__ cnt, DeviceStatus* status,
                          const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B,
                          uint32_t* scratch, int64_t nw_cap) {
+    pdl_wait();
+    pdl_launch_dependents();
     using S = TopkSmem<kFinishThreads, 12>;
     __shared__ S sh;
     extern __shared__ __align__(16) uint32_t dyn_list[];   // [kFinishCand] keys, positions
@@ -894,6 +904,8 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
                     int32_t* __restrict__ idx, int32_t* __restrict__ cnt, DeviceStatus* status,
                     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B,
                     const uint32_t* __restrict__ hist1, int32_t nw_slice_cap) {
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ ClusterTopkSmem sh;
     extern __shared__ __align__(16) uint32_t dyn_cl[];
     uint32_t* cand_key = dyn_cl;
@@ -1242,11 +1254,13 @@ static bool uses_split(const TopkArgs& a) {
 
 uint32_t* topk_split_row_hist(const TopkArgs& a) { return uses_split(a) ? a.bits_scratch : nullptr; }
 
-cudaError_t topk_prepare(TopkArgs* a, cudaStream_t stream) {
-    if (!uses_split(*a) || a->hist_state != 0) return cudaSuccess;
-    cudaError_t e = cudaMemsetAsync(a->bits_scratch, 0, split_hist_bytes(a->T), stream);
-    if (e == cudaSuccess) a->hist_state = 1;
-    return e;
+void topk_prepare(TopkArgs* a, void** ptr, size_t* bytes) {
+    *ptr = nullptr;
+    *bytes = 0;
+    if (!uses_split(*a) || a->hist_state != 0) return;
+    *ptr = a->bits_scratch;
+    *bytes = split_hist_bytes(a->T);
+    a->hist_state = 1;
 }
 
 size_t topk_scratch_bytes(int32_t T, int64_t max_len) {
@@ -1270,9 +1284,10 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
         cudaError_t e = ensure_smem_optin(
             (const void*)kern, (kStageCap + 2 * ((kStageCap + 31) / 32)) * 4);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kStagedThreads, smem, stream>>>(a.scores, a.ld, a.n_valid, a.n_from_pos, a.T,
-                                                     a.max_len, a.topk, a.idx, a.cnt, a.status,
-                                                     a.cu_q, a.cu_k, a.B, stage);
+        e = launch_kernel(kern, dim3(grid), dim3(kStagedThreads), smem, stream, 1, a.scores, a.ld,
+                          a.n_valid, a.n_from_pos, a.T, a.max_len, a.topk, a.idx, a.cnt, a.status,
+                          a.cu_q, a.cu_k, a.B, stage);
+        if (e != cudaSuccess) return e;
     } else if (a.T <= kSplitMaxRows && row_cap <= kClusterRowCap) {
         const int C = cluster_ctas(a.T, row_cap);
         const int64_t sl_cap = ((row_cap + C - 1) / C + 127) / 128 * 128;
@@ -1281,22 +1296,10 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
         cudaError_t e = ensure_smem_optin((const void*)topk_cluster_kernel,
                                           ((int64_t)2 * kClCand + kClGather + 3 * (kClSliceCap / 32)) * 4);
         if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(a.T * C));
-        cfg.blockDim = dim3(kClThreads);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
         const uint32_t* h1 = a.hist_state == 2 ? a.bits_scratch : nullptr;
-        e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a.scores, a.ld, a.n_valid, a.n_from_pos,
-                               a.max_len, a.topk, a.idx, a.cnt, a.status, a.cu_q, a.cu_k, a.B, h1,
-                               nw_slice_cap);
+        e = launch_kernel(topk_cluster_kernel, dim3((unsigned)(a.T * C)), dim3(kClThreads), smem, stream,
+                          C, a.scores, a.ld, a.n_valid, a.n_from_pos, a.max_len, a.topk, a.idx, a.cnt,
+                          a.status, a.cu_q, a.cu_k, a.B, h1, nw_slice_cap);
         if (e != cudaSuccess) return e;
     } else if (a.T <= kSplitMaxRows) {
         if (a.bits_scratch == nullptr) return cudaErrorInvalidValue;
@@ -1308,21 +1311,24 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
         const int64_t blocks = (int64_t)a.T * slices;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
         if (a.hist_state != 2) {   // the scorer did not histogram the rows
-            topk_split_hist_kernel<<<(unsigned)blocks, kSplitThreads, 0, stream>>>(
-                a.scores, a.ld, a.n_valid, a.n_from_pos, a.max_len, a.topk, a.cu_q, a.cu_k, a.B,
-                slices, a.bits_scratch, a.T, nw_cap);
-            count_launch();
+            cudaError_t e = launch_kernel(topk_split_hist_kernel, dim3((unsigned)blocks), dim3(kSplitThreads),
+                                          0, stream, 1, a.scores, a.ld, a.n_valid, a.n_from_pos,
+                                          a.max_len, a.topk, a.cu_q, a.cu_k, a.B, slices,
+                                          a.bits_scratch, a.T, nw_cap);
+            if (e != cudaSuccess) return e;
         }
-        topk_split_mark_kernel<<<(unsigned)blocks, kSplitThreads, 0, stream>>>(
-            a.scores, a.ld, a.n_valid, a.n_from_pos, a.max_len, a.topk, a.cu_q, a.cu_k, a.B, slices,
-            a.bits_scratch, a.T, nw_cap);
+        cudaError_t e1 = launch_kernel(topk_split_mark_kernel, dim3((unsigned)blocks), dim3(kSplitThreads),
+                                       0, stream, 1, a.scores, a.ld, a.n_valid, a.n_from_pos,
+                                       a.max_len, a.topk, a.cu_q, a.cu_k, a.B, slices, a.bits_scratch,
+                                       a.T, nw_cap);
+        if (e1 != cudaSuccess) return e1;
         const int64_t list_bytes = (int64_t)kFinishCand * 8;
         cudaError_t e2 = ensure_smem_optin((const void*)topk_split_finish_kernel, list_bytes);
         if (e2 != cudaSuccess) return e2;
-        topk_split_finish_kernel<<<a.T, kFinishThreads, (size_t)list_bytes, stream>>>(
-            a.scores, a.ld, a.n_valid, a.n_from_pos, a.T, a.max_len, a.topk, a.idx, a.cnt, a.status,
-            a.cu_q, a.cu_k, a.B, a.bits_scratch, nw_cap);
-        count_launch();
+        e2 = launch_kernel(topk_split_finish_kernel, dim3(a.T), dim3(kFinishThreads), (size_t)list_bytes,
+                           stream, 1, a.scores, a.ld, a.n_valid, a.n_from_pos, a.T, a.max_len, a.topk,
+                           a.idx, a.cnt, a.status, a.cu_q, a.cu_k, a.B, a.bits_scratch, nw_cap);
+        if (e2 != cudaSuccess) return e2;
     } else {
         const bool in_smem = bitmaps_fit_in_smem(row_cap);
         if (!in_smem && a.bits_scratch == nullptr) return cudaErrorInvalidValue;
@@ -1333,12 +1339,11 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
         if (st < 0 || st > kStreamStaticBound) return cudaErrorInvalidValue;
         cudaError_t e = ensure_smem_optin((const void*)kern, kBlockSmem - kStreamStaticBound);
         if (e != cudaSuccess) return e;
-        kern<<<g, kStreamThreads, smem, stream>>>(a.scores, a.ld, a.n_valid, a.n_from_pos, a.T,
-                                                  a.max_len, a.topk, a.idx, a.cnt, a.status,
-                                                  a.cu_q, a.cu_k, a.B, nw_cap,
-                                                  in_smem ? nullptr : a.bits_scratch);
+        e = launch_kernel(kern, dim3(g), dim3(kStreamThreads), smem, stream, 1, a.scores, a.ld,
+                          a.n_valid, a.n_from_pos, a.T, a.max_len, a.topk, a.idx, a.cnt, a.status,
+                          a.cu_q, a.cu_k, a.B, nw_cap, in_smem ? nullptr : a.bits_scratch);
+        if (e != cudaSuccess) return e;
     }
-    count_launch();
     return cudaGetLastError();
 }
 
