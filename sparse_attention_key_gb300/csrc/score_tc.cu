@@ -380,6 +380,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
             StepCursor cur;
             cur.init(beg, plan, n_groups);
             bool new_group = true;
+            const uint64_t key_policy = C::GQ == 1 ? l2_policy_evict_first() : 0ull;
             for (int32_t s = beg; s < end; ++s) {
                 if (s > beg) new_group = cur.advance(s, plan);
                 if (new_group) {
@@ -404,8 +405,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                 mbar_arrive_expect_tx(k_full + stage, C::K_STAGE);
                 const int32_t key_row = __ldg(cu_k + cur.desc.x) + cur.j * 128;
                 uint8_t* dst = k_smem + stage * C::K_STAGE;
-                tma_load_2d(smem_addr(dst), &tmap_k, k_full + stage, 0, key_row);
-                tma_load_2d(smem_addr(dst + C::K_HALF), &tmap_k, k_full + stage, 64, key_row);
+                if (C::GQ == 1) {
+                    // one query per group: each key tile is read about once, so
+                    // it should not push the staged scores out of L2
+                    tma_load_2d_hint(smem_addr(dst), &tmap_k, k_full + stage, 0, key_row, key_policy);
+                    tma_load_2d_hint(smem_addr(dst + C::K_HALF), &tmap_k, k_full + stage, 64, key_row,
+                                     key_policy);
+                } else {
+                    tma_load_2d(smem_addr(dst), &tmap_k, k_full + stage, 0, key_row);
+                    tma_load_2d(smem_addr(dst + C::K_HALF), &tmap_k, k_full + stage, 64, key_row);
+                }
                 ++issued[stage];
                 if (++stage == C::STAGES) {
                     stage = 0;

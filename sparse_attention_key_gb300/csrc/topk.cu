@@ -52,10 +52,9 @@ constexpr int kScratchBlocks = 512;         // blocks when the bitmaps live in g
 template <int THREADS, int D1BITS>
 struct TopkSmem {
     static constexpr int kWarps = THREADS / 32;
-    uint32_t hist[1 << D1BITS];
+    alignas(16) uint32_t hist[1 << D1BITS];
     uint32_t scan[THREADS / 32 + 1];
     uint64_t scan64[THREADS / 32];
-    uint32_t super[128];           // sums of 32-bin groups (select_bin)
     uint32_t sel_bin, sel_rank, cand_count;
 };
 
@@ -115,63 +114,44 @@ __device__ __forceinline__ uint64_t block_excl_scan64(S& sh, uint64_t v) {
 
 // The bin (counting from the highest) holding the element of rank `rank`
 // (1-based from the largest) in sh.hist[0..nbins); writes sh.sel_bin and the
-// rank inside that bin to sh.sel_rank. Two levels: the warps sum groups of 32
-// consecutive bins (lanes read consecutive words), then warp 0 finds the group
-// and the bin inside it with warp scans. nbins: 1024, 2048 or 4096.
+// rank inside that bin to sh.sel_rank. Thread j sums the nbins/THREADS bins
+// just below the top j*nbins/THREADS ones; an exclusive block scan of those
+// sums gives every thread the count above its bins, and the one thread whose
+// range holds the rank finds the bin. nbins is a multiple of THREADS. When the
+// histogram holds fewer than `rank` elements (only for inputs outside the
+// contract, such as scores an aborted scorer left half-written), bin 0 and
+// rank 0 are returned.
 template <int THREADS, class S>
 __device__ __forceinline__ void select_bin(S& sh, int nbins, uint32_t rank) {
-    constexpr int W = THREADS / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int ngroups = nbins >> 5;
-    for (int g = warp; g < ngroups; g += W) {
-        uint32_t v = sh.hist[(g << 5) + lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) sh.super[g] = v;
+    const int per = nbins / THREADS;
+    const int top = nbins - 1 - (int)threadIdx.x * per;   // this thread's highest bin
+    uint32_t s = 0;
+    if ((per & 3) == 0) {
+        const uint4* h4 = reinterpret_cast<const uint4*>(sh.hist + (top + 1 - per));
+        for (int i = 0; i < per / 4; ++i) {
+            const uint4 v = h4[i];
+            s += (v.x + v.y) + (v.z + v.w);
+        }
+    } else {
+        for (int i = 0; i < per; ++i) s += sh.hist[top - i];
     }
-    __syncthreads();
-    if (warp == 0) {
-        // lane l owns groups top-per*l .. top-per*l-per+1 (from the highest)
-        const int per = ngroups >> 5;
-        const int top = ngroups - 1 - lane * per;
-        uint32_t sum = 0;
-        for (int i = 0; i < per; ++i) sum += sh.super[top - i];
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += x;
-        }
-        const uint32_t excl = incl - sum;
-        const int src = __ffs(__ballot_sync(0xffffffffu, excl < rank && rank <= incl)) - 1;
-        int grp = 0;
-        uint32_t r = 0;
-        if (lane == src) {
-            uint32_t acc = excl;
-            for (int i = 0; i < per; ++i) {
-                const uint32_t c = sh.super[top - i];
-                if (acc + c >= rank) {
-                    grp = top - i;
-                    r = rank - acc;
-                    break;
-                }
-                acc += c;
+    // (the scan's first barrier also separates the callers' reads of the
+    // previous sel_bin / sel_rank from the writes below)
+    const uint32_t excl = block_excl_scan<THREADS>(sh, s);
+    if (threadIdx.x == THREADS - 1 && excl + s < rank) {   // fewer elements than rank
+        sh.sel_bin = 0;
+        sh.sel_rank = 0;
+    }
+    if (excl < rank && rank <= excl + s) {
+        uint32_t acc = excl;
+        for (int i = 0; i < per; ++i) {
+            const uint32_t c = sh.hist[top - i];
+            if (acc + c >= rank) {
+                sh.sel_bin = (uint32_t)(top - i);
+                sh.sel_rank = rank - acc;
+                break;
             }
-        }
-        grp = __shfl_sync(0xffffffffu, grp, src);
-        r = __shfl_sync(0xffffffffu, r, src);
-        // inside the group: lane l holds bin grp*32 + 31 - l (from the highest)
-        const uint32_t c = sh.hist[(grp << 5) + 31 - lane];
-        uint32_t ci = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_up_sync(0xffffffffu, ci, o);
-            if (lane >= o) ci += x;
-        }
-        const int l2 = __ffs(__ballot_sync(0xffffffffu, ci >= r)) - 1;
-        if (lane == l2) {
-            sh.sel_bin = (uint32_t)((grp << 5) + 31 - l2);
-            sh.sel_rank = r - (ci - c);
+            acc += c;
         }
     }
     __syncthreads();
@@ -881,6 +861,7 @@ struct ClusterTopkSmem : TopkSmem<kClThreads, 12> {
     uint32_t ext_tie[kClusterMax];     // leader: candidates equal to tau per CTA
     uint32_t n_above[kClusterMax];     // leader (overflow path): marked positions per CTA
     uint32_t n_tie[kClusterMax];
+    uint32_t seg[kClusterMax + 1];     // leader: first gathered key of each CTA
     uint32_t tau, need, a_off, t_off;  // written by the leader
 };
 
@@ -904,8 +885,6 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
                     int32_t* __restrict__ idx, int32_t* __restrict__ cnt, DeviceStatus* status,
                     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B,
                     const uint32_t* __restrict__ hist1, int32_t nw_slice_cap) {
-    pdl_wait();
-    pdl_launch_dependents();
     __shared__ ClusterTopkSmem sh;
     extern __shared__ __align__(16) uint32_t dyn_cl[];
     uint32_t* cand_key = dyn_cl;
@@ -919,22 +898,7 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
     const int r = (int)cl.block_rank();
     const int t = blockIdx.x / C;
     int32_t* out = idx + (int64_t)t * K;
-    // every CTA of the cluster takes the same decision; only the leader writes
-    // the output of a bad or dormant row
-    const int64_t n64 = r == 0 ? row_prologue<kClThreads>(t, n_valid, n_from_pos, max_len, ld, K,
-                                                          out, cnt, status, cu_q, cu_k, B)
-                               : selecting_row(t, n_valid, n_from_pos, max_len, ld, K, cu_q, cu_k, B);
-    if (n64 < 0) return;   // the whole cluster returns, before any cluster barrier
-    const int32_t n = (int32_t)n64;
-    const int32_t sl = (int32_t)((((int64_t)n + C - 1) / C + 127) / 128 * 128);
-    const int32_t p0 = (int32_t)((int64_t)r * sl < n ? (int64_t)r * sl : n);
-    const int32_t p1 = (int32_t)((int64_t)p0 + sl < n ? (int64_t)p0 + sl : n);
-    const int32_t nwl = (p1 - p0 + 31) >> 5;          // this slice's bitmap words
-    const float* row = scores + (int64_t)t * ld;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int kWarps = kClThreads / 32;
-    ClusterTopkSmem* lead = cl.map_shared_rank(&sh, 0);
-
+    if (hist1 == nullptr) zero<kClThreads>(sh.hist, 4096);
     zero<kClThreads>(sh.h2, 1024);
     zero<kClThreads>(sh.h3, 1024);
     zero<kClThreads>(sh.m2, 1024);
@@ -944,21 +908,48 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
         sh.ext_tie[threadIdx.x] = 0;
         sh.n_above[threadIdx.x] = 0;
         sh.n_tie[threadIdx.x] = 0;
+        sh.seg[threadIdx.x + 1] = 0;
     }
     if (threadIdx.x == 0) {
         sh.cand_count = 0;
         sh.n_above_b1 = 0;
+        sh.seg[0] = 0;
     }
-    if (hist1 != nullptr) {
-        const uint32_t* g1 = hist1 + (size_t)t * 4096;
-        for (int b = threadIdx.x; b < 4096; b += kClThreads) sh.hist[b] = g1[b];
-    } else {
-        zero<kClThreads>(sh.hist, 4096);
+    // The row check reads only the call's inputs, which the kernels before
+    // this one on the stream no longer write (each waits for its predecessor
+    // before it lets its successor start), so it runs before pdl_wait;
+    // outputs and the scores are touched after it. Every CTA of the cluster
+    // takes the same decision; only the leader writes the output of a bad or
+    // dormant row.
+    const int64_t n64 = selecting_row(t, n_valid, n_from_pos, max_len, ld, K, cu_q, cu_k, B);
+    pdl_wait();
+    pdl_launch_dependents();
+    if (n64 < 0) {   // the whole cluster returns, before any cluster barrier
+        if (r == 0) row_prologue<kClThreads>(t, n_valid, n_from_pos, max_len, ld, K, out, cnt, status,
+                                             cu_q, cu_k, B);
+        return;
     }
+    if (hist1 != nullptr) {   // the row's first-digit histogram, from the scorer
+        const uint4* g1 = reinterpret_cast<const uint4*>(hist1 + (size_t)t * 4096);
+        uint4* h4 = reinterpret_cast<uint4*>(sh.hist);
+        for (int b = threadIdx.x; b < 1024; b += kClThreads) h4[b] = g1[b];
+    }
+    const int32_t n = (int32_t)n64;
+    const int32_t sl = (int32_t)((((int64_t)n + C - 1) / C + 127) / 128 * 128);
+    const int32_t p0 = (int32_t)((int64_t)r * sl < n ? (int64_t)r * sl : n);
+    const int32_t p1 = (int32_t)((int64_t)p0 + sl < n ? (int64_t)p0 + sl : n);
+    const int32_t nwl = (p1 - p0 + 31) >> 5;          // this slice's bitmap words
+    const float* row = scores + (int64_t)t * ld;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kClThreads / 32;
+    ClusterTopkSmem* lead = cl.map_shared_rank(&sh, 0);
     __syncthreads();
-    cl.sync();   // every CTA has started and zeroed what the others add into
+    // Remote accesses come after the cluster barrier that ends the split pass
+    // (every CTA has started and cleared its shared memory by then); only the
+    // first-digit count below adds into the leader earlier, after a barrier.
 
     if (hist1 == nullptr) {   // digit 1: count the slice, sum in the leader
+        cl.sync();
         // a non-empty slice starts at a multiple of 128; an empty one (p0 == n)
         // must not round p0 down into the previous slice
         const int32_t v_end = p0 < p1 ? (p1 + 3) >> 2 : (p0 >> 2);
@@ -1064,13 +1055,13 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
     if (gathered) {
         if (r == 0) {
             // the cluster's candidate keys, CTA by CTA
-            uint32_t seg[kClusterMax + 1];
-            seg[0] = 0;
-            for (int i = 0; i < C; ++i) seg[i + 1] = seg[i] + sh.cta_cand[i];
-            for (int i = 0; i < C; ++i) {
-                const uint32_t* rk = cl.map_shared_rank(cand_key, i);
-                for (uint32_t e = threadIdx.x; e < sh.cta_cand[i]; e += kClThreads)
-                    g_key[seg[i] + e] = rk[e];
+            if (threadIdx.x == 0)
+                for (int i = 0; i < C; ++i) sh.seg[i + 1] = sh.seg[i] + sh.cta_cand[i];
+            __syncthreads();
+            for (uint32_t e = threadIdx.x; e < total_cand; e += kClThreads) {   // one round trip
+                int i = 0;
+                while (i + 1 < C && e >= sh.seg[i + 1]) ++i;
+                g_key[e] = cl.map_shared_rank(cand_key, i)[e - sh.seg[i]];
             }
             zero<kClThreads>(sh.hist, 1024);
             __syncthreads();
@@ -1095,7 +1086,7 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
                 const uint32_t kk = g_key[e];
                 if (kk < tau0) continue;
                 int i = 0;
-                while (i + 1 < C && e >= seg[i + 1]) ++i;
+                while (i + 1 < C && e >= sh.seg[i + 1]) ++i;
                 atomicAdd(kk > tau0 ? &sh.ext_above[i] : &sh.ext_tie[i], 1u);
             }
             __syncthreads();
