@@ -5,8 +5,10 @@
 One step = one pass of the whole indexer over one batch of the named workload:
 key LayerNorm (when the workload chains it), head scores with the relu/head-
 weighted epilogue, and the exact top-2048 with the tie/order rule. Inputs are
-resident in HBM when the timed region starts; L2 is flushed (a 256 MB write)
-between timed steps. Rank 0 prints one JSON line.
+resident in HBM when the timed region starts; between timed steps L2 is
+flushed by writing a 256 MB buffer and then reading another 256 MB buffer (so
+that every step starts with a cold L2 that holds no dirty lines of the
+flush). Rank 0 prints one JSON line.
 
 --impl reference times the CPU oracle (the plain fp64 definition) on the host's
 cores on a bounded row sample of the same workload, as the reference arm.
@@ -125,6 +127,64 @@ def dram_traffic(workload: int, kernel: str):
     return rec["bytes_per_launch"]
 
 
+KERNEL_SOURCES = {"key_layernorm": "layernorm.cu", "score": "score_tc.cu", "topk": "topk.cu"}
+
+
+def _kernel_class(name: str):
+    if "key_layernorm" in name:
+        return "key_layernorm"
+    if "score_tc_kernel" in name:
+        return "score"
+    if "topk" in name:
+        return "topk"
+    return None
+
+
+def record_traffic(workload: int, csv_path: str):
+    """Average DRAM bytes per call of each kernel class in an ncu CSV of a
+    --fused-only run, stored with the sha256 of the class's source file."""
+    import csv
+    import hashlib
+    rows = list(csv.reader(open(csv_path)))
+    hdr = next(i for i, r in enumerate(rows) if "Kernel Name" in r and "Metric Name" in r)
+    h = rows[hdr]
+    ki, mi, vi, ui, ii = (h.index("Kernel Name"), h.index("Metric Name"), h.index("Metric Value"),
+                          h.index("Metric Unit"), h.index("ID"))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+    launches = {}
+    for r in rows[hdr + 1:]:
+        if len(r) <= vi or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        cls = _kernel_class(r[ki])
+        if cls is None:
+            continue
+        launches.setdefault((r[ii], cls), 0.0)
+        launches[(r[ii], cls)] += float(r[vi].replace(",", "")) * scale.get(r[ui], 1)
+    calls = sum(1 for (_, c) in launches if c == "score")
+    if calls == 0:
+        raise SystemExit("no scorer launch in " + csv_path)
+    out_path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    data = json.load(open(out_path)) if os.path.exists(out_path) else {}
+    entry = {}
+    for cls, src in KERNEL_SOURCES.items():
+        total = sum(v for (_, c), v in launches.items() if c == cls)
+        n = sum(1 for (_, c) in launches if c == cls)
+        if n == 0:
+            continue
+        path = os.path.join(ROOT, "sparse_attention_key_gb300", "csrc", src)
+        entry[cls] = {"source": src,
+                      "sha256": hashlib.sha256(open(path, "rb").read()).hexdigest(),
+                      "bytes_per_launch": int(round(total / calls))}
+    data[wl.NAMES[workload]] = entry
+    data["_note"] = ("DRAM bytes per fused call of each kernel class (dram__bytes_read.sum + "
+                     "dram__bytes_write.sum, ncu --clock-control none, default cache control) "
+                     "from a `bench.py --fused-only` capture, recorded by `bench.py "
+                     "--record-traffic`; topk sums the selection kernels of one call. bench.py "
+                     "reports a value only while the source file's sha256 matches.")
+    json.dump(data, open(out_path, "w"), indent=1, sort_keys=True)
+    print(json.dumps({wl.NAMES[workload]: entry}))
+
+
 # ---------------------------------------------------------------------------
 # algorithmic work per launch
 # ---------------------------------------------------------------------------
@@ -181,7 +241,12 @@ def run_ours(args, rank, world, local_rank):
     scores = torch.empty((T, ld), dtype=torch.float32, device=dev)
     ws_small = B.workspace(max(B.score_workspace_size(w.B, T, max_len),
                                B.topk_workspace_size(T, max_len, K)), dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()        # evicts everything the step could reuse
+        flush_r.max()          # writes the flush's dirty lines back before the step
     stream = torch.cuda.current_stream()
 
     def step():
@@ -222,7 +287,7 @@ def run_ours(args, rank, world, local_rank):
     launches0 = B.kernel_launches()
     t_wall0 = time.time()
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -233,11 +298,19 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = float(sum(step_ms))
+    if args.fused_only:   # profiling runs: the timed fused steps only
+        clocks.stop()
+        if rank == 0:
+            print(json.dumps({"mode": "fused-only", "workload": wl.NAMES[args.workload],
+                              "steps": args.steps, "ms_per_step": total_ms / args.steps,
+                              "value": w.pairs * args.steps / (total_ms / 1e3), "unit": UNIT}),
+                  flush=True)
+        return
 
     # ---- per-kernel durations: the same kernels through the split entry points
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         step_split(evs[i])
     torch.cuda.synchronize()
     t_wall2 = time.time()
@@ -278,7 +351,7 @@ def run_ours(args, rank, world, local_rank):
     e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         e_start[i].record(stream)
         e2e_step()
         e_end[i].record(stream)
@@ -333,7 +406,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": wl.NAMES[args.workload], "B": w.B, "T": T, "L": w.L,
                    "pairs_per_step": pairs, "topk": K, "max_len": max_len,
-                   "layernorm_in_step": chained_ln, "l2": "flushed (256 MB write) between steps",
+                   "layernorm_in_step": chained_ln, "l2": "flushed between steps: 256 MB written, then 256 MB read (cold, clean)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "matches_device_result": bool(ok)},
@@ -438,7 +511,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--fused-only", action="store_true",
+                    help="time only the fused steps (for profiler captures); prints a short line")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="record per-launch DRAM bytes of --workload's kernels from an ncu CSV "
+                         "(gpu__time_duration.sum, dram__bytes_read.sum, dram__bytes_write.sum of "
+                         "a --fused-only run) into profiles/dram_traffic.json, then exit")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(args.workload, args.record_traffic)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
