@@ -51,16 +51,22 @@ struct TcPlanHeader {
     int32_t pad[2];
 };
 
+constexpr int kMaxScorerCtas = 1024;   // per-CTA start descriptors in the plan
+
 size_t tc_plan_bytes(int32_t B, int32_t T) {
     const size_t g = (size_t)T + (size_t)B + 1;  // >= number of groups for any GQ >= 1
     return align_up(sizeof(TcPlanHeader), 256) + align_up(g * sizeof(int4), 256) +
-           align_up((g + 1) * sizeof(int32_t), 256);
+           align_up((g + 1) * sizeof(int32_t), 256) + 2 * kMaxScorerCtas * sizeof(int4);
 }
 
 struct TcPlan {
     TcPlanHeader* hdr;
     int4* groups;        // {sequence, first query row, queries, key tiles}
     int32_t* step_begin; // [n_groups + 1]
+    // Per scorer CTA c: [2c] = {group of its first step, key tile of that
+    // step within the group, first step of the next group, end of the CTA's
+    // range}, [2c+1] = that group's entry of `groups`.
+    int4* cta_desc;
     int32_t capacity;    // entries of groups
 };
 
@@ -72,8 +78,34 @@ static TcPlan plan_layout(void* base, int32_t B, int32_t T) {
     pl.groups = reinterpret_cast<int4*>(p + align_up(sizeof(TcPlanHeader), 256));
     pl.step_begin = reinterpret_cast<int32_t*>(p + align_up(sizeof(TcPlanHeader), 256) +
                                                align_up(g * sizeof(int4), 256));
+    pl.cta_desc = reinterpret_cast<int4*>(p + align_up(sizeof(TcPlanHeader), 256) +
+                                          align_up(g * sizeof(int4), 256) +
+                                          align_up((g + 1) * sizeof(int32_t), 256));
     pl.capacity = (int32_t)g;
     return pl;
+}
+
+// CTA c of `grid` scorer CTAs takes the steps [total*c/grid, total*(c+1)/grid).
+// Descriptor of scorer CTA c, whose first step is found by binary search in
+// sb[0..n_groups] (shared or global memory; sb[n_groups] == total > 0).
+__device__ __forceinline__ void write_cta_desc(const TcPlan& plan, const int32_t* sb, int n_groups,
+                                               int64_t total, int grid, int c) {
+    const int64_t beg = total * c / grid, end = total * (c + 1) / grid;
+    int lo = 0, hi = n_groups - 1;   // the last group whose first step is <= beg
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sb[mid] <= beg) lo = mid; else hi = mid - 1;
+    }
+    plan.cta_desc[2 * c] = make_int4(lo, (int)(beg - sb[lo]), sb[lo + 1], (int)end);
+    plan.cta_desc[2 * c + 1] = plan.groups[lo];
+}
+
+// Descriptors of a plan with no steps: every CTA has an empty range.
+__device__ __forceinline__ void write_empty_descs(const TcPlan& plan, int grid) {
+    for (int c = threadIdx.x; c < grid; c += blockDim.x) {
+        plan.cta_desc[2 * c] = make_int4(0, 0, 0, 0);
+        plan.cta_desc[2 * c + 1] = make_int4(0, 0, 0, 0);
+    }
 }
 
 constexpr int kPlanThreads = 1024;
@@ -114,7 +146,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 tc_plan_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu_q,
                const int32_t* __restrict__ cu_k, int B, int T, int64_t n_keys, int64_t max_len,
                TcPlan plan, DeviceStatus* status, bool zero_status, uint4* zero_ptr,
-               int64_t zero_vec) {
+               int64_t zero_vec, int grid) {
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x > 0) {
@@ -164,6 +196,7 @@ tc_plan_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu
             plan.hdr->total_steps = 0;
             plan.step_begin[0] = 0;
         }
+        write_empty_descs(plan, grid);
         return;
     }
     const int n_groups = carry;
@@ -203,6 +236,149 @@ tc_plan_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu
         plan.hdr->n_groups = n_groups;
         plan.hdr->total_steps = carry;
     }
+    // per-CTA start descriptors, one thread per CTA
+    if (carry == 0) {
+        write_empty_descs(plan, grid);
+        return;
+    }
+    __syncthreads();   // step_begin and groups are complete
+    for (int c = threadIdx.x; c < grid; c += kPlanThreads)
+        write_cta_desc(plan, plan.step_begin, n_groups, carry, grid, c);
+}
+
+// Fast plan for up to kPlanSeqs sequences: one thread per sequence reads its
+// bounds and counts its groups (a block scan places them), then each thread
+// takes a contiguous run of groups, finds their sequence in shared memory,
+// reads the queries' positions (all at once) and counts the key tiles; a
+// second block scan gives the groups' first steps. Two rounds of global reads
+// in all, instead of a chain of dependent ones. Argument checks and error
+// reports are those of tc_plan_kernel.
+constexpr int kPlanSeqs = 2048;
+constexpr int kPlanSbShared = 2048;   // groups whose first steps are kept in shared memory
+constexpr int kPlanRegGroups = 8;     // groups per thread kept in registers
+
+template <int GQ>
+__global__ void __launch_bounds__(kPlanThreads)
+tc_plan_fast_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu_q,
+                    const int32_t* __restrict__ cu_k, int B, int T, int64_t n_keys,
+                    int64_t max_len, TcPlan plan, DeviceStatus* status, bool zero_status,
+                    uint4* zero_ptr, int64_t zero_vec, int grid) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x > 0) {
+        for (int64_t i = (int64_t)(blockIdx.x - 1) * kPlanThreads + threadIdx.x; i < zero_vec;
+             i += (int64_t)(gridDim.x - 1) * kPlanThreads)
+            zero_ptr[i] = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    __shared__ int s_q0[kPlanSeqs], s_nq[kPlanSeqs], s_lk[kPlanSeqs], s_gofs[kPlanSeqs + 1];
+    __shared__ int s_sb[kPlanSbShared + 1];   // groups' first steps, when they fit
+    __shared__ int warp_sums[33];
+    if (zero_status && threadIdx.x == 0) {
+        status->code = 0;
+        status->detail = 0;
+    }
+    __syncthreads();
+
+    // sequences: bounds, validity and group counts
+    int carry = 0;
+    for (int base = 0; base < B; base += kPlanThreads) {
+        const int b = base + threadIdx.x;
+        int cnt = 0;
+        if (b < B) {
+            const int q0 = __ldg(cu_q + b), q1 = __ldg(cu_q + b + 1);
+            const int64_t k0 = __ldg(cu_k + b), k1 = __ldg(cu_k + b + 1);
+            int nq = q1 - q0;
+            if (q0 < 0 || nq < 0 || (int64_t)q0 + nq > T) {
+                report_error(status, IDX_ERR_DEVICE_ARG, -1 - b);
+                nq = 0;
+            }
+            const bool seq_ok = k0 >= 0 && k1 >= k0 && k1 <= n_keys;
+            cnt = (nq + GQ - 1) / GQ;
+            s_q0[b] = q0;
+            s_nq[b] = nq;
+            s_lk[b] = seq_ok ? (int)(k1 - k0 < 0x7fffffffLL ? k1 - k0 : 0x7fffffffLL) : -1;
+        }
+        int total;
+        const int off = carry + block_exclusive_sum(cnt, warp_sums, &total);
+        if (b < B) s_gofs[b] = off;
+        carry += total;
+    }
+    if (threadIdx.x == 0) s_gofs[B] = carry;
+    __syncthreads();
+    const int n_groups = carry;
+    if (n_groups >= plan.capacity) {   // cu_q is not a partition of 0..T
+        if (threadIdx.x == 0) {
+            report_error(status, IDX_ERR_DEVICE_ARG, -1);
+            plan.hdr->n_groups = 0;
+            plan.hdr->total_steps = 0;
+            plan.step_begin[0] = 0;
+        }
+        write_empty_descs(plan, grid);
+        return;
+    }
+
+    // groups: a contiguous run per thread
+    const int per = (n_groups + kPlanThreads - 1) / kPlanThreads;
+    const int g0 = min(n_groups, (int)threadIdx.x * per), g1 = min(n_groups, g0 + per);
+    int b = 0;
+    if (g0 < g1) {   // the sequence of group g0: the last b with s_gofs[b] <= g0
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_gofs[mid] <= g0) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+    }
+    int steps_r[kPlanRegGroups];
+    int my_steps = 0;
+    for (int g = g0, k = 0; g < g1; ++g, ++k) {
+        while (g >= s_gofs[b + 1]) ++b;   // empty sequences own no group
+        const int j = g - s_gofs[b];
+        const int q0 = s_q0[b] + j * GQ;
+        const int nq = min(GQ, s_nq[b] - j * GQ);
+        const int lk = s_lk[b];
+        int qp[GQ];
+#pragma unroll
+        for (int i = 0; i < GQ; ++i) qp[i] = i < nq ? __ldg(q_pos + q0 + i) : 0;
+        int64_t nmax = 0;
+#pragma unroll
+        for (int i = 0; i < GQ; ++i) {
+            if (i >= nq) break;
+            const int64_t n = (int64_t)qp[i] + 1;
+            if (lk < 0 || n < 1 || n > lk || n > max_len) {
+                report_error(status, IDX_ERR_DEVICE_ARG, q0 + i);
+                continue;
+            }
+            nmax = n > nmax ? n : nmax;
+        }
+        const int steps = (int)((nmax + 127) / 128);
+        plan.groups[g] = make_int4(b, q0, nq, steps);
+        if (k < kPlanRegGroups) steps_r[k] = steps;
+        my_steps += steps;
+    }
+    int total;
+    int sb = block_exclusive_sum(my_steps, warp_sums, &total);
+    const bool sb_shared = n_groups <= kPlanSbShared;
+    for (int g = g0, k = 0; g < g1; ++g, ++k) {
+        plan.step_begin[g] = sb;
+        if (sb_shared) s_sb[g] = sb;
+        const int4 d = k < kPlanRegGroups ? make_int4(0, 0, 0, steps_r[k]) : plan.groups[g];
+        sb += d.w;
+    }
+    if (threadIdx.x == 0) {
+        plan.step_begin[n_groups] = total;
+        if (sb_shared) s_sb[n_groups] = total;
+        plan.hdr->n_groups = n_groups;
+        plan.hdr->total_steps = total;
+    }
+    if (total == 0) {
+        write_empty_descs(plan, grid);
+        return;
+    }
+    __syncthreads();   // step offsets and groups are complete
+    for (int c = threadIdx.x; c < grid; c += kPlanThreads)
+        write_cta_desc(plan, sb_shared ? s_sb : plan.step_begin, n_groups, total, grid, c);
 }
 
 // ---------------------------------------------------------------------------
@@ -262,6 +438,14 @@ struct StepCursor {
     int32_t next_begin;    // first step of the next group
     int4 desc;
 
+    // From a CTA's start descriptor (see TcPlan::cta_desc).
+    __device__ __forceinline__ void init(int4 start, int4 group) {
+        g = start.x;
+        j = start.y;
+        next_begin = start.z;
+        desc = group;
+    }
+    // By binary search for step s among the groups' first steps.
     __device__ __forceinline__ void init(int32_t s, const TcPlan& p, int n_groups) {
         int lo = 0, hi = n_groups - 1;
         while (lo < hi) {
@@ -356,10 +540,28 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
     pdl_wait();
     pdl_launch_dependents();
 
-    const int n_groups = plan.hdr->n_groups;
-    const int64_t total = plan.hdr->total_steps;
-    const int32_t beg = (int32_t)(total * blockIdx.x / gridDim.x);
-    const int32_t end = (int32_t)(total * (blockIdx.x + 1) / gridDim.x);
+    // This CTA's steps [beg, end). One query per group (decode, where the
+    // start-up latency matters): from the CTA's start descriptor. Otherwise
+    // the cursors search the plan (measured faster for the 16-query
+    // configuration, whose start-up is negligible against its work).
+    int4 start = make_int4(0, 0, 0, 0), start_group = make_int4(0, 0, 0, 0);
+    int n_groups = 0;
+    int32_t beg, end;
+    if (C::GQ == 1) {
+        start = plan.cta_desc[2 * blockIdx.x];
+        start_group = plan.cta_desc[2 * blockIdx.x + 1];
+        end = start.w;
+        beg = start.z - start_group.w + start.y;
+    } else {
+        n_groups = plan.hdr->n_groups;
+        const int64_t total = plan.hdr->total_steps;
+        beg = (int32_t)(total * blockIdx.x / gridDim.x);
+        end = (int32_t)(total * (blockIdx.x + 1) / gridDim.x);
+    }
+    auto start_cursor = [&](StepCursor& c) {
+        if (C::GQ == 1) c.init(start, start_group);
+        else c.init(beg, plan, n_groups);
+    };
 
     bool aborted = false;
     auto give_up = [&](int site) {
@@ -378,7 +580,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
 #pragma unroll
             for (int s = 0; s < C::STAGES; ++s) issued[s] = 0;
             StepCursor cur;
-            cur.init(beg, plan, n_groups);
+            start_cursor(cur);
             bool new_group = true;
             const uint64_t key_policy = C::GQ == 1 ? l2_policy_evict_first() : 0ull;
             for (int32_t s = beg; s < end; ++s) {
@@ -438,7 +640,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
             int stage = 0, acc = 0, q_uses = 0;
             uint32_t phase = 0, aphase = 0;
             StepCursor cur;
-            cur.init(beg, plan, n_groups);
+            start_cursor(cur);
             bool new_group = true;
             for (int32_t s = beg; s < end && !aborted; ++s) {
                 if (s > beg) new_group = cur.advance(s, plan);
@@ -526,7 +728,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         int hist_row = -1;
         if (beg < end) {
             StepCursor cur;
-            cur.init(beg, plan, n_groups);
+            start_cursor(cur);
             bool new_group = true;
             for (int32_t s = beg; s < end && !aborted; ++s) {
                 if (s > beg) new_group = cur.advance(s, plan);
@@ -662,14 +864,16 @@ static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream
     const int64_t zero_vec = a.zero_ptr != nullptr ? (int64_t)(a.zero_bytes / 16) : 0;
     const int64_t zero_blocks = zero_vec > 0 ? (zero_vec + 4 * kPlanThreads - 1) / (4 * kPlanThreads) : 0;
     const int plan_grid = 1 + (int)(zero_blocks < 64 ? zero_blocks : 64);
-    cudaError_t e = launch_kernel(tc_plan_kernel<C::GQ>, dim3(plan_grid), dim3(kPlanThreads), 0, stream,
-                                  1, a.q_pos, a.cu_q, a.cu_k, a.B, a.T, a.n_keys, a.max_len, plan,
-                                  a.status, a.zero_status, reinterpret_cast<uint4*>(a.zero_ptr),
-                                  zero_vec);
+    const DeviceInfo& dev = device_info();
+    if (dev.sm_count < 1 || dev.sm_count > kMaxScorerCtas) return cudaErrorInvalidValue;
+    cudaError_t e = launch_kernel(a.B <= kPlanSeqs ? tc_plan_fast_kernel<C::GQ> : tc_plan_kernel<C::GQ>,
+                                  dim3(plan_grid), dim3(kPlanThreads), 0, stream, 1, a.q_pos, a.cu_q,
+                                  a.cu_k, a.B, a.T, a.n_keys, a.max_len, plan, a.status,
+                                  a.zero_status, reinterpret_cast<uint4*>(a.zero_ptr), zero_vec,
+                                  dev.sm_count);
     if (e != cudaSuccess) return e;
     e = ensure_smem_optin((const void*)score_tc_kernel<C>, C::SMEM);
     if (e != cudaSuccess) return e;
-    const DeviceInfo& dev = device_info();
     return launch_kernel(score_tc_kernel<C>, dim3(dev.sm_count), dim3(C::THREADS), (size_t)C::SMEM,
                          stream, 1, tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan,
                          a.status, row_hist, g_wait_limit_ns.load());

@@ -303,6 +303,16 @@ def test_indexer_decode_integer_ties_long_histories(B):
     _check_exact(B, w)
 
 
+def test_indexer_many_sequences(B):
+    # more sequences than the fast plan kernel takes (2048): the general plan,
+    # one query per sequence, some sequences without queries
+    rng = np.random.default_rng(403)
+    k_lens = rng.integers(1, 600, size=2100)
+    q_counts = np.where(rng.random(2100) < 0.1, 0, 1)
+    w = wl.custom(403, q_counts=q_counts, k_lens=k_lens, kind="int2")
+    _check_exact(B, w)
+
+
 def test_indexer_batch_with_empty_sequences(B):
     w = wl.custom(301, q_counts=[0, 4, 0, 2, 0], k_lens=[0, 2500, 10, 3000, 0], kind="int2")
     _check_exact(B, w)
