@@ -540,14 +540,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
     pdl_wait();
     pdl_launch_dependents();
 
-    // This CTA's steps [beg, end). One query per group (decode, where the
-    // start-up latency matters): from the CTA's start descriptor. Otherwise
-    // the cursors search the plan (measured faster for the 16-query
-    // configuration, whose start-up is negligible against its work).
+    // This CTA's steps [beg, end). A few queries per group (decode and
+    // verification, where the start-up latency matters): from the CTA's start
+    // descriptor. Otherwise the cursors search the plan (measured faster for
+    // the 16-query configuration, whose start-up is negligible against its
+    // work).
     int4 start = make_int4(0, 0, 0, 0), start_group = make_int4(0, 0, 0, 0);
     int n_groups = 0;
     int32_t beg, end;
-    if (C::GQ == 1) {
+    if (C::GQ <= 4) {
         start = plan.cta_desc[2 * blockIdx.x];
         start_group = plan.cta_desc[2 * blockIdx.x + 1];
         end = start.w;
@@ -559,7 +560,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         end = (int32_t)(total * (blockIdx.x + 1) / gridDim.x);
     }
     auto start_cursor = [&](StepCursor& c) {
-        if (C::GQ == 1) c.init(start, start_group);
+        if (C::GQ <= 4) c.init(start, start_group);
         else c.init(beg, plan, n_groups);
     };
 
@@ -582,7 +583,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
             StepCursor cur;
             start_cursor(cur);
             bool new_group = true;
-            const uint64_t key_policy = C::GQ == 1 ? l2_policy_evict_first() : 0ull;
+            const uint64_t key_policy = C::GQ <= 4 ? l2_policy_evict_first() : 0ull;
             for (int32_t s = beg; s < end; ++s) {
                 if (s > beg) new_group = cur.advance(s, plan);
                 if (new_group) {
@@ -607,9 +608,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
                 mbar_arrive_expect_tx(k_full + stage, C::K_STAGE);
                 const int32_t key_row = __ldg(cu_k + cur.desc.x) + cur.j * 128;
                 uint8_t* dst = k_smem + stage * C::K_STAGE;
-                if (C::GQ == 1) {
-                    // one query per group: each key tile is read about once, so
-                    // it should not push the staged scores out of L2
+                if (C::GQ <= 4) {
+                    // a few queries per sequence: each key tile is read about
+                    // once, so it should not push the staged scores out of L2
                     tma_load_2d_hint(smem_addr(dst), &tmap_k, k_full + stage, 0, key_row, key_policy);
                     tma_load_2d_hint(smem_addr(dst + C::K_HALF), &tmap_k, k_full + stage, 64, key_row,
                                      key_policy);
@@ -852,6 +853,10 @@ static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int box_
 using PrefillCfg = TcCfg<8, 2, 2, 3, 16>;
 // Decode: one query per group, N = 32, four accumulators, 6-stage key ring.
 using DecodeCfg = TcCfg<1, 1, 4, 6, 4>;
+// Speculative verification (a few queries per sequence): 4 queries per group
+// as one MMA of N = 128, four 128-column accumulators, 5-stage key ring, 8
+// epilogue warps (2 per TMEM lane quarter, 2 queries each).
+using VerifyCfg = TcCfg<4, 1, 4, 5, 8>;
 
 template <class C>
 static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream_t stream,
@@ -882,8 +887,10 @@ static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream
 cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream,
                             bool* hist_filled) {
     const TcPlan plan = plan_layout(plan_ws, a.B, a.T);
-    // Mostly one query per sequence (decode) vs. many (prefill / chunks).
+    // Mostly one query per sequence (decode), a few (speculative
+    // verification), or many (prefill / chunks).
     if ((int64_t)a.T <= 2 * (int64_t)a.B) return launch_cfg<DecodeCfg>(a, plan, stream, hist_filled);
+    if ((int64_t)a.T <= 4 * (int64_t)a.B) return launch_cfg<VerifyCfg>(a, plan, stream, hist_filled);
     return launch_cfg<PrefillCfg>(a, plan, stream, hist_filled);
 }
 

@@ -29,6 +29,10 @@ Named workloads (sizes from the indexer's use in Kimi K3.1 Pro's MLA layers:
 5. ``long_decode``    64 sequences, one query each, histories uniform in
                       [65,536, 131,072] keys; post-LN keys ~ N(0,1), q ~ N(0,1),
                       w ~ U(0, 1/32).
+6. ``spec_verify``    speculative-decoding verification: 16 sequences, each
+                      with 4 queries at the last 4 positions of a history
+                      uniform in [50,000, 100,000] keys (64 rows); post-LN keys
+                      ~ N(0,1), q ~ N(0,1), w ~ U(0, 1/32).
 """
 from __future__ import annotations
 
@@ -41,7 +45,7 @@ DIM = 128
 TOPK = 2048
 
 NAMES = {1: "tiny_exact", 2: "decode_batch", 3: "prefill_ties", 4: "agentic_chunk",
-         5: "long_decode"}
+         5: "long_decode", 6: "spec_verify"}
 
 
 def f32_to_bf16_bits(x) -> np.ndarray:
@@ -178,9 +182,22 @@ def long_decode(seed: int = 5, B: int = 64, lo: int = 65_536, hi: int = 131_072)
     return Workload("long_decode", q, w, pos, cu_q, cu_k, k, exact=False)
 
 
+def spec_verify(seed: int = 6, B: int = 16, m: int = 4, lo: int = 50_000,
+                hi: int = 100_000) -> Workload:
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int64)
+    cu_q, cu_k = _ragged([m] * B, lens)
+    k = _normal_bf16(rng, (int(cu_k[-1]), DIM))
+    q = _normal_bf16(rng, (B * m, HEADS, DIM))
+    w = rng.uniform(0.0, 1.0 / 32, size=(B * m, HEADS)).astype(np.float32)
+    pos = np.concatenate([np.arange(l - m, l, dtype=np.int32) for l in lens])
+    return Workload("spec_verify", q, w, pos, cu_q, cu_k, k, exact=False)
+
+
 def by_index(i: int, seed: int | None = None) -> Workload:
-    """Workload i in 1..5 (see the module docstring); the default seed is i."""
-    fn = {1: tiny_exact, 2: decode_batch, 3: prefill_ties, 4: agentic_chunk, 5: long_decode}[i]
+    """Workload i in 1..6 (see the module docstring); the default seed is i."""
+    fn = {1: tiny_exact, 2: decode_batch, 3: prefill_ties, 4: agentic_chunk, 5: long_decode,
+          6: spec_verify}[i]
     return fn(i if seed is None else seed)
 
 

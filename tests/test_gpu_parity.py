@@ -279,6 +279,19 @@ def test_indexer_long_decode_sampled(B):
         assert rule_order_ok(S[t, :n], idx[t], 2048) is None, t
 
 
+def test_indexer_spec_verify_sampled(B):
+    w = workload(6)
+    rows = [0, 3, 4, 29, 30, 63]
+    _check_tolerance(B, w, rows)
+    d = to_device(w)
+    idx, _ = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len)
+    S = gpu_scores(B, d, w.max_len).cpu().numpy()
+    idx = idx.cpu().numpy()
+    for t in range(w.T):
+        n = int(w.q_pos[t]) + 1
+        assert rule_order_ok(S[t, :n], idx[t], 2048) is None, t
+
+
 # ---------------------------------------------------------------------------
 # edge cases and errors
 # ---------------------------------------------------------------------------
@@ -293,6 +306,15 @@ def test_indexer_few_chunk_queries_with_long_histories(B):
     # many queries per sequence (tensor-core prefill tiles) but few rows in all:
     # the few-rows selection path, with its own histogram pass
     w = wl.custom(401, q_counts=[60, 40], k_lens=[20000, 15000], kind="int2")
+    _check_exact(B, w)
+
+
+def test_indexer_spec_verify_shapes_exact(B):
+    # a few queries per sequence (the speculative-verification configuration,
+    # 4 queries per tensor-core group), one history long enough for the
+    # cluster selection; integer inputs: bit-exact
+    w = wl.custom(404, q_counts=[4, 4, 3, 4, 1], k_lens=[20000, 3000, 9000, 130, 2100], kind="int2")
+    assert w.B < w.T <= 4 * w.B
     _check_exact(B, w)
 
 

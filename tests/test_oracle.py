@@ -341,3 +341,10 @@ def test_workloads_shapes_and_pairs():
     assert w3.pairs == 512 * 513 // 2
     w2 = wl.decode_batch()
     assert w2.pairs == 249856 and w2.k is None and w2.k_raw.shape == (249856, 128)
+    # speculative verification: 16 users x the last 4 positions of their histories
+    w6 = wl.spec_verify(B=3, lo=100, hi=200)
+    lens = np.diff(w6.cu_k)
+    assert w6.T == 12 and w6.B == 3 and np.array_equal(np.diff(w6.cu_q), [4, 4, 4])
+    assert np.array_equal(w6.q_pos, np.concatenate([np.arange(l - 4, l) for l in lens]))
+    assert w6.pairs == int(sum(4 * l - 6 for l in lens))
+    assert wl.NAMES[6] == "spec_verify" and wl.by_index(6).T == 64
