@@ -421,6 +421,57 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_ln_append(args):
+    """Key-cache append with the LayerNorm fused in, on one GPU."""
+    import torch
+    from sparse_attention_key_gb300 import build as lib_build
+    lib_build.build()
+    from sparse_attention_key_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    n = args.ln_append
+    rng = np.random.default_rng(2024)
+    x = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal((n, 128), dtype=np.float32))
+                         .view(np.int16)).to(dev)
+    g = torch.from_numpy(wl.f32_to_bf16_bits((1 + 0.1 * rng.standard_normal(128)).astype(np.float32))
+                         .view(np.int16)).to(dev)
+    b = torch.from_numpy(wl.f32_to_bf16_bits((0.1 * rng.standard_normal(128)).astype(np.float32))
+                         .view(np.int16)).to(dev)
+    rows = 4 * n
+    cache = torch.zeros((rows, 128), dtype=torch.int16, device=dev)
+    slot = torch.from_numpy(rng.permutation(rows)[:n].astype(np.int64)).to(dev)
+    staging = torch.empty_like(x)
+    flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(args.steps):
+            flush_w.zero_()
+            flush_r.max()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(e))
+        return float(np.median(ms)) * 1e3
+
+    fused_us = timed(lambda: B.key_layernorm_append(x, g, b, 1e-6, cache, slot))
+    unfused_us = timed(lambda: cache.index_copy_(0, slot, B.key_layernorm(x, g, b, 1e-6, out=staging)))
+    pk = peaks()
+    alg = n * (256 + 256 + 8)
+    ach = alg / (fused_us * 1e-6) / 1e9
+    print(json.dumps({"mode": "ln-append", "rows": n, "cache_rows": rows, "steps": args.steps,
+                      "us_per_call": fused_us, "unfused_us_per_call": unfused_us,
+                      "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                                   "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                                   "bytes_per_call": alg},
+                      "l2": "flushed between calls: 256 MB written, then 256 MB read"}), flush=True)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
@@ -511,6 +562,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--ln-append", type=int, metavar="ROWS", default=0,
+                    help="time the key LayerNorm fused into the key-cache append of ROWS new keys "
+                         "(random distinct slots of a 4*ROWS-row cache) against LayerNorm into a "
+                         "staging buffer plus a scatter copy; prints its own JSON line")
     ap.add_argument("--fused-only", action="store_true",
                     help="time only the fused steps (for profiler captures); prints a short line")
     ap.add_argument("--record-traffic", metavar="CSV",
@@ -520,6 +575,9 @@ def main():
     args = ap.parse_args()
     if args.record_traffic:
         record_traffic(args.workload, args.record_traffic)
+        return
+    if args.ln_append:
+        run_ln_append(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

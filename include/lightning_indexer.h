@@ -92,6 +92,30 @@ IDX_API idx_status idx_key_layernorm(const uint16_t* k_raw, const void* ln_w, co
                              void* stream);
 
 /*
+ * Key LayerNorm fused into the key-cache append: the same LayerNorm as
+ * idx_key_layernorm (bit-identical results), each output row written
+ * straight into its slot of the key cache instead of a staging buffer
+ * (port notes, indexer paragraph: new keys pass the LayerNorm before they
+ * are cached; "Kimi K3 on AMD Instinct GPUs with TokenSpeed", section 2.2
+ * "Fused cache writes and output processing": the cache rows are prepared,
+ * normalisation included, by one kernel rather than several small ones).
+ *   k_raw      bf16 [n_rows,128], new raw keys (must not overlap the cache
+ *              rows being written)
+ *   ln_w, ln_b [128], bf16 or fp32 as ln_dtype
+ *   k_cache    bf16 [cache_rows,128]; row slot[r] receives LN(k_raw[r])
+ *   slot       int64 [n_rows], device memory: destination row of each new
+ *              key, distinct among the rows written; -1 marks a padding row.
+ *              Any slot outside [0, cache_rows) writes nothing (no error).
+ *   n_rows     >= 0 (0 enqueues nothing)
+ * Rows of k_cache that no slot names are left untouched. Asynchronous on
+ * `stream`; allocates nothing.
+ */
+IDX_API idx_status idx_key_layernorm_append(const uint16_t* k_raw, const void* ln_w,
+                                            const void* ln_b, int ln_dtype, float eps,
+                                            uint16_t* k_cache, int64_t cache_rows,
+                                            const int64_t* slot, int64_t n_rows, void* stream);
+
+/*
  * Head scores (indexer paragraph: per-head relu of q_h . k over the causal
  * past, combined with a per-head weight; item (3): no rotary):
  *     scores[t*ld + s] = sum_h w[t,h] * max(sum_d q[t,h,d] * k[cu_k[b]+s, d], 0)

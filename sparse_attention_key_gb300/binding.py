@@ -33,7 +33,7 @@ _lock = threading.Lock()
 EXPORTS = ("idx_key_layernorm", "idx_score", "idx_score_workspace_size", "idx_topk",
            "idx_topk_workspace_size", "idx_score_topk", "idx_score_topk_workspace_size",
            "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches",
-           "idx_score_topk_noalloc", "idx_set_wait_limit_ns")
+           "idx_score_topk_noalloc", "idx_set_wait_limit_ns", "idx_key_layernorm_append")
 
 
 class IndexerError(RuntimeError):
@@ -143,6 +143,30 @@ def key_layernorm(k_raw: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Tensor, e
     _check(lib().idx_key_layernorm(_ptr(k_raw), _ptr(ln_w), _ptr(ln_b), pdt, float(eps),
                                    _ptr(out), k_raw.shape[0], _stream()), "idx_key_layernorm")
     return out
+
+
+def key_layernorm_append(k_raw: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Tensor, eps: float,
+                         k_cache: torch.Tensor, slot: torch.Tensor) -> torch.Tensor:
+    """LayerNorm of the new raw keys written into rows `slot` of `k_cache` (in place)."""
+    _dev(k_raw, "k_raw", _BF16)
+    if k_raw.dim() != 2 or k_raw.shape[1] != DIM:
+        raise ValueError("k_raw must be [n,128]")
+    if ln_w.dtype != ln_b.dtype:
+        raise TypeError("ln_w and ln_b must share a dtype")
+    _dev(ln_w, "ln_w", _BF16 + _F32, (DIM,))
+    _dev(ln_b, "ln_b", _BF16 + _F32, (DIM,))
+    _dev(k_cache, "k_cache", _BF16)
+    if k_cache.dim() != 2 or k_cache.shape[1] != DIM:
+        raise ValueError("k_cache must be [rows,128]")
+    _dev(slot, "slot", (torch.int64,), (k_raw.shape[0],))
+    pdt = PARAM_F32 if ln_w.dtype == torch.float32 else PARAM_BF16
+    fn = lib().idx_key_layernorm_append
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    _check(fn(_ptr(k_raw), _ptr(ln_w), _ptr(ln_b), pdt, float(eps), _ptr(k_cache),
+              k_cache.shape[0], _ptr(slot), k_raw.shape[0], _stream()), "idx_key_layernorm_append")
+    return k_cache
 
 
 def _batch(q, k, w, q_pos, cu_q, cu_k):

@@ -183,6 +183,26 @@ idx_status idx_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void
     return e == cudaSuccess ? IDX_OK : cuda_fail(e, "key_layernorm launch");
 }
 
+idx_status idx_key_layernorm_append(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
+                                    int ln_dtype, float eps, uint16_t* k_cache, int64_t cache_rows,
+                                    const int64_t* slot, int64_t n_rows, void* stream) {
+    g_last_error[0] = 0;
+    if (n_rows < 0 || cache_rows < 0) return fail(IDX_ERR_INVALID_ARG, "n_rows and cache_rows must be >= 0");
+    if (ln_dtype != IDX_PARAM_BF16 && ln_dtype != IDX_PARAM_F32)
+        return fail(IDX_ERR_INVALID_ARG, "ln_dtype must be IDX_PARAM_BF16 or IDX_PARAM_F32");
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(IDX_ERR_INVALID_ARG, "eps must be finite, >= 0");
+    if (n_rows == 0) return IDX_OK;
+    if (!k_raw || !ln_w || !ln_b || !k_cache || !slot)
+        return fail(IDX_ERR_INVALID_ARG, "k_raw, ln_w, ln_b, k_cache, slot must not be NULL");
+    if (!aligned(k_raw, 16) || !aligned(k_cache, 16) || !aligned(ln_w, 4) || !aligned(ln_b, 4) ||
+        !aligned(slot, 8))
+        return fail(IDX_ERR_INVALID_ARG, "k_raw/k_cache must be 16-byte aligned, slot 8-byte aligned");
+    if (idx_status st = check_device()) return st;
+    cudaError_t e = launch_key_layernorm(k_raw, ln_w, ln_b, ln_dtype == IDX_PARAM_F32, eps, k_cache,
+                                         n_rows, (cudaStream_t)stream, slot, cache_rows);
+    return e == cudaSuccess ? IDX_OK : cuda_fail(e, "key_layernorm_append launch");
+}
+
 size_t idx_score_workspace_size(int32_t B, int32_t T, int64_t /*max_len*/) {
     return kWsHeader + align_up(score_plan_bytes(B, T), 256);
 }

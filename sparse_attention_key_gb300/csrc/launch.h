@@ -61,9 +61,12 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// slot == NULL: row r of k_raw -> row r of k_out. Otherwise row r -> row
+// slot[r] of k_out ([out_rows,128]); out-of-range slots write nothing.
 cudaError_t launch_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
                                  bool f32_params, float eps, uint16_t* k_out, int64_t n_rows,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, const int64_t* slot = nullptr,
+                                 int64_t out_rows = 0);
 
 // Arguments of one scoring call (device pointers, host sizes).
 struct ScoreArgs {

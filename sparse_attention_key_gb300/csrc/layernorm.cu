@@ -21,10 +21,13 @@ namespace lidx {
 constexpr int kLnWarpsPerBlock = 8;
 constexpr int kLnRowsInFlight = 4;   // row pairs per warp per iteration
 
-template <bool kF32Params>
+// kScatter: row r of the output is row slot[r] of y (a key cache of
+// `y_rows` rows); slots outside [0, y_rows) (-1 marks padding) write nothing.
+template <bool kF32Params, bool kScatter>
 __global__ void __launch_bounds__(kLnWarpsPerBlock * 32)
 key_layernorm_kernel(const uint4* x, const void* __restrict__ ln_w, const void* __restrict__ ln_b,
-                     float eps, uint4* y, int64_t n_rows) {
+                     float eps, uint4* y, int64_t n_rows, const int64_t* __restrict__ slot,
+                     int64_t y_rows) {
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -49,10 +52,16 @@ key_layernorm_kernel(const uint4* x, const void* __restrict__ ln_w, const void* 
     constexpr int kRowsPerIter = 2 * kLnRowsInFlight;
     for (int64_t r0 = warp_id * kRowsPerIter; r0 < n_rows; r0 += n_warps * kRowsPerIter) {
         uint4 v[kLnRowsInFlight];
+        int64_t dst[kLnRowsInFlight];
 #pragma unroll
         for (int i = 0; i < kLnRowsInFlight; ++i) {   // loads first
             const int64_t row = r0 + 2 * i + half;
             v[i] = row < n_rows ? x[row * 16 + hl] : make_uint4(0u, 0u, 0u, 0u);
+            dst[i] = row;
+            if (kScatter) {
+                const int64_t sr = row < n_rows ? __ldg(slot + row) : -1;
+                dst[i] = sr >= 0 && sr < y_rows ? sr : -1;
+            }
         }
 #pragma unroll
         for (int i = 0; i < kLnRowsInFlight; ++i) {
@@ -86,14 +95,14 @@ key_layernorm_kernel(const uint4* x, const void* __restrict__ ln_w, const void* 
                 const float2 o = __ffma2_rn(__fmul2_rn(c[k], inv2), g[k], b[k]);
                 o16[k] = f32x2_to_bf16x2_rn(o.x, o.y);
             }
-            if (row < n_rows) y[row * 16 + hl] = make_uint4(o16[0], o16[1], o16[2], o16[3]);
+            if (row < n_rows && dst[i] >= 0) y[dst[i] * 16 + hl] = make_uint4(o16[0], o16[1], o16[2], o16[3]);
         }
     }
 }
 
 cudaError_t launch_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
                                  bool f32_params, float eps, uint16_t* k_out, int64_t n_rows,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const int64_t* slot, int64_t out_rows) {
     const DeviceInfo& dev = device_info();
     constexpr int64_t kRowsPerBlock = kLnWarpsPerBlock * 2 * kLnRowsInFlight;
     const int64_t blocks_needed = (n_rows + kRowsPerBlock - 1) / kRowsPerBlock;
@@ -101,9 +110,11 @@ cudaError_t launch_key_layernorm(const uint16_t* k_raw, const void* ln_w, const 
     const int grid = (int)(blocks_needed < cap ? blocks_needed : cap);
     const uint4* x = reinterpret_cast<const uint4*>(k_raw);
     uint4* y = reinterpret_cast<uint4*>(k_out);
-    return launch_kernel(f32_params ? key_layernorm_kernel<true> : key_layernorm_kernel<false>,
-                         dim3(grid), dim3(kLnWarpsPerBlock * 32), 0, stream, 1, x, ln_w, ln_b, eps, y,
-                         n_rows);
+    auto kern = slot != nullptr
+                    ? (f32_params ? key_layernorm_kernel<true, true> : key_layernorm_kernel<false, true>)
+                    : (f32_params ? key_layernorm_kernel<true, false> : key_layernorm_kernel<false, false>);
+    return launch_kernel(kern, dim3(grid), dim3(kLnWarpsPerBlock * 32), 0, stream, 1, x, ln_w, ln_b,
+                         eps, y, n_rows, slot, slot != nullptr ? out_rows : n_rows);
 }
 
 }  // namespace lidx

@@ -66,6 +66,40 @@ def oracle_rows(w, rows, want_scores=True, K=2048, k_bits=None):
 # LayerNorm
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("f32_params", [False, True])
+def test_layernorm_cache_append(B, f32_params):
+    # new keys normalised straight into their cache rows: the same values as
+    # idx_key_layernorm (bit-identical) and within the oracle's tolerance;
+    # padding (-1) and out-of-range slots write nothing; other rows untouched
+    rng = np.random.default_rng(9 + f32_params)
+    n_new, rows = 1000, 5000
+    x = wl.f32_to_bf16_bits(rng.standard_normal((n_new, 128)).astype(np.float32) * 1.5 - 0.2)
+    g = wl.f32_to_bf16_bits((1 + 0.1 * rng.standard_normal(128)).astype(np.float32))
+    b = wl.f32_to_bf16_bits((0.1 * rng.standard_normal(128)).astype(np.float32))
+    slot = rng.permutation(rows)[:n_new].astype(np.int64)
+    slot[::97] = -1
+    slot[5] = rows            # out of range: ignored
+    slot[6] = -7
+    if f32_params:
+        gw = torch.from_numpy(wl.bf16_bits_to_f32(g)).cuda()
+        gb = torch.from_numpy(wl.bf16_bits_to_f32(b)).cuda()
+    else:
+        gw, gb = torch.from_numpy(g.view(np.int16)).cuda(), torch.from_numpy(b.view(np.int16)).cuda()
+    guard = np.int16(0x7FBF)  # a bf16 NaN pattern no LayerNorm output takes
+    cache = torch.full((rows, 128), int(guard), dtype=torch.int16, device="cuda")
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    B.key_layernorm_append(xd, gw, gb, 1e-6, cache, torch.from_numpy(slot).cuda())
+    plain = bits_of(B.key_layernorm(xd, gw, gb, 1e-6))
+    got = bits_of(cache)
+    ok = (slot >= 0) & (slot < rows)
+    assert np.array_equal(got[slot[ok]], plain[ok])
+    untouched = np.ones(rows, bool)
+    untouched[slot[ok]] = False
+    assert (got[untouched] == np.uint16(guard)).all()
+    ref = _ln_check(B, x[ok], g, b, 1e-6, f32_params=f32_params)
+    assert np.array_equal(ref, plain[ok])
+
+
 def _ln_check(B, k_raw_bits, ln_w_bits, ln_b_bits, eps, f32_params=False):
     dev = torch.from_numpy(k_raw_bits.view(np.int16)).cuda()
     if f32_params:

@@ -132,6 +132,26 @@ def test_layernorm_host_errors(L):
     assert call(n=0) == 0             # nothing to do: no device needed
 
 
+def test_layernorm_append_host_errors(L):
+    fn = L.idx_key_layernorm_append
+    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
+                                           ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                           ctypes.c_void_p]
+
+    def call(**kw):
+        a = dict(k_raw=FAKE, w=FAKE, b=FAKE, dt=0, eps=1e-6, cache=FAKE, rows=100, slot=FAKE, n=10)
+        a.update(kw)
+        return fn(a["k_raw"], a["w"], a["b"], a["dt"], a["eps"], a["cache"], a["rows"], a["slot"],
+                  a["n"], NULL)
+    assert call(n=-1) == 1
+    assert call(rows=-1) == 1
+    assert call(dt=3) == 1
+    assert call(slot=NULL) == 1
+    assert call(cache=NULL) == 1
+    assert call(slot=ctypes.c_void_p(4096 + 4)) == 1   # int64 slots: 8-byte aligned
+    assert call(n=0) == 0                               # nothing to do: no device needed
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     from sparse_attention_key_gb300 import binding
     monkeypatch.setattr(binding, "_lib", None)
