@@ -472,6 +472,57 @@ def run_ln_append(args):
                       "l2": "flushed between calls: 256 MB written, then 256 MB read"}), flush=True)
 
 
+def run_project(args):
+    """Indexer projections of T tokens (random weights), on one GPU."""
+    import torch
+    from sparse_attention_key_gb300 import build as lib_build
+    lib_build.build()
+    from sparse_attention_key_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    T, H, R = args.project, args.hidden, args.q_rank
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    mk = lambda *shape, s=1.0: (torch.randn(*shape, generator=gen) * s).to(torch.bfloat16).to(dev)
+    x, ql = mk(T, H), mk(T, R)
+    wq, wk, ww = mk(4096, R, s=R ** -0.5), mk(128, H, s=H ** -0.5), mk(32, H, s=0.01)
+    g, b = mk(128, s=0.1) + 1, mk(128, s=0.1)
+    cache = torch.zeros((2 * T, 128), dtype=torch.bfloat16, device=dev)
+    slot = torch.randperm(2 * T, generator=gen)[:T].to(dev)
+    q = torch.empty((T, 32, 128), dtype=torch.bfloat16, device=dev)
+    w = torch.empty((T, 32), dtype=torch.float32, device=dev)
+    ws = B.workspace(64 << 20, dev)
+    flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    call = lambda: B.indexer_project(x, ql, wq, wk, ww, g, b, 1e-6, cache, slot, q=q, w=w, ws=ws)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        flush_w.zero_()
+        flush_r.max()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        e.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(e))
+    us = float(np.median(ms)) * 1e3
+    flops = 2.0 * T * (4096 * R + 128 * H + 32 * H)
+    weight_bytes = 2.0 * (4096 * R + 128 * H + 32 * H)
+    io_bytes = 2.0 * T * (H + R + 4096 + 128 * 2) + 4.0 * T * 32
+    pk = peaks()
+    tflops = flops / (us * 1e-6) / 1e12
+    gbs = (weight_bytes + io_bytes) / (us * 1e-6) / 1e9
+    bound = "tensor" if flops / (weight_bytes + io_bytes) > pk["bf16_tflops"] * 1e3 / pk["hbm_gbs"] else "hbm"
+    roof = ({"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+             "frac": tflops / pk["bf16_tflops"]} if bound == "tensor" else
+            {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"]})
+    print(json.dumps({"mode": "project", "T": T, "hidden": H, "q_rank": R, "steps": args.steps,
+                      "us_per_call": us, "tflops": tflops, "bytes_per_call": weight_bytes + io_bytes,
+                      "roofline": roof, "gemm": "cuBLASLt (bf16 in, fp32 accumulate)",
+                      "l2": "flushed between calls: 256 MB written, then 256 MB read"}), flush=True)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
@@ -566,6 +617,12 @@ def main():
                     help="time the key LayerNorm fused into the key-cache append of ROWS new keys "
                          "(random distinct slots of a 4*ROWS-row cache) against LayerNorm into a "
                          "staging buffer plus a scatter copy; prints its own JSON line")
+    ap.add_argument("--project", type=int, metavar="T", default=0,
+                    help="time the indexer projections (q, key LayerNorm into the cache, w) of T "
+                         "tokens; prints its own JSON line")
+    ap.add_argument("--hidden", type=int, default=7168, help="--project: attention input width")
+    ap.add_argument("--q-rank", type=int, default=1536,
+                    help="--project: q-LoRA rank (not given by the pages; a stand-in)")
     ap.add_argument("--fused-only", action="store_true",
                     help="time only the fused steps (for profiler captures); prints a short line")
     ap.add_argument("--record-traffic", metavar="CSV",
@@ -578,6 +635,9 @@ def main():
         return
     if args.ln_append:
         run_ln_append(args)
+        return
+    if args.project:
+        run_project(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

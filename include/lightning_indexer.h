@@ -116,6 +116,33 @@ IDX_API idx_status idx_key_layernorm_append(const uint16_t* k_raw, const void* l
                                             const int64_t* slot, int64_t n_rows, void* stream);
 
 /*
+ * Indexer projections from the layer's activations (port notes, indexer
+ * paragraph: the query comes off the normalised q-LoRA projection, the key
+ * from the attention input through the key LayerNorm, and a per-head weight
+ * vector sums the heads). Per token t (weights in the [out, in] layout of a
+ * linear layer; bf16 products accumulated in fp32):
+ *   q[t]             = W_q . q_lora[t]   W_q [32*128, q_rank]  -> q bf16 [T,32,128]
+ *   k_pre[t]         = W_k . x[t]        W_k [128, hidden]     -> bf16 (workspace)
+ *   k_cache[slot[t]] = LayerNorm(k_pre[t]) as idx_key_layernorm_append
+ *   w[t]             = W_w . x[t]        W_w [32, hidden]      -> w fp32 [T,32]
+ * Any scale of the per-head weights is part of W_w. The three products are
+ * plain GEMMs run by cuBLASLt inside the caller's workspace (ws: 256-byte
+ * aligned, idx_indexer_project_workspace_size(T) bytes); the library
+ * allocates nothing. x [T,hidden] and q_lora [T,q_rank] are bf16 row-major;
+ * hidden and q_rank are multiples of 8; matrices 16-byte aligned. slot and
+ * the LayerNorm parameters are as for idx_key_layernorm_append. The first
+ * call creates the process's cuBLASLt handle (host state only).
+ */
+IDX_API size_t idx_indexer_project_workspace_size(int32_t T);
+IDX_API idx_status idx_indexer_project(const uint16_t* x, const uint16_t* q_lora,
+                                       const uint16_t* w_q, const uint16_t* w_k,
+                                       const uint16_t* w_w, const void* ln_w, const void* ln_b,
+                                       int ln_dtype, float eps, int32_t T, int32_t hidden,
+                                       int32_t q_rank, uint16_t* q, uint16_t* k_cache,
+                                       int64_t cache_rows, const int64_t* slot, float* w, void* ws,
+                                       size_t ws_bytes, void* stream);
+
+/*
  * Head scores (indexer paragraph: per-head relu of q_h . k over the causal
  * past, combined with a per-head weight; item (3): no rotary):
  *     scores[t*ld + s] = sum_h w[t,h] * max(sum_d q[t,h,d] * k[cu_k[b]+s, d], 0)

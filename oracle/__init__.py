@@ -116,6 +116,27 @@ def key_layernorm(k_raw_bits, gamma, beta, eps: float):
     return out, y
 
 
+def indexer_project(x_bits, qlora_bits, wq_bits, wk_bits, ww_bits, gamma, beta, eps: float):
+    """The indexer's projections from a layer's activations, in fp64.
+
+    Port notes, indexer paragraph: the query comes off the normalised q-LoRA
+    projection, the key from the attention input through the key LayerNorm,
+    and a per-head weight vector sums the heads. Per token (weights in the
+    [out, in] layout of a linear layer): q = W_q qlora and k_pre = W_k x, each
+    rounded once to bf16 (the 16-bit activations of the model); k = the key
+    LayerNorm of k_pre; w = W_w x, kept in fp64. The products are float64
+    matrix products of the exact bf16 values (a library matmul as one step).
+    Returns (q bits [T,32,128], k bits [T,128], w fp64 [T,32], k_pre bits [T,128]).
+    """
+    x = bf16_bits_to_f64(x_bits)
+    ql = bf16_bits_to_f64(qlora_bits)
+    q = f64_to_bf16_bits(ql @ bf16_bits_to_f64(wq_bits).T).reshape(-1, HEADS, DIM)
+    k_pre = f64_to_bf16_bits(x @ bf16_bits_to_f64(wk_bits).T)
+    w = x @ bf16_bits_to_f64(ww_bits).T
+    k, _ = key_layernorm(k_pre, gamma, beta, eps)
+    return q, k, w, k_pre
+
+
 def scores(q_t_bits, k_seq_bits, w_t, n: int) -> np.ndarray:
     """S[s] = sum_h w[h] relu(q_h . k_s) for s < n, in fp64 (one query)."""
     lib = _load()

@@ -33,7 +33,8 @@ _lock = threading.Lock()
 EXPORTS = ("idx_key_layernorm", "idx_score", "idx_score_workspace_size", "idx_topk",
            "idx_topk_workspace_size", "idx_score_topk", "idx_score_topk_workspace_size",
            "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches",
-           "idx_score_topk_noalloc", "idx_set_wait_limit_ns", "idx_key_layernorm_append")
+           "idx_score_topk_noalloc", "idx_set_wait_limit_ns", "idx_key_layernorm_append",
+           "idx_indexer_project", "idx_indexer_project_workspace_size")
 
 
 class IndexerError(RuntimeError):
@@ -167,6 +168,49 @@ def key_layernorm_append(k_raw: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Te
     _check(fn(_ptr(k_raw), _ptr(ln_w), _ptr(ln_b), pdt, float(eps), _ptr(k_cache),
               k_cache.shape[0], _ptr(slot), k_raw.shape[0], _stream()), "idx_key_layernorm_append")
     return k_cache
+
+
+def indexer_project(x: torch.Tensor, q_lora: torch.Tensor, w_q: torch.Tensor, w_k: torch.Tensor,
+                    w_w: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Tensor, eps: float,
+                    k_cache: torch.Tensor, slot: torch.Tensor, q: torch.Tensor | None = None,
+                    w: torch.Tensor | None = None, ws: torch.Tensor | None = None):
+    """Indexer projections -> (q [T,32,128] bf16, w [T,32] fp32); keys go to k_cache[slot]."""
+    _dev(x, "x", _BF16)
+    _dev(q_lora, "q_lora", _BF16)
+    if x.dim() != 2 or q_lora.dim() != 2 or x.shape[0] != q_lora.shape[0]:
+        raise ValueError("x [T,hidden] and q_lora [T,rank] with the same T")
+    T, hidden, rank = x.shape[0], x.shape[1], q_lora.shape[1]
+    _dev(w_q, "w_q", _BF16, (HEADS * DIM, rank))
+    _dev(w_k, "w_k", _BF16, (DIM, hidden))
+    _dev(w_w, "w_w", _BF16, (HEADS, hidden))
+    if ln_w.dtype != ln_b.dtype:
+        raise TypeError("ln_w and ln_b must share a dtype")
+    _dev(ln_w, "ln_w", _BF16 + _F32, (DIM,))
+    _dev(ln_b, "ln_b", _BF16 + _F32, (DIM,))
+    _dev(k_cache, "k_cache", _BF16)
+    _dev(slot, "slot", (torch.int64,), (T,))
+    if q is None:
+        q = torch.empty((T, HEADS, DIM), dtype=x.dtype, device=x.device)
+    if w is None:
+        w = torch.empty((T, HEADS), dtype=torch.float32, device=x.device)
+    _dev(q, "q", _BF16, (T, HEADS, DIM))
+    _dev(w, "w", _F32, (T, HEADS))
+    L = lib()
+    L.idx_indexer_project_workspace_size.argtypes = [ctypes.c_int32]
+    L.idx_indexer_project_workspace_size.restype = ctypes.c_size_t
+    need = int(L.idx_indexer_project_workspace_size(T))
+    if ws is None:
+        ws = workspace(need, x.device)
+    P = ctypes.c_void_p
+    fn = L.idx_indexer_project
+    fn.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_float, ctypes.c_int32, ctypes.c_int32,
+                   ctypes.c_int32, P, P, ctypes.c_int64, P, P, P, ctypes.c_size_t, P]
+    fn.restype = ctypes.c_int
+    pdt = PARAM_F32 if ln_w.dtype == torch.float32 else PARAM_BF16
+    _check(fn(_ptr(x), _ptr(q_lora), _ptr(w_q), _ptr(w_k), _ptr(w_w), _ptr(ln_w), _ptr(ln_b), pdt,
+              float(eps), T, hidden, rank, _ptr(q), _ptr(k_cache), k_cache.shape[0], _ptr(slot),
+              _ptr(w), _ptr(ws), ws.numel(), _stream()), "idx_indexer_project")
+    return q, w
 
 
 def _batch(q, k, w, q_pos, cu_q, cu_k):

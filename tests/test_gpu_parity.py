@@ -215,6 +215,76 @@ def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
 
 
 # ---------------------------------------------------------------------------
+# projections (q-LoRA -> q, attention input -> key LayerNorm -> cache, -> w)
+# ---------------------------------------------------------------------------
+
+def _proj_inputs(seed, T, hidden, rank, integer):
+    rng = np.random.default_rng(seed)
+    if integer:
+        mk = lambda shape, lo, hi: wl.f32_to_bf16_bits(rng.integers(lo, hi + 1, size=shape).astype(np.float32))
+        x, ql = mk((T, hidden), -2, 2), mk((T, rank), -2, 2)
+        wq, wk, ww = mk((4096, rank), -1, 1), mk((128, hidden), -1, 1), mk((32, hidden), -1, 1)
+    else:
+        mk = lambda shape, s: wl.f32_to_bf16_bits((rng.standard_normal(shape) * s).astype(np.float32))
+        x, ql = mk((T, hidden), 1.0), mk((T, rank), 1.0)
+        wq, wk, ww = mk((4096, rank), rank ** -0.5), mk((128, hidden), hidden ** -0.5), mk((32, hidden), 0.01)
+    g = wl.f32_to_bf16_bits((1 + 0.1 * rng.standard_normal(128)).astype(np.float32))
+    b = wl.f32_to_bf16_bits((0.1 * rng.standard_normal(128)).astype(np.float32))
+    return x, ql, wq, wk, ww, g, b
+
+
+def _proj_run(B, x, ql, wq, wk, ww, g, b, cache_rows, slot):
+    dv = lambda a: torch.from_numpy(a.view(np.int16)).cuda()
+    cache = torch.zeros((cache_rows, 128), dtype=torch.int16, device="cuda")
+    q, w = B.indexer_project(dv(x), dv(ql), dv(wq), dv(wk), dv(ww), dv(g), dv(b), 1e-6, cache,
+                             torch.from_numpy(slot).cuda())
+    return bits_of(q), w.cpu().numpy(), bits_of(cache)
+
+
+def test_indexer_project_integer_inputs_exact(B):
+    T, hidden, rank = 37, 7168, 1536
+    x, ql, wq, wk, ww, g, b = _proj_inputs(41, T, hidden, rank, integer=True)
+    slot = np.random.default_rng(1).permutation(100)[:T].astype(np.int64)
+    q, w, cache = _proj_run(B, x, ql, wq, wk, ww, g, b, 100, slot)
+    rq, rk, rw, rk_pre = oracle.indexer_project(x, ql, wq, wk, ww, oracle.bf16_bits_to_f64(g),
+                                                oracle.bf16_bits_to_f64(b), float(np.float32(1e-6)))
+    assert np.array_equal(q, rq)                    # exact integers, rounded once to bf16
+    assert np.array_equal(w, rw.astype(np.float32))
+    # identical pre-LayerNorm keys on both sides: the key LayerNorm's tolerance
+    beta = oracle.bf16_bits_to_f64(b)
+    _, y = oracle.key_layernorm(rk_pre, oracle.bf16_bits_to_f64(g), beta, float(np.float32(1e-6)))
+    got = cache[slot]
+    dist = bf16_ulp_distance(got, rk)
+    err = np.abs(oracle.bf16_bits_to_f64(got) - y)
+    bound = 2.0 ** -17 * (np.abs(y - beta[None, :]) + np.abs(beta[None, :]))
+    assert not ((dist > 1) & (err > bound)).any()
+    untouched = np.setdiff1d(np.arange(100), slot)
+    assert (cache[untouched] == 0).all()
+
+
+def test_indexer_project_real_valued(B):
+    T, hidden, rank = 64, 1024, 512
+    x, ql, wq, wk, ww, g, b = _proj_inputs(42, T, hidden, rank, integer=False)
+    slot = np.arange(T, dtype=np.int64)
+    q, w, cache = _proj_run(B, x, ql, wq, wk, ww, g, b, T, slot)
+    rq, rk, rw, _ = oracle.indexer_project(x, ql, wq, wk, ww, oracle.bf16_bits_to_f64(g),
+                                           oracle.bf16_bits_to_f64(b), float(np.float32(1e-6)))
+    # one bf16 rounding of an fp32-accumulated sum: 1 ulp, or the fp32
+    # accumulation bound where the sum cancels (sum of |products| x 2^-20)
+    dist = bf16_ulp_distance(q, rq)
+    err = np.abs(oracle.bf16_bits_to_f64(q) - oracle.bf16_bits_to_f64(rq)).reshape(T, -1)
+    mag = np.abs(oracle.bf16_bits_to_f64(ql)) @ np.abs(oracle.bf16_bits_to_f64(wq)).T
+    assert not ((dist.reshape(T, -1) > 1) & (err > 2.0 ** -20 * mag + 2.0 ** -9 * np.abs(
+        oracle.bf16_bits_to_f64(rq).reshape(T, -1)))).any()
+    assert (dist <= 1).mean() > 0.999
+    assert np.allclose(w, rw, rtol=1e-5, atol=1e-6)
+    # a one-ulp flip of a pre-LayerNorm key can move its row's outputs by ~2 ulps
+    d = np.abs(oracle.bf16_bits_to_f64(cache) - oracle.bf16_bits_to_f64(rk))
+    assert (d <= 2.0 ** -6 * np.maximum(np.abs(oracle.bf16_bits_to_f64(rk)), 1.0)).all()
+    assert (cache == rk).mean() > 0.95
+
+
+# ---------------------------------------------------------------------------
 # the whole indexer
 # ---------------------------------------------------------------------------
 

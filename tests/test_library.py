@@ -152,6 +152,31 @@ def test_layernorm_append_host_errors(L):
     assert call(n=0) == 0                               # nothing to do: no device needed
 
 
+def test_indexer_project_host_errors(L):
+    fn = L.idx_indexer_project
+    P = ctypes.c_void_p
+    fn.argtypes = [P] * 7 + [ctypes.c_int, ctypes.c_float, ctypes.c_int32, ctypes.c_int32,
+                             ctypes.c_int32, P, P, ctypes.c_int64, P, P, P, ctypes.c_size_t, P]
+    L.idx_indexer_project_workspace_size.argtypes = [ctypes.c_int32]
+    L.idx_indexer_project_workspace_size.restype = ctypes.c_size_t
+    need = L.idx_indexer_project_workspace_size(4)
+    assert need >= 4 * 256
+
+    def call(**kw):
+        a = dict(T=4, hidden=7168, rank=1536, dt=0, ws_bytes=need, ws=FAKE, x=FAKE)
+        a.update(kw)
+        return fn(a["x"], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["dt"], 1e-6, a["T"], a["hidden"],
+                  a["rank"], FAKE, FAKE, 100, FAKE, FAKE, a["ws"], a["ws_bytes"], NULL)
+    assert call(hidden=7170) == 1       # not a multiple of 8
+    assert call(rank=0) == 1
+    assert call(T=-1) == 1
+    assert call(dt=5) == 1
+    assert call(x=NULL) == 1
+    assert call(ws_bytes=need - 1) == 3
+    assert call(ws=ctypes.c_void_p(4096 + 16)) == 3
+    assert call(T=0) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     from sparse_attention_key_gb300 import binding
     monkeypatch.setattr(binding, "_lib", None)

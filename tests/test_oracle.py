@@ -348,3 +348,48 @@ def test_workloads_shapes_and_pairs():
     assert np.array_equal(w6.q_pos, np.concatenate([np.arange(l - 4, l) for l in lens]))
     assert w6.pairs == int(sum(4 * l - 6 for l in lens))
     assert wl.NAMES[6] == "spec_verify" and wl.by_index(6).T == 64
+
+
+# ---------------------------------------------------------------------------
+# projections (indexer paragraph: q from the normalised q-LoRA, k from the
+# attention input through the key LayerNorm, per-head weights)
+# ---------------------------------------------------------------------------
+
+def _int_bf16_bits(rng, shape, lo, hi):
+    return wl.f32_to_bf16_bits(rng.integers(lo, hi + 1, size=shape).astype(np.float32))
+
+
+def test_projection_integer_inputs_match_int64_matmul():
+    # small integers: every product sum is an exact integer; q and k_pre are
+    # those integers rounded once to bf16, w is the integer itself
+    rng = np.random.default_rng(31)
+    T, hidden, rank = 5, 96, 40
+    x, ql = _int_bf16_bits(rng, (T, hidden), -2, 2), _int_bf16_bits(rng, (T, rank), -2, 2)
+    wq = _int_bf16_bits(rng, (32 * 128, rank), -1, 1)
+    wk = _int_bf16_bits(rng, (128, hidden), -1, 1)
+    ww = _int_bf16_bits(rng, (32, hidden), -1, 1)
+    g, b = np.ones(128), np.zeros(128)
+    q, k, w, k_pre = oracle.indexer_project(x, ql, wq, wk, ww, g, b, 1e-6)
+    xi = wl.bf16_bits_to_f32(x).astype(np.int64)
+    qli = wl.bf16_bits_to_f32(ql).astype(np.int64)
+    q_int = qli @ wl.bf16_bits_to_f32(wq).astype(np.int64).T
+    k_int = xi @ wl.bf16_bits_to_f32(wk).astype(np.int64).T
+    w_int = xi @ wl.bf16_bits_to_f32(ww).astype(np.int64).T
+    assert np.array_equal(w, w_int.astype(np.float64))
+    assert np.array_equal(q.reshape(T, -1), wl.f32_to_bf16_bits(q_int.astype(np.float32)))
+    assert np.array_equal(k_pre, wl.f32_to_bf16_bits(k_int.astype(np.float32)))
+    assert np.array_equal(k, oracle.key_layernorm(k_pre, g, b, 1e-6)[0])
+
+
+def test_projection_identity_weights_select_inputs():
+    # W = [I | 0]: the outputs are the leading inputs themselves
+    rng = np.random.default_rng(32)
+    T, hidden, rank = 3, 160, 4096
+    x = wl.f32_to_bf16_bits(rng.standard_normal((T, hidden)).astype(np.float32))
+    ql = wl.f32_to_bf16_bits(rng.standard_normal((T, rank)).astype(np.float32))
+    eye = lambda n, m: wl.f32_to_bf16_bits(np.eye(n, m, dtype=np.float32))
+    q, k, w, k_pre = oracle.indexer_project(x, ql, eye(4096, rank), eye(128, hidden), eye(32, hidden),
+                                            np.ones(128), np.zeros(128), 1e-6)
+    assert np.array_equal(q.reshape(T, -1), ql)
+    assert np.array_equal(k_pre, x[:, :128])
+    assert np.array_equal(w, wl.bf16_bits_to_f32(x[:, :32]).astype(np.float64))
