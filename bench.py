@@ -186,6 +186,27 @@ def record_traffic(workload: int, csv_path: str):
 
 
 # ---------------------------------------------------------------------------
+# replicas over ranks (the indexer has no exchange step: each rank runs an
+# independent replica of the workload)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(values, world: int, device):
+    """Element-wise maximum of per-rank timings over all ranks (a MAX
+    all-reduce of one float64 vector on `device`; the identity for world 1)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_value(pairs_per_step: int, world: int, steps: int, max_ms: float) -> float:
+    """Pairs per second of the whole job: every rank's pairs over the slowest
+    rank's time."""
+    return pairs_per_step * world * steps / (max_ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # algorithmic work per launch
 # ---------------------------------------------------------------------------
 
@@ -359,17 +380,13 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = float(sum(s.elapsed_time(e) for s, e in zip(e_start, e_end)))
     ok = np.array_equal(h_idx.numpy(), idx.cpu().numpy())
 
-    # max over ranks
-    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], world, dev)
     if rank != 0:
         return
 
     pairs = w.pairs
-    value = pairs * world * args.steps / (total_ms / 1e3)
-    e2e_value = pairs * world * args.steps / (e2e_ms / 1e3)
+    value = whole_job_value(pairs, world, args.steps, total_ms)
+    e2e_value = whole_job_value(pairs, world, args.steps, e2e_ms)
     pk = peaks()
     alg = algorithmic(w)
     kernels = {
