@@ -1,0 +1,70 @@
+"""The workspace entry points inside a CUDA graph.
+
+Serving engines capture a decode step once and replay it. The fused call
+launches only kernels (programmatic dependent launches; the plan kernel clears
+the status word and the selection histograms itself), so it can be captured
+after one direct call has done the per-process set-up. These tests capture it
+in a torch CUDA graph, replay it, change the inputs in place and replay again,
+comparing with direct calls.
+"""
+import numpy as np
+import pytest
+
+from sparse_attention_key_gb300 import workloads as wl
+from tests._util import to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_attention_key_gb300 import build
+    build.build()
+    from sparse_attention_key_gb300 import binding
+    return binding
+
+
+@pytest.mark.parametrize("shape", ["decode", "prefill"])
+def test_fused_call_replays_in_a_cuda_graph(B, shape):
+    if shape == "decode":   # one query per sequence: scorer histogram + cluster selection
+        w = wl.custom(801, q_counts=[1, 1, 1, 1], k_lens=[30000, 14000, 5000, 20000], kind="normal")
+    else:                   # many queries per sequence: 16-query scorer + staged selection
+        w = wl.custom(802, q_counts=[200, 40], k_lens=[4000, 900], kind="normal")
+    d = to_device(w)
+    T = w.T
+    ws = B.workspace(B.score_topk_workspace_size(w.B, T, w.max_len), "cuda")
+    idx = torch.empty((T, 2048), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((T,), dtype=torch.int32, device="cuda")
+    call = lambda: B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"],
+                                w.max_len, idx=idx, cnt=cnt, ws=ws)
+    call()                                   # per-process set-up outside the capture
+    torch.cuda.synchronize()
+    ref_idx, ref_cnt = idx.clone(), cnt.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    idx.fill_(-7)
+    cnt.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(idx, ref_idx) and torch.equal(cnt, ref_cnt)
+    assert B.get_status(ws) == (0, 0)
+    # new weights in place: the replay follows them
+    rng = np.random.default_rng(803)
+    d["w"].copy_(torch.from_numpy(rng.uniform(0, 1.0 / 32, size=(T, 32)).astype(np.float32)))
+    g.replay()
+    torch.cuda.synchronize()
+    got = idx.clone()
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(got, idx)
+    assert not torch.equal(got, ref_idx)
