@@ -157,6 +157,40 @@ __device__ __forceinline__ void select_bin(S& sh, int nbins, uint32_t rank) {
     __syncthreads();
 }
 
+// Shared-memory slot of histogram bin b in a swizzled histogram: the low five
+// bits are XORed with the next five, a bijection that sends bins 32 apart to
+// different banks. Integer-valued scores leave the low key bits zero, so
+// their second and third digits are multiples of 32 or 64; unswizzled, all of
+// them would hit one bank.
+__device__ __forceinline__ uint32_t swz(uint32_t b) { return b ^ ((b >> 5) & 31u); }
+
+// select_bin over a histogram stored at swizzled slots (scalar reads).
+template <int THREADS, class S>
+__device__ __forceinline__ void select_bin_swz(S& sh, int nbins, uint32_t rank) {
+    const int per = nbins / THREADS;
+    const int top = nbins - 1 - (int)threadIdx.x * per;
+    uint32_t s = 0;
+    for (int i = 0; i < per; ++i) s += sh.hist[swz((uint32_t)(top - i))];
+    const uint32_t excl = block_excl_scan<THREADS>(sh, s);
+    if (threadIdx.x == THREADS - 1 && excl + s < rank) {
+        sh.sel_bin = 0;
+        sh.sel_rank = 0;
+    }
+    if (excl < rank && rank <= excl + s) {
+        uint32_t acc = excl;
+        for (int i = 0; i < per; ++i) {
+            const uint32_t c = sh.hist[swz((uint32_t)(top - i))];
+            if (acc + c >= rank) {
+                sh.sel_bin = (uint32_t)(top - i);
+                sh.sel_rank = rank - acc;
+                break;
+            }
+            acc += c;
+        }
+    }
+    __syncthreads();
+}
+
 template <int THREADS>
 __device__ __forceinline__ void zero(uint32_t* p, int64_t n) {
     for (int64_t i = threadIdx.x; i < n; i += THREADS) p[i] = 0;
@@ -327,7 +361,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
             zero<THREADS>(sh.hist, 1 << bits);
             __syncthreads();
             auto add = [&](uint32_t kk) {
-                if ((kk & mask_hi) == prefix) atomicAdd(&sh.hist[(kk >> shift) & bin_mask], 1u);
+                if ((kk & mask_hi) == prefix) atomicAdd(&sh.hist[swz((kk >> shift) & bin_mask)], 1u);
             };
             for (int32_t v = threadIdx.x; v < nvec; v += THREADS) {
                 const uint4 k = reinterpret_cast<const uint4*>(keys)[v];
@@ -335,7 +369,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
             }
             if (threadIdx.x < n - tail0) add(keys[tail0 + threadIdx.x]);
             __syncthreads();
-            select_bin<THREADS>(sh, 1 << bits, rank);
+            select_bin_swz<THREADS>(sh, 1 << bits, rank);
             prefix |= sh.sel_bin << shift;
             rank = sh.sel_rank;
         }
