@@ -288,7 +288,7 @@ __device__ __forceinline__ int64_t row_prologue(int t, const int32_t* __restrict
 // Short rows: staged in shared memory as keys.
 // ---------------------------------------------------------------------------
 template <int THREADS>
-__global__ void __launch_bounds__(THREADS, 4)
+__global__ void __launch_bounds__(THREADS, 5)
 topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ n_valid,
                    bool n_from_pos, int T, int64_t max_len, int K, int32_t* __restrict__ idx,
                    int32_t* __restrict__ cnt, DeviceStatus* status, const int32_t* __restrict__ cu_q,
