@@ -56,7 +56,9 @@ key_layernorm_kernel(const uint4* x, const void* __restrict__ ln_w, const void* 
 #pragma unroll
         for (int i = 0; i < kLnRowsInFlight; ++i) {   // loads first
             const int64_t row = r0 + 2 * i + half;
-            v[i] = row < n_rows ? x[row * 16 + hl] : make_uint4(0u, 0u, 0u, 0u);
+            // raw keys are read once: streaming loads (evict first), so the
+            // LayerNorm output stays in L2 for a scorer that follows
+            v[i] = row < n_rows ? __ldcs(x + row * 16 + hl) : make_uint4(0u, 0u, 0u, 0u);
             dst[i] = row;
             if (kScatter) {
                 const int64_t sr = row < n_rows ? __ldg(slot + row) : -1;
