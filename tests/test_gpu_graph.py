@@ -68,3 +68,43 @@ def test_fused_call_replays_in_a_cuda_graph(B, shape):
     torch.cuda.synchronize()
     assert torch.equal(got, idx)
     assert not torch.equal(got, ref_idx)
+
+
+def test_concurrent_calls_from_several_host_threads(B):
+    # the library's host-side state (device info, shared-memory opt-ins, the
+    # tensor-map encoder) is shared; calls from several threads, each on its
+    # own stream and workspace, must give the results of sequential calls
+    import threading
+    ws_list, outs, refs, errors = [], [], [], []
+    batches = [wl.custom(810 + i, q_counts=[1, 2, 1], k_lens=[9000 + 1000 * i, 20000, 3000],
+                         kind="int2") for i in range(4)]
+    devs = [to_device(w) for w in batches]
+    for w, d in zip(batches, devs):
+        ws_list.append(B.workspace(B.score_topk_workspace_size(w.B, w.T, w.max_len), "cuda"))
+        refs.append(B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len,
+                                 ws=ws_list[-1])[0].clone())
+        outs.append(None)
+    torch.cuda.synchronize()
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream()
+            w, d = batches[i], devs[i]
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    idx, _ = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"],
+                                          w.max_len, ws=ws_list[i])
+                s.synchronize()
+            outs[i] = idx
+        except Exception as e:   # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    for i in range(4):
+        assert torch.equal(outs[i], refs[i]), i
+        assert B.get_status(ws_list[i]) == (0, 0)
