@@ -28,9 +28,11 @@
 //            positions in increasing order, then the first `need` tie positions
 //            in increasing order.
 // Short rows (staged kernel) are copied into shared memory as keys during pass
-// A; every later step reads that copy. Long rows (streamed kernel) are read
-// twice from global memory (pass A and the split); the candidates' keys are
-// gathered from global memory again where needed. No block waits on another.
+// A; every later step reads that copy. Long rows (streamed kernel) are first
+// requested into L2 as a whole (bulk prefetch), then read twice (pass A and the
+// split); the candidates' keys are gathered once into a shared-memory list
+// that digits 2-3 and the mark read (or, when the list would overflow, gathered
+// again at each step). No block waits on another.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -206,6 +208,25 @@ __device__ __forceinline__ uint4 gkeys(const float* row, int32_t v) {
 
 __device__ __forceinline__ uint32_t comp(const uint4& k, int j) {
     return j == 0 ? k.x : j == 1 ? k.y : j == 2 ? k.z : k.w;
+}
+
+// Ask L2 to fetch [p, p + bytes) ahead of the reads (p 16-byte aligned, bytes
+// a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// The first n scores of a 16-byte aligned row (rows hold ld scores, ld a
+// multiple of 4, so the rounded-up request stays inside the row), in 16 KB
+// requests spread over the block's threads.
+template <int THREADS>
+__device__ __forceinline__ void prefetch_row_l2(const float* row, int64_t n) {
+    const int64_t bytes = (n * 4 + 15) & ~(int64_t)15;
+    constexpr int64_t kChunk = 16384;
+    for (int64_t off = (int64_t)threadIdx.x * kChunk; off < bytes; off += (int64_t)THREADS * kChunk) {
+        const int64_t sz = bytes - off < kChunk ? bytes - off : kChunk;
+        prefetch_l2_bulk(reinterpret_cast<const char*>(row) + off, (uint32_t)sz);
+    }
 }
 
 __device__ __forceinline__ void set_bit(uint32_t* bits, int64_t pos) {
@@ -398,8 +419,10 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
 }
 
 // ---------------------------------------------------------------------------
-// Long rows: streamed from global memory (L2), bitmaps in shared memory, or in
-// per-block global scratch when a row's bitmaps do not fit.
+// Long rows: streamed from L2 after a bulk prefetch of the row; bitmaps in
+// shared memory (or in per-block global scratch when a row's bitmaps do not
+// fit), then a shared-memory list of the candidates: positions in increasing
+// order from a block scan of the cand bits' counts, then their keys.
 // ---------------------------------------------------------------------------
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, 2)
@@ -407,17 +430,19 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
                    bool n_from_pos, int T, int64_t max_len, int K, int32_t* __restrict__ idx,
                    int32_t* __restrict__ cnt, DeviceStatus* status, const int32_t* __restrict__ cu_q,
                    const int32_t* __restrict__ cu_k, int B, int64_t nw_cap,
-                   uint32_t* __restrict__ gbits) {
+                   uint32_t* __restrict__ gbits, int32_t list_cap) {
     pdl_wait();
     pdl_launch_dependents();
     constexpr int D1 = 12;                      // digits: bits 31..20, 19..10, 9..0
     constexpr int kD1Shift = 32 - D1;
     using S = TopkSmem<THREADS, D1>;
     __shared__ S sh;
-    extern __shared__ __align__(16) uint32_t dyn[];   // above | tie | cand bitmaps
+    // above | tie | cand bitmaps, then (16-byte aligned) list_cap (key, position) pairs
+    extern __shared__ __align__(16) uint32_t dyn[];
     uint32_t* above = gbits ? gbits + (int64_t)blockIdx.x * 3 * nw_cap : dyn;
     uint32_t* tie = above + nw_cap;
     uint32_t* cand = tie + nw_cap;
+    uint2* list = reinterpret_cast<uint2*>(dyn + (gbits ? 0 : (3 * nw_cap + 3) / 4 * 4));
 
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         int32_t* out = idx + (int64_t)t * K;
@@ -428,6 +453,7 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         const int32_t nvec = n >> 2, tail0 = nvec << 2;
         const int32_t nw = (n + 31) >> 5;
         const float* row = scores + (int64_t)t * ld;
+        prefetch_row_l2<THREADS>(row, n);
 
         // ---- pass A: first digit
         __syncthreads();
@@ -492,7 +518,43 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         }
         __syncthreads();
 
-        // ---- digits 2 and 3 over the candidates (keys gathered from the row)
+        // ---- compact: candidate positions in order (block scan of counts), then their keys
+        const int32_t per = (nw + THREADS - 1) / THREADS;
+        const int32_t w0 = threadIdx.x * per < nw ? threadIdx.x * per : nw;
+        const int32_t w1 = w0 + per < nw ? w0 + per : nw;
+        uint32_t mine = 0;
+        for (int32_t w = w0; w < w1; ++w) mine += __popc(cand[w]);
+        const uint32_t off0 = block_excl_scan<THREADS>(sh, mine);
+        if (threadIdx.x == THREADS - 1) sh.cand_count = off0 + mine;
+        __syncthreads();
+        const uint32_t n_cand = sh.cand_count;
+        const bool listed = n_cand <= (uint32_t)list_cap;
+        if (listed) {
+            uint32_t o = off0;
+            for (int32_t w = w0; w < w1; ++w) {
+                uint32_t m = cand[w];
+                while (m) {
+                    list[o++].y = (uint32_t)((w << 5) + (__ffs(m) - 1));
+                    m &= m - 1u;
+                }
+            }
+            __syncthreads();
+            for (uint32_t i = threadIdx.x; i < n_cand; i += 4 * THREADS) {
+                float x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t ii = i + u * THREADS;
+                    x[u] = ii < n_cand ? __ldg(row + list[ii].y) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t ii = i + u * THREADS;
+                    if (ii < n_cand) list[ii].x = fkey(x[u]);
+                }
+            }
+        }
+
+        // ---- digits 2 and 3 over the candidates (from the list, else gathered from the row)
 #pragma unroll 1
         for (int d = 0; d < 2; ++d) {
             const int shift = d == 0 ? kD3Bits : 0;
@@ -502,13 +564,20 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
             __syncthreads();
             zero<THREADS>(sh.hist, 1 << bits);
             __syncthreads();
-            for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
-                uint32_t m = cand[w];
-                while (m) {
-                    const int32_t p = (w << 5) + (__ffs(m) - 1);
-                    m &= m - 1u;
-                    const uint32_t kk = fkey(__ldg(row + p));
+            if (listed) {
+                for (uint32_t i = threadIdx.x; i < n_cand; i += THREADS) {
+                    const uint32_t kk = list[i].x;
                     if ((kk & mask_hi) == prefix) atomicAdd(&sh.hist[(kk >> shift) & bin_mask], 1u);
+                }
+            } else {
+                for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
+                    uint32_t m = cand[w];
+                    while (m) {
+                        const int32_t p = (w << 5) + (__ffs(m) - 1);
+                        m &= m - 1u;
+                        const uint32_t kk = fkey(__ldg(row + p));
+                        if ((kk & mask_hi) == prefix) atomicAdd(&sh.hist[(kk >> shift) & bin_mask], 1u);
+                    }
                 }
             }
             __syncthreads();
@@ -520,19 +589,27 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         const uint32_t need = rank;   // tau-valued keys kept; every key above tau is kept
 
         // ---- mark: candidates above tau -> above bits, equal -> tie bits
-        for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
-            uint32_t m = cand[w];
-            if (!m) continue;
-            uint32_t a = 0, e = 0;
-            while (m) {
-                const int b = __ffs(m) - 1;
-                m &= m - 1u;
-                const uint32_t kk = fkey(__ldg(row + (w << 5) + b));
-                a |= (kk > tau ? 1u : 0u) << b;
-                e |= (kk == tau ? 1u : 0u) << b;
+        if (listed) {
+            for (uint32_t i = threadIdx.x; i < n_cand; i += THREADS) {
+                const uint2 e = list[i];
+                if (e.x > tau) atomicOr(above + (e.y >> 5), 1u << (e.y & 31));
+                else if (e.x == tau) atomicOr(tie + (e.y >> 5), 1u << (e.y & 31));
             }
-            above[w] |= a;   // this thread owns word w in this step
-            tie[w] = e;
+        } else {
+            for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
+                uint32_t m = cand[w];
+                if (!m) continue;
+                uint32_t a = 0, e = 0;
+                while (m) {
+                    const int b = __ffs(m) - 1;
+                    m &= m - 1u;
+                    const uint32_t kk = fkey(__ldg(row + (w << 5) + b));
+                    a |= (kk > tau ? 1u : 0u) << b;
+                    e |= (kk == tau ? 1u : 0u) << b;
+                }
+                above[w] |= a;   // this thread owns word w in this step
+                tie[w] = e;
+            }
         }
         __syncthreads();
 
@@ -1254,10 +1331,12 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
 // alignment padding).
 constexpr int64_t kBlockSmem = 227 * 1024;
 constexpr int64_t kStreamStaticBound = (int64_t)sizeof(TopkSmem<kStreamThreads, 12>) + 256;
+constexpr int64_t kStreamList = 8192;   // candidates listed in shared memory (64 KB)
 
+// The three bitmaps, rounded up to 16 bytes (the candidate list follows them).
 bool bitmaps_fit_in_smem(int64_t row_cap) {
     const int64_t nw_cap = (row_cap + 31) / 32;
-    return 3 * nw_cap * 4 + kStreamStaticBound <= kBlockSmem;
+    return (3 * nw_cap + 3) / 4 * 16 + kStreamStaticBound <= kBlockSmem;
 }
 
 }  // namespace
@@ -1357,7 +1436,10 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     } else {
         const bool in_smem = bitmaps_fit_in_smem(row_cap);
         if (!in_smem && a.bits_scratch == nullptr) return cudaErrorInvalidValue;
-        const size_t smem = in_smem ? (size_t)(3 * nw_cap * 4) : 0;
+        const int64_t bm_bytes = in_smem ? (3 * nw_cap + 3) / 4 * 16 : 0;
+        const int64_t room = in_smem ? (kBlockSmem - kStreamStaticBound - bm_bytes) / 8 : 0;
+        const int32_t list_cap = (int32_t)(room < 0 ? 0 : room < kStreamList ? room : kStreamList);
+        const size_t smem = (size_t)(bm_bytes + (int64_t)list_cap * 8);
         const int g = in_smem ? grid : (grid < kScratchBlocks ? grid : kScratchBlocks);
         auto kern = topk_stream_kernel<kStreamThreads>;
         const int64_t st = kernel_static_smem((const void*)kern);
@@ -1366,7 +1448,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         e = launch_kernel(kern, dim3(g), dim3(kStreamThreads), smem, stream, 1, a.scores, a.ld,
                           a.n_valid, a.n_from_pos, a.T, a.max_len, a.topk, a.idx, a.cnt, a.status,
-                          a.cu_q, a.cu_k, a.B, nw_cap, in_smem ? nullptr : a.bits_scratch);
+                          a.cu_q, a.cu_k, a.B, nw_cap, in_smem ? nullptr : a.bits_scratch, list_cap);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

@@ -191,9 +191,11 @@ def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
     if lens == "short":
         n_valid = np.concatenate([[0, 1, K - 1 if K > 1 else 0, K, K + 1, 2047, 2048, 2049, 4096],
                                   rng.integers(1, 20000, size=20), [50_000]]).astype(np.int32)
-    elif lens == "mid":   # many rows of 16K..32K positions: clusters of 2 CTAs
+    elif lens == "mid":   # many rows of 16K..30K positions: the streamed kernel
         n_valid = rng.integers(16_000, 30_001, size=400).astype(np.int32)
-        n_valid[:3] = [30_000, 16_385, K + 1]
+        # around the candidate list's capacity (8192): const rows are all candidates
+        n_valid[:10] = [30_000, 16_385, K + 1, 2047, 2048, 2051, 8191, 8192, 8195, 12_289]
+        n_valid[:10] = np.maximum(n_valid[:10], K + 1)
     elif lens == "long":   # few long rows
         n_valid = np.array([70_000, 131_072, 65_537, K + 3, 100_001], np.int32)
         if kind in ("normal", "ties"):
