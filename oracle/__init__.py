@@ -26,6 +26,8 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 HEADS = 32
 DIM = 128
+MLA_DIM = 576    # MLA cache row: 512-wide latent + 64 key dims
+MLA_VDIM = 512
 
 _lib = None
 _lock = threading.Lock()
@@ -63,6 +65,8 @@ def _load():
             lib.oracle_select.restype = i64
             lib.oracle_score_topk.argtypes = [P, P, P, P, P, P, i32, i32, P, P, P, i64, i64, i64]
             lib.oracle_score_topk.restype = ctypes.c_int
+            lib.oracle_sparse_mla.argtypes = [P, P, P, i64, i32, ctypes.c_double, P, P]
+            lib.oracle_sparse_mla.restype = None
             _lib = lib
     return _lib
 
@@ -205,3 +209,49 @@ def score_topk(q_bits, k_bits, w, q_pos, cu_q, cu_k, K: int = 2048, rows=None,
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda r: run(r, r + 1), row_list))
     return idx, cnt, sc
+
+
+# ---------------------------------------------------------------------------
+# sparse MLA attention over the selected positions (the indexer's consumer)
+# ---------------------------------------------------------------------------
+
+def sparse_mla(q_t_bits, cache_bits, rows, scale: float):
+    """Attention of one query token over the selected cache rows, in fp64.
+
+    Port notes (opening paragraph, item (5)) and the TokenSpeed K3 post
+    (section 2, MLA): NoPE latent attention, a 512-wide latent plus 64 key dims
+    per cached token. Per head h: l_j = scale * (q_h . c_j) over the selected
+    rows c_j (576 wide), p = softmax(l), o_h = sum_j p_j c_j[:512],
+    lse_h = log sum_j exp(l_j). ``rows`` are absolute row numbers of
+    ``cache_bits`` [L, 576]; q is [H, 576]. Returns (o [H, 512], lse [H]).
+    """
+    lib = _load()
+    q = _c(q_t_bits, np.uint16).reshape(-1, MLA_DIM)
+    c = _c(cache_bits, np.uint16).reshape(-1, MLA_DIM)
+    r = _c(rows, np.int64).reshape(-1)
+    assert r.size == 0 or (r.min() >= 0 and r.max() < c.shape[0])
+    H = q.shape[0]
+    o = np.empty((H, MLA_VDIM), dtype=np.float64)
+    lse = np.empty(H, dtype=np.float64)
+    lib.oracle_sparse_mla(_ptr(q), _ptr(c), _ptr(r), r.size, H, float(scale), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def sparse_mla_batch(q_bits, cache_bits, idx, cnt, cu_q, cu_k, scale: float, rows=None):
+    """sparse_mla for each query row t of a packed ragged batch.
+
+    The selected positions of row t are idx[t, :cnt[t]], positions inside the
+    row's sequence (cache rows cu_k[b] .. cu_k[b+1]). Returns (o [T, H, 512],
+    lse [T, H]); rows outside ``rows`` (when given) are left NaN.
+    """
+    q = _c(q_bits, np.uint16)
+    T, H = q.shape[0], q.shape[1]
+    cq = np.asarray(cu_q).reshape(-1)
+    ck = np.asarray(cu_k).reshape(-1)
+    o = np.full((T, H, MLA_VDIM), np.nan)
+    lse = np.full((T, H), np.nan)
+    for t in (range(T) if rows is None else rows):
+        b = int(np.searchsorted(cq, t, side="right")) - 1
+        pos = np.asarray(idx[t][:int(cnt[t])], dtype=np.int64)
+        o[t], lse[t] = sparse_mla(q[t], cache_bits, ck[b] + pos, scale)
+    return o, lse

@@ -27,6 +27,10 @@
  *   - oracle_key_layernorm: constant rows, +/-a rows (closed form), and the
  *     fp64 result against torch.nn.functional.layer_norm in float64; the
  *     bf16 rounding against the fp32 round-to-nearest-even bit rule.
+ *   - oracle_sparse_mla: one selected row (o = its latent), identical rows,
+ *     a zero query (o = the mean latent, lse = log n), a large scale (o tends
+ *     to the top-logit row), order of the selected rows, and the result
+ *     against scipy's softmax/logsumexp over a numpy matmul of the rows.
  */
 #include <math.h>
 #include <stdint.h>
@@ -239,4 +243,55 @@ int oracle_score_topk(const uint16_t* q, const uint16_t* k, const float* w, cons
         }
     }
     return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Sparse NoPE MLA attention over the selected positions (one query token)
+ *
+ * The port notes ("Notes from an NVFP4 port of Kimi K3.1 Pro", opening
+ * paragraph and item (5)): the indexer keeps the best 2048 keys for each
+ * full-attention layer, and those layers are NoPE multi-head latent attention
+ * (the 64 "rope" dims are ordinary key dims). The TokenSpeed post on Kimi K3,
+ * section 2 (MLA): per token the cache holds a shared 512-wide latent and a
+ * 64-wide key component, there are 96 heads, and decode moves the query into
+ * the compressed space. Neither page writes the attention out, so this is the
+ * plain reading: head h of the absorbed query q_h (576 = 512 latent + 64 key
+ * dims) attends to the selected cache rows c_j (576 wide),
+ *     l_hj = scale * (q_h . c_j),   p_h = softmax over j of l_h,
+ *     o_h  = sum_j p_hj * c_j[0..512),   lse_h = log sum_j exp(l_hj);
+ * the value of a row is its 512-wide latent and the softmax scale is an
+ * argument. With no selected row, o_h = 0 and lse_h = -infinity.
+ * ------------------------------------------------------------------------- */
+#define MLA_DIM 576    /* cache row: 512 latent + 64 key dims */
+#define MLA_VDIM 512   /* latent (value) part */
+
+void oracle_sparse_mla(const uint16_t* q_t, const uint16_t* cache, const int64_t* rows, int64_t n,
+                       int32_t heads, double scale, double* o, double* lse) {
+    double* logit = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    for (int32_t h = 0; h < heads; ++h) {
+        const uint16_t* qh = q_t + (int64_t)h * MLA_DIM;
+        double* oh = o + (int64_t)h * MLA_VDIM;
+        for (int d = 0; d < MLA_VDIM; ++d) oh[d] = 0.0;
+        if (n <= 0) {
+            lse[h] = -INFINITY;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < n; ++j) {
+            const uint16_t* c = cache + rows[j] * MLA_DIM;
+            double dot = 0.0;
+            for (int d = 0; d < MLA_DIM; ++d) dot += oracle_bf16_to_double(qh[d]) * oracle_bf16_to_double(c[d]);
+            logit[j] = scale * dot;
+            if (logit[j] > m) m = logit[j];
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < n; ++j) sum += exp(logit[j] - m);
+        for (int64_t j = 0; j < n; ++j) {
+            const double p = exp(logit[j] - m) / sum;
+            const uint16_t* c = cache + rows[j] * MLA_DIM;
+            for (int d = 0; d < MLA_VDIM; ++d) oh[d] += p * oracle_bf16_to_double(c[d]);
+        }
+        lse[h] = m + log(sum);
+    }
+    free(logit);
 }

@@ -393,3 +393,97 @@ def test_projection_identity_weights_select_inputs():
     assert np.array_equal(q.reshape(T, -1), ql)
     assert np.array_equal(k_pre, x[:, :128])
     assert np.array_equal(w, wl.bf16_bits_to_f32(x[:, :32]).astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# sparse MLA attention over the selected positions
+# ---------------------------------------------------------------------------
+
+def _mla_inputs(seed, H=4, L=40, qscale=1.0):
+    rng = np.random.default_rng(seed)
+    q = wl.f32_to_bf16_bits((qscale * rng.standard_normal((H, oracle.MLA_DIM))).astype(np.float32))
+    c = wl.f32_to_bf16_bits(rng.standard_normal((L, oracle.MLA_DIM)).astype(np.float32))
+    return q, c
+
+
+def test_mla_single_row_returns_its_latent():
+    q, c = _mla_inputs(1)
+    o, lse = oracle.sparse_mla(q, c, [17], 0.07)
+    lat = oracle.bf16_bits_to_f64(c[17, :oracle.MLA_VDIM])
+    for h in range(q.shape[0]):
+        assert np.array_equal(o[h], lat)
+        dot = float(oracle.bf16_bits_to_f64(q[h]) @ oracle.bf16_bits_to_f64(c[17]))
+        assert lse[h] == pytest.approx(0.07 * dot, rel=1e-12, abs=1e-12)
+
+
+def test_mla_identical_rows_and_zero_query():
+    q, c = _mla_inputs(2)
+    c[5:9] = c[5]          # four identical rows
+    o, lse = oracle.sparse_mla(q, c, [5, 6, 7, 8], 0.1)
+    lat = oracle.bf16_bits_to_f64(c[5, :oracle.MLA_VDIM])
+    np.testing.assert_allclose(o, np.broadcast_to(lat, o.shape), rtol=1e-13, atol=1e-13)
+    # a zero query: every logit is 0, so o is the mean latent and lse = log n
+    rows = [0, 3, 9, 21, 30]
+    oz, lz = oracle.sparse_mla(np.zeros_like(q), c, rows, 0.1)
+    mean = oracle.bf16_bits_to_f64(c[rows, :oracle.MLA_VDIM]).mean(axis=0)
+    np.testing.assert_allclose(oz, np.broadcast_to(mean, oz.shape), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lz, np.log(len(rows)), rtol=1e-14)
+
+
+def test_mla_large_scale_tends_to_the_top_row():
+    q, c = _mla_inputs(3)
+    rows = list(range(0, 40, 3))
+    o, _ = oracle.sparse_mla(q, c, rows, 50.0)
+    qd, cd = oracle.bf16_bits_to_f64(q), oracle.bf16_bits_to_f64(c)
+    for h in range(q.shape[0]):
+        logits = 50.0 * (cd[rows] @ qd[h])
+        i = int(np.argmax(logits))
+        top = cd[rows[i], :oracle.MLA_VDIM]
+        # |o - c_top| = |sum_j p_j (c_j - c_top)| <= (1 - p_top) max_j |c_j - c_top|,
+        # and 1 - p_top <= sum over the other rows of exp(l_j - l_top)
+        rest = np.exp(np.delete(logits, i) - logits[i]).sum()
+        spread = np.abs(cd[rows, :oracle.MLA_VDIM] - top).max()
+        assert np.abs(o[h] - top).max() <= rest * spread + 1e-12
+
+
+def test_mla_row_order_does_not_matter():
+    q, c = _mla_inputs(4)
+    rows = [2, 11, 19, 7, 33, 25]
+    o1, l1 = oracle.sparse_mla(q, c, rows, 0.05)
+    o2, l2 = oracle.sparse_mla(q, c, rows[::-1], 0.05)
+    np.testing.assert_allclose(o1, o2, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, rtol=1e-14)
+
+
+def test_mla_empty_selection():
+    q, c = _mla_inputs(5)
+    o, lse = oracle.sparse_mla(q, c, [], 0.05)
+    assert np.all(o == 0.0) and np.all(np.isneginf(lse))
+
+
+def test_mla_against_scipy_softmax_over_numpy_matmul():
+    """The definition through library routines: a float64 matmul of the
+    selected rows, scipy's softmax and logsumexp, another matmul for o."""
+    special = pytest.importorskip("scipy.special")
+    q, c = _mla_inputs(6, H=8, L=300, qscale=0.5)
+    rows = np.random.default_rng(7).choice(300, size=120, replace=False)
+    scale = 1.0 / np.sqrt(192.0)
+    o, lse = oracle.sparse_mla(q, c, rows, scale)
+    cd = oracle.bf16_bits_to_f64(c)[rows]
+    logits = scale * (oracle.bf16_bits_to_f64(q) @ cd.T)          # [H, n]
+    p = special.softmax(logits, axis=1)
+    np.testing.assert_allclose(o, p @ cd[:, :oracle.MLA_VDIM], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, special.logsumexp(logits, axis=1), rtol=1e-12)
+
+
+def test_mla_batch_maps_positions_through_the_sequence_offsets():
+    q, c = _mla_inputs(8, H=4, L=60)
+    qb = np.stack([q, q[::-1]])                    # two query rows, one per sequence
+    cu_q, cu_k = [0, 1, 2], [0, 25, 60]
+    idx = np.array([[3, 0, 24, -1], [0, 34, 10, -1]], np.int32)
+    cnt = np.array([3, 3], np.int32)
+    o, lse = oracle.sparse_mla_batch(qb, c, idx, cnt, cu_q, cu_k, 0.05)
+    o0, l0 = oracle.sparse_mla(qb[0], c, [3, 0, 24], 0.05)
+    o1, l1 = oracle.sparse_mla(qb[1], c, [25, 59, 35], 0.05)
+    assert np.array_equal(o[0], o0) and np.array_equal(o[1], o1)
+    assert np.array_equal(lse[0], l0) and np.array_equal(lse[1], l1)
