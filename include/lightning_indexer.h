@@ -226,6 +226,38 @@ IDX_API idx_status idx_score_topk_noalloc(const uint16_t* q, const uint16_t* k, 
                                           int32_t* cnt, void* stream);
 
 /*
+ * Sparse NoPE MLA attention over the selected positions (decode; the step that
+ * consumes the indexer's output). The port notes (opening paragraph and item
+ * (5)) say the indexer keeps the best 2048 keys for each full-attention layer
+ * and that those layers are NoPE multi-head latent attention; the TokenSpeed
+ * post on Kimi K3 (section 2, MLA) gives the cache row (a shared 512-wide
+ * latent and a 64-wide key part per token), 96 heads, and decode's query moved
+ * into the compressed space. For query row t of sequence b and head h, with
+ * S_t = idx[t, 0 .. cnt[t]) (sequence-local positions, as idx_score_topk
+ * writes them) and c_s = cache row cu_k[b] + s:
+ *   l_s  = scale * (q[t,h,:] . c_s)   over the 576 dims, s in S_t
+ *   out[t,h,:] = sum_s softmax(l)_s * c_s[0..512)      (fp32 [T,heads,512])
+ *   lse[t,h]   = log sum_s exp(l_s)                   (fp32 [T,heads], natural log)
+ * An empty selection gives out = 0 and lse = -infinity. Arguments:
+ *   q        bf16 [T, heads, 576], the absorbed queries
+ *   cache    bf16 [cache_rows, 576], rows packed by sequence as cu_k says
+ *   idx      int32 [T, topk]; cnt int32 [T] (0 .. topk) valid entries per row
+ *   heads    32, 64 or 96;  topk 1 .. 2048;  scale > 0 and finite
+ * A position outside its sequence is left out of the softmax and reported as
+ * IDX_ERR_DEVICE_ARG in the status word. Queries are split over key ranges
+ * when T is small (partial results in the workspace, merged by a second
+ * kernel); ws is 256-byte aligned and holds idx_sparse_mla_workspace_size(T,
+ * heads, topk) bytes, a size that depends on the current device's SM count.
+ * q and cache are 16-byte aligned. Asynchronous on `stream`; allocates nothing.
+ */
+IDX_API size_t idx_sparse_mla_workspace_size(int32_t T, int32_t heads, int32_t topk);
+IDX_API idx_status idx_sparse_mla(const uint16_t* q, const uint16_t* cache, int64_t cache_rows,
+                                  const int32_t* idx, const int32_t* cnt, const int32_t* cu_q,
+                                  const int32_t* cu_k, int32_t B, int32_t T, int32_t heads,
+                                  int32_t topk, float scale, float* out, float* lse, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/*
  * Device status word of a workspace, written by the kernels of the last call
  * that used it: IDX_OK, IDX_ERR_DEVICE_ARG or IDX_ERR_TIMEOUT. Synchronises
  * `stream` (a blocking read of 8 bytes). *detail (may be NULL) receives the

@@ -34,7 +34,8 @@ EXPORTS = ("idx_key_layernorm", "idx_score", "idx_score_workspace_size", "idx_to
            "idx_topk_workspace_size", "idx_score_topk", "idx_score_topk_workspace_size",
            "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches",
            "idx_score_topk_noalloc", "idx_set_wait_limit_ns", "idx_key_layernorm_append",
-           "idx_indexer_project", "idx_indexer_project_workspace_size")
+           "idx_indexer_project", "idx_indexer_project_workspace_size", "idx_sparse_mla",
+           "idx_sparse_mla_workspace_size")
 
 
 class IndexerError(RuntimeError):
@@ -353,3 +354,58 @@ def set_wait_limit_ns(limit_ns: int) -> int:
     fn.argtypes = [ctypes.c_uint64]
     fn.restype = ctypes.c_uint64
     return int(fn(int(limit_ns)))
+
+
+MLA_DIM = 576    # MLA cache row: 512-wide latent + 64 key dims
+MLA_VDIM = 512
+
+
+def sparse_mla_workspace_size(T: int, heads: int, topk: int) -> int:
+    L = lib()
+    fn = L.idx_sparse_mla_workspace_size
+    fn.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+    fn.restype = ctypes.c_size_t
+    return int(fn(T, heads, topk))
+
+
+def sparse_mla(q, cache, idx, cnt, cu_q, cu_k, scale: float, out: torch.Tensor | None = None,
+               lse: torch.Tensor | None = None, ws: torch.Tensor | None = None):
+    """Sparse MLA attention over the selected positions -> (out [T,H,512] fp32, lse [T,H] fp32).
+
+    q bf16 [T, H, 576]; cache bf16 [rows, 576]; idx int32 [T, topk] and cnt int32 [T]
+    as the indexer writes them; cu_q / cu_k int32 [B+1].
+    """
+    _dev(q, "q", _BF16)
+    _dev(cache, "cache", _BF16)
+    _dev(idx, "idx", _I32)
+    _dev(cnt, "cnt", _I32)
+    _dev(cu_q, "cu_q", _I32)
+    _dev(cu_k, "cu_k", _I32)
+    if q.dim() != 3 or q.shape[2] != MLA_DIM:
+        raise ValueError("q must be [T, heads, 576]")
+    if cache.dim() != 2 or cache.shape[1] != MLA_DIM:
+        raise ValueError("cache must be [rows, 576]")
+    T, H = int(q.shape[0]), int(q.shape[1])
+    if idx.dim() != 2 or idx.shape[0] != T:
+        raise ValueError("idx must be [T, topk]")
+    topk = int(idx.shape[1])
+    _dev(cnt, "cnt", _I32, (T,))
+    B = int(cu_q.numel()) - 1
+    if out is None:
+        out = torch.empty((T, H, MLA_VDIM), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    _dev(out, "out", _F32, (T, H, MLA_VDIM))
+    _dev(lse, "lse", _F32, (T, H))
+    need = sparse_mla_workspace_size(T, H, topk)
+    if ws is None:
+        ws = workspace(need, q.device)
+    L = lib()
+    fn = L.idx_sparse_mla
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    fn.argtypes = [P, P, i64, P, P, P, P, i32, i32, i32, i32, ctypes.c_float, P, P, P, ctypes.c_size_t, P]
+    fn.restype = ctypes.c_int
+    _check(fn(_ptr(q), _ptr(cache), int(cache.shape[0]), _ptr(idx), _ptr(cnt), _ptr(cu_q), _ptr(cu_k),
+              B, T, H, topk, float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream()),
+           "idx_sparse_mla")
+    return out, lse

@@ -313,3 +313,51 @@ idx_status idx_get_status(const void* ws, void* stream, int32_t* detail) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Sparse MLA attention over the selected positions
+// ---------------------------------------------------------------------------
+extern "C" {
+
+size_t idx_sparse_mla_workspace_size(int32_t T, int32_t heads, int32_t topk) {
+    if (T < 0 || (heads != 32 && heads != 64 && heads != 96) || topk < 1 || topk > IDX_TOPK_MAX)
+        return kWsHeader;
+    return kWsHeader + mla_partial_bytes(T, heads, topk);
+}
+
+idx_status idx_sparse_mla(const uint16_t* q, const uint16_t* cache, int64_t cache_rows,
+                          const int32_t* idx, const int32_t* cnt, const int32_t* cu_q,
+                          const int32_t* cu_k, int32_t B, int32_t T, int32_t heads, int32_t topk,
+                          float scale, float* out, float* lse, void* ws, size_t ws_bytes,
+                          void* stream) {
+    g_last_error[0] = 0;
+    if (B < 1) return fail(IDX_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
+    if (T < 0) return fail(IDX_ERR_INVALID_ARG, "T must be >= 0 (got %d)", T);
+    if (heads != 32 && heads != 64 && heads != 96)
+        return fail(IDX_ERR_INVALID_ARG, "heads must be 32, 64 or 96 (got %d)", heads);
+    if (topk < 1 || topk > IDX_TOPK_MAX)
+        return fail(IDX_ERR_INVALID_ARG, "topk must be in [1, %d] (got %d)", IDX_TOPK_MAX, topk);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(IDX_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (cache_rows < 0) return fail(IDX_ERR_INVALID_ARG, "cache_rows must be >= 0");
+    if (!cu_q || !cu_k) return fail(IDX_ERR_INVALID_ARG, "cu_q / cu_k must not be NULL");
+    if (T > 0 && (!q || !idx || !cnt || !out || !lse || (cache_rows > 0 && !cache)))
+        return fail(IDX_ERR_INVALID_ARG, "q, cache, idx, cnt, out and lse must not be NULL");
+    if (!aligned(q, 16) || !aligned(cache, 16) || !aligned(idx, 4) || !aligned(cnt, 4) ||
+        !aligned(out, 16) || !aligned(lse, 4) || !aligned(cu_q, 4) || !aligned(cu_k, 4))
+        return fail(IDX_ERR_INVALID_ARG,
+                    "q, cache and out must be 16-byte aligned; int32 and lse arrays 4-byte");
+    if ((int64_t)T * heads > 0x7fffffffLL)
+        return fail(IDX_ERR_INVALID_ARG, "T * heads must be below 2^31");
+    if (idx_status st = check_ws(ws, ws_bytes, idx_sparse_mla_workspace_size(T, heads, topk))) return st;
+    if (idx_status st = check_device()) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (idx_status st = clear_status(ws, s)) return st;
+    if (T == 0) return IDX_OK;
+    MlaArgs a{q, cache, cache_rows, idx, cnt, cu_q, cu_k, B, T, heads, topk, scale, out, lse,
+              (DeviceStatus*)ws};
+    cudaError_t e = launch_sparse_mla(a, (char*)ws + kWsHeader, s);
+    return e == cudaSuccess ? IDX_OK : cuda_fail(e, "sparse_mla launch");
+}
+
+}  // extern "C"

@@ -138,4 +138,28 @@ uint32_t* topk_split_row_hist(const TopkArgs& a);
 void topk_prepare(TopkArgs* a, void** ptr, size_t* bytes);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
+// Arguments of one sparse MLA call (device pointers, host sizes).
+struct MlaArgs {
+    const uint16_t* q;       // bf16 [T, heads, 576]
+    const uint16_t* cache;   // bf16 [cache_rows, 576]
+    int64_t cache_rows;
+    const int32_t* idx;      // [T, topk]
+    const int32_t* cnt;      // [T]
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int32_t B, T, heads, topk;
+    float scale;
+    float* out;              // fp32 [T, heads, 512]
+    float* lse;              // fp32 [T, heads]
+    DeviceStatus* status;
+};
+
+// Key splits per query row (1: the kernel writes out/lse itself).
+int mla_splits(int32_t T, int32_t topk);
+// Device scratch for the splits' partial results (0 when there is one split).
+size_t mla_partial_bytes(int32_t T, int32_t heads, int32_t topk);
+// The attention kernel, then (several splits) the merge; `partials` holds
+// mla_partial_bytes(T, heads, topk) bytes, 256-byte aligned.
+cudaError_t launch_sparse_mla(const MlaArgs& a, void* partials, cudaStream_t stream);
+
 }  // namespace lidx

@@ -287,3 +287,42 @@ def score_rows(seed: int, T: int, n_valid, ld: int, kind: str = "ties") -> np.nd
             raise ValueError(kind)
         S[t, :n] = v
     return S
+
+
+# ---------------------------------------------------------------------------
+# Sparse MLA attention inputs (the consumer of the indexer's selection)
+# ---------------------------------------------------------------------------
+MLA_DIM = 576     # cache row: 512-wide latent + 64 key dims
+MLA_HEADS = 96
+
+
+def mla_case(seed: int, k_lens, q_per_seq: int = 1, heads: int = MLA_HEADS, topk: int = 2048,
+             n_sel=None, qscale: float = 1.0):
+    """Seeded inputs of one sparse MLA call over a packed ragged batch.
+
+    Sequence b holds k_lens[b] cached rows (bf16 ~ N(0,1), 576 wide) and
+    q_per_seq query rows at its last positions (absorbed queries, bf16 ~
+    N(0, qscale^2)). Each query keeps min(topk, its causal length) distinct
+    positions (or n_sel[t] when given), drawn uniformly and sorted ascending,
+    as the indexer emits them; idx is -1 padded to topk. Returns
+    (q [T,H,576] bits, cache [L,576] bits, idx [T,topk] int32, cnt [T] int32,
+    cu_q, cu_k).
+    """
+    rng = np.random.default_rng(seed)
+    k_lens = np.asarray(k_lens, dtype=np.int64)
+    B = k_lens.size
+    cu_k = np.concatenate([[0], np.cumsum(k_lens)]).astype(np.int32)
+    cu_q = (np.arange(B + 1) * q_per_seq).astype(np.int32)
+    T = B * q_per_seq
+    cache = _normal_bf16(rng, (int(cu_k[-1]), MLA_DIM))
+    q = f32_to_bf16_bits((qscale * rng.standard_normal((T, heads, MLA_DIM))).astype(np.float32))
+    idx = np.full((T, topk), -1, dtype=np.int32)
+    cnt = np.zeros(T, dtype=np.int32)
+    for t in range(T):
+        b = t // q_per_seq
+        n = int(k_lens[b]) - (q_per_seq - 1 - t % q_per_seq)   # causal length of this query
+        m = min(topk, max(n, 0)) if n_sel is None else int(n_sel[t])
+        if m > 0:
+            idx[t, :m] = np.sort(rng.choice(n, size=m, replace=False)).astype(np.int32)
+        cnt[t] = m
+    return q, cache, idx, cnt, cu_q, cu_k

@@ -1,0 +1,126 @@
+"""Sparse MLA attention over the selected positions: CUDA path against the oracle.
+
+Tolerance (derived from the arithmetic): the kernel rounds the softmax weights
+to bf16 before the weighted sum of the latents (relative error <= 2^-9 per
+weight, while the normaliser keeps fp32 weights), accumulates in fp32 and uses
+exp2f. So |out - oracle| <= 2^-8 * max |latent| over the selected rows, and
+lse (from an fp32 sum of at most 2048 terms) within 2e-4.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_key_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from sparse_attention_key_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _run(B, q, cache, idx, cnt, cu_q, cu_k, scale):
+    dv = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a if dt is None else a.view(dt))).cuda()
+    out, lse = B.sparse_mla(dv(q, np.int16), dv(cache, np.int16), dv(idx), dv(cnt), dv(cu_q), dv(cu_k), scale)
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def _check(o_gpu, l_gpu, o_ref, l_ref, cache, idx, cnt, cu_q, cu_k, rows):
+    lat = oracle.bf16_bits_to_f64(cache[:, :512])
+    for t in rows:
+        b = int(np.searchsorted(cu_q, t, side="right")) - 1
+        n = int(cnt[t])
+        if n == 0:
+            assert np.all(o_gpu[t] == 0) and np.all(np.isneginf(l_gpu[t])), f"row {t}"
+            continue
+        vmax = np.abs(lat[cu_k[b] + idx[t, :n]]).max()
+        err = np.abs(o_gpu[t] - o_ref[t]).max()
+        assert err <= 2.0 ** -8 * vmax, f"row {t}: |d out| {err} > {2.0 ** -8 * vmax}"
+        np.testing.assert_allclose(l_gpu[t], l_ref[t], rtol=0, atol=2e-4, err_msg=f"row {t}")
+
+
+@pytest.mark.parametrize("heads", [32, 64, 96])
+def test_mla_small_batches_against_oracle(B, heads):
+    # selections of 0, 1, 17 (one partial tile), 33, 100 rows and full ones
+    lens = [40, 3000, 2100, 5000]
+    n_sel = [0, 1, 17, 33, 100, 2048, 2048, 1500]
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(11 + heads, lens, q_per_seq=2, heads=heads,
+                                                  n_sel=[min(s, l) for s, l in zip(n_sel, np.repeat(lens, 2))])
+    scale = 1.0 / np.sqrt(192.0)
+    o, l = _run(B, q, cache, idx, cnt, cu_q, cu_k, scale)
+    o_ref, l_ref = oracle.sparse_mla_batch(q, cache, idx, cnt, cu_q, cu_k, scale)
+    _check(o, l, o_ref, l_ref, cache, idx, cnt, cu_q, cu_k, range(q.shape[0]))
+
+
+def test_mla_peaked_softmax_rescales_across_tiles(B):
+    """A large scale: the running maximum grows by more than 2^8 between tiles,
+    so the kernel rescales its accumulator."""
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(21, [4096, 2500], q_per_seq=1)
+    for scale in (0.5, 2.0):
+        o, l = _run(B, q, cache, idx, cnt, cu_q, cu_k, scale)
+        o_ref, l_ref = oracle.sparse_mla_batch(q, cache, idx, cnt, cu_q, cu_k, scale)
+        _check(o, l, o_ref, l_ref, cache, idx, cnt, cu_q, cu_k, range(q.shape[0]))
+
+
+def test_mla_many_rows_single_split(B):
+    """T >= the SM count: one CTA per query row writes the result directly."""
+    lens = [3000] * 40
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(31, lens, q_per_seq=4, heads=32, topk=256)
+    scale = 1.0 / np.sqrt(192.0)
+    o, l = _run(B, q, cache, idx, cnt, cu_q, cu_k, scale)
+    rows = list(range(0, q.shape[0], 7)) + [q.shape[0] - 1]
+    o_ref, l_ref = oracle.sparse_mla_batch(q, cache, idx, cnt, cu_q, cu_k, scale, rows=rows)
+    _check(o, l, o_ref, l_ref, cache, idx, cnt, cu_q, cu_k, rows)
+
+
+def test_mla_positions_outside_the_sequence_are_left_out(B):
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(41, [300, 400], q_per_seq=1, topk=64)
+    idx[1, 5] = 400          # one past the sequence
+    idx[1, 9] = -3
+    scale = 0.1
+    dv = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a if dt is None else a.view(dt))).cuda()
+    ws = B.workspace(B.sparse_mla_workspace_size(2, 96, 64), "cuda")
+    out, lse = B.sparse_mla(dv(q, np.int16), dv(cache, np.int16), dv(idx), dv(cnt), dv(cu_q), dv(cu_k),
+                            scale, ws=ws)
+    code, detail = B.get_status(ws)
+    assert code == 6 and detail == 1
+    keep = [p for j, p in enumerate(idx[1, :cnt[1]]) if j not in (5, 9)]
+    o_ref, l_ref = oracle.sparse_mla(q[1], cache, 300 + np.asarray(keep), scale)
+    o, l = out.cpu().numpy()[1], lse.cpu().numpy()[1]
+    vmax = np.abs(oracle.bf16_bits_to_f64(cache[300 + np.asarray(keep), :512])).max()
+    assert np.abs(o - o_ref).max() <= 2.0 ** -8 * vmax
+    np.testing.assert_allclose(l, l_ref, atol=2e-4)
+
+
+def test_mla_consumes_the_indexer_selection(B):
+    """idx_score_topk's output fed straight into the attention."""
+    w = wl.custom(51, q_counts=[1, 1, 1], k_lens=[3000, 5000, 2100], kind="normal", positions="chunk")
+    dv = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a if dt is None else a.view(dt))).cuda()
+    qi, k, wt = dv(w.q, np.int16), dv(w.k, np.int16), dv(w.w)
+    qp, cq, ck = dv(w.q_pos), dv(w.cu_q), dv(w.cu_k)
+    idx, cnt = B.score_topk(qi, k, wt, qp, cq, ck, w.max_len)
+    rng = np.random.default_rng(52)
+    cache = wl.f32_to_bf16_bits(rng.standard_normal((int(w.cu_k[-1]), 576)).astype(np.float32))
+    qm = wl.f32_to_bf16_bits(rng.standard_normal((w.T, 96, 576)).astype(np.float32))
+    out, lse = B.sparse_mla(dv(qm, np.int16), dv(cache, np.int16), idx, cnt, cq, ck, 0.07)
+    idx_h, cnt_h = idx.cpu().numpy(), cnt.cpu().numpy()
+    ref_idx, ref_cnt, _ = oracle.score_topk(w.q, w.k, w.w, w.q_pos, w.cu_q, w.cu_k)
+    assert np.array_equal(cnt_h, ref_cnt)
+    o_ref, l_ref = oracle.sparse_mla_batch(qm, cache, idx_h, cnt_h, w.cu_q, w.cu_k, 0.07)
+    _check(out.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, cache, idx_h, cnt_h, w.cu_q, w.cu_k,
+           range(w.T))
+
+
+def test_mla_decode_batch_full_size(B):
+    """The decode batch's shapes: 8 sequences of 8K..64K cached rows, one query
+    each, 2048 selected rows, 96 heads; every row against the oracle."""
+    lens = [8192, 12288, 16384, 24576, 32768, 40960, 49152, 65536]
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(61, lens)
+    scale = 1.0 / np.sqrt(192.0)
+    o, l = _run(B, q, cache, idx, cnt, cu_q, cu_k, scale)
+    o_ref, l_ref = oracle.sparse_mla_batch(q, cache, idx, cnt, cu_q, cu_k, scale)
+    _check(o, l, o_ref, l_ref, cache, idx, cnt, cu_q, cu_k, range(q.shape[0]))

@@ -177,6 +177,42 @@ def test_indexer_project_host_errors(L):
     assert call(T=0) == 0
 
 
+def test_sparse_mla_host_errors(L):
+    fn = L.idx_sparse_mla
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    fn.argtypes = [P, P, ctypes.c_int64, P, P, P, P, i32, i32, i32, i32, ctypes.c_float, P, P, P,
+                   ctypes.c_size_t, P]
+    L.idx_sparse_mla_workspace_size.argtypes = [i32, i32, i32]
+    L.idx_sparse_mla_workspace_size.restype = ctypes.c_size_t
+    need = L.idx_sparse_mla_workspace_size(8, 96, 2048)
+    assert need >= 256 and need % 256 == 0
+    assert L.idx_sparse_mla_workspace_size(8, 48, 2048) == 256   # unsupported heads: header only
+
+    def call(**kw):
+        a = dict(q=FAKE, cache=FAKE, rows=1000, idx=FAKE, cnt=FAKE, cu_q=FAKE, cu_k=FAKE, B=1, T=8,
+                 H=96, topk=2048, scale=0.07, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=need)
+        a.update(kw)
+        return fn(a["q"], a["cache"], a["rows"], a["idx"], a["cnt"], a["cu_q"], a["cu_k"], a["B"],
+                  a["T"], a["H"], a["topk"], a["scale"], a["out"], a["lse"], a["ws"], a["ws_bytes"],
+                  NULL)
+    assert call(H=48) == 1
+    assert call(H=128) == 1
+    assert call(topk=0) == 1
+    assert call(topk=2049) == 1
+    assert call(scale=0.0) == 1
+    assert call(scale=float("inf")) == 1
+    assert call(B=0) == 1
+    assert call(T=-1) == 1
+    assert call(rows=-5) == 1
+    assert call(q=NULL) == 1
+    assert call(idx=NULL) == 1
+    assert call(cu_k=NULL) == 1
+    assert call(out=ctypes.c_void_p(4096 + 4)) == 1   # out must be 16-byte aligned
+    assert call(ws=NULL) == 3
+    assert call(ws=ctypes.c_void_p(4096 + 16)) == 3
+    assert L.idx_last_error()
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     from sparse_attention_key_gb300 import binding
     monkeypatch.setattr(binding, "_lib", None)
