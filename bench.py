@@ -540,6 +540,83 @@ def run_project(args):
                       "l2": "flushed between calls: 256 MB written, then 256 MB read"}), flush=True)
 
 
+def _mla_lengths(name: str):
+    if name == "decode_batch":
+        return [8192, 12288, 16384, 24576, 32768, 40960, 49152, 65536]
+    if name == "long_decode":
+        w = wl.by_index(5)
+        return list(np.diff(w.cu_k).astype(np.int64))
+    raise ValueError(f"unknown --mla workload {name}")
+
+
+def run_mla(args):
+    """Sparse MLA attention over 2048 selected positions per query (one GPU):
+    96 heads, 576-wide bf16 cache rows; synthetic seeded inputs made on the device."""
+    import torch
+    from sparse_attention_key_gb300 import build as lib_build
+    lib_build.build()
+    from sparse_attention_key_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    lens = _mla_lengths(args.mla)
+    H, K = 96, 2048
+    T, L = len(lens), int(sum(lens))
+    gen = torch.Generator(device=dev).manual_seed(17)
+    cache = torch.empty((L, 576), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, L, 1 << 20):   # N(0,1) rows, in chunks
+        r1 = min(L, r0 + (1 << 20))
+        cache[r0:r1] = torch.randn((r1 - r0, 576), generator=gen, device=dev).to(torch.bfloat16)
+    q = torch.randn((T, H, 576), generator=gen, device=dev).to(torch.bfloat16)
+    idx = torch.full((T, K), -1, dtype=torch.int32, device=dev)
+    for t, n in enumerate(lens):   # distinct positions, ascending, as the indexer emits them
+        idx[t] = torch.randperm(int(n), generator=gen, device=dev)[:K].sort().values.to(torch.int32)
+    cnt = torch.full((T,), K, dtype=torch.int32, device=dev)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+    cu_q = torch.arange(T + 1, dtype=torch.int32, device=dev)
+    scale = 1.0 / np.sqrt(192.0)
+    out = torch.empty((T, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws = B.workspace(B.sparse_mla_workspace_size(T, H, K), dev)
+    flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    call = lambda: B.sparse_mla(q, cache, idx, cnt, cu_q, cu_k, scale, out=out, lse=lse, ws=ws)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    assert B.get_status(ws)[0] == 0
+    n0 = B.kernel_launches()
+    ms = []
+    for _ in range(args.steps):
+        flush_w.zero_()
+        flush_r.max()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        e.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(e))
+    launches = (B.kernel_launches() - n0) // max(args.steps, 1)
+    us = float(np.median(ms)) * 1e3
+    pairs = T * K
+    bytes_alg = pairs * 576 * 2 + T * H * 576 * 2 + T * H * 512 * 4 + T * H * 4 + T * K * 4
+    flops = 2.0 * pairs * H * (576 + 512)
+    pk = peaks()
+    gbs = bytes_alg / (us * 1e-6) / 1e9
+    tflops = flops / (us * 1e-6) / 1e12
+    print(json.dumps({
+        "mode": "sparse_mla", "metric": "sparse MLA (query, selected position) pairs/s",
+        "value": pairs / (us * 1e-6), "unit": "pairs/s", "higher_is_better": True,
+        "config": {"workload": args.mla, "queries": T, "heads": H, "topk": K, "cache_rows": L,
+                   "row": "576 bf16 (512 latent + 64 key dims)", "scale": "1/sqrt(192)"},
+        "steps": args.steps, "us_per_call": us, "gpu_launches_per_call": launches,
+        "dtype": "bf16 in, fp32 accumulate and out",
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "bytes_per_call": bytes_alg},
+        "tensor": {"achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                   "frac": tflops / pk["bf16_tflops"], "flops_per_call": flops},
+        "data": "synthetic, seeded on the device",
+        "l2": "flushed between calls: 256 MB written, then 256 MB read"}), flush=True)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
@@ -640,6 +717,9 @@ def main():
     ap.add_argument("--hidden", type=int, default=7168, help="--project: attention input width")
     ap.add_argument("--q-rank", type=int, default=1536,
                     help="--project: q-LoRA rank (not given by the pages; a stand-in)")
+    ap.add_argument("--mla", choices=["decode_batch", "long_decode"], default=None,
+                    help="time the sparse MLA attention over 2048 selected positions per query "
+                         "(96 heads) on that workload's shapes; prints its own JSON line")
     ap.add_argument("--fused-only", action="store_true",
                     help="time only the fused steps (for profiler captures); prints a short line")
     ap.add_argument("--record-traffic", metavar="CSV",
@@ -655,6 +735,9 @@ def main():
         return
     if args.project:
         run_project(args)
+        return
+    if args.mla:
+        run_mla(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

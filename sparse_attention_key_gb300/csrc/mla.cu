@@ -19,7 +19,7 @@
 //                      tile read a second time as an MN-major operand, P (bf16)
 //                      from shared memory; O^T stays in TMEM (4 x H columns)
 //   warps 1-4  gather the selected rows with 16-byte cp.async into the swizzled
-//              tile layout (two stages), one lane also loads Q by TMA
+//              tile layout (three stages), one lane also loads Q by TMA
 //   warps 5-8  softmax: a TMEM lane is a head, so each thread owns one row of S:
 //              running maximum in the log2 domain, P = exp2(S - m), sum l.
 //              O is rescaled (in TMEM) only when a head's maximum grows by more
@@ -48,9 +48,9 @@ constexpr int kChunks = kMlaDim / 64;           // 64-dim (128-byte) chunks of a
 constexpr int kTileRows = 32;                   // selected rows per tile
 constexpr int kChunkBytes = kTileRows * 128;    // one chunk of a tile
 constexpr int kStageBytes = kChunks * kChunkBytes;
-constexpr int kStages = 2;
-constexpr int kPBytes = 128 * 128;              // P: one 128-byte row per head (64 B used)
-constexpr int kThreads = 288;
+constexpr int kStages = 3;
+constexpr int kPrefetchTiles = 8;               // rows of the tile this far ahead go to L2 early
+constexpr int kThreads = 320;                   // warp 0 MMA1, 1-4 gather, 5-8 softmax, 9 MMA2
 constexpr int kGather = 128;                    // warps 1-4
 constexpr int kSoft = 128;                      // warps 5-8
 constexpr uint32_t kTmemCols = 512;
@@ -63,12 +63,13 @@ struct MlaLayout {
     static constexpr int kQChunk = H * 128;     // a 64-dim chunk of Q (H rows)
     static constexpr int kQBytes = kChunks * kQChunk;
     static constexpr int kC = kQBytes;          // 1024-byte aligned since H % 8 == 0
-    static constexpr int kP = kC + kStages * kStageBytes;
+    static constexpr int kP = kC + kStages * kStageBytes;   // 1024-byte aligned
+    static constexpr int kPBytes = H * 64;      // P: a 64-byte row (32 bf16) per head, 64-byte swizzle
     static constexpr int kF = kP + kPBytes;     // per-head rescale factors [2][128]
     static constexpr int kM = kF + 1024;        // per-head m [128]
     static constexpr int kL = kM + 512;         // per-head l [128]
     static constexpr int kBar = kL + 512;
-    static constexpr int kBytes = kBar + 16 * 8 + 16;
+    static constexpr int kBytes = kBar + 16 * 8 + 16;   // 15 barriers, TMEM slot, flags
     static constexpr uint32_t kOCols = 4 * H;   // O^T: 4 tiles of 128 dims, H columns each
     static constexpr uint32_t kSCol = kOCols;   // S: two buffers of 32 columns
     static_assert(H % 32 == 0 && H >= 32 && H <= 96, "heads: 32, 64 or 96");
@@ -79,12 +80,34 @@ struct MlaLayout {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// 16 bytes of zeros (a source size of 0 reads nothing from global memory).
+__device__ __forceinline__ void cp_async16_zero(uint32_t dst, const void* any_global) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(dst), "l"(any_global) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread has issued so far has landed
+// (the arrival is counted against the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(bar)) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Make this thread's shared-memory writes (st.shared, cp.async) visible to the
 // async proxy that tcgen05.mma reads operands through.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Ask L2 to fetch [p, p + bytes) ahead of the reads (16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 2^x by the hardware approximation (ex2.approx: relative error near 2^-22,
+// well inside the bf16 rounding the weights get next; 2^-inf = +0).
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Barrier `id` over `threads` threads that also ORs a predicate across them.
@@ -113,6 +136,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t 
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Shared-memory descriptor of a K-major operand with the 64-byte swizzle: rows
+// of 64 B (32 bf16), 8-row groups 512 B apart; the 16-byte pieces of row r sit
+// at piece ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                      // leading byte offset (unused here), 16 B
+    d |= (uint64_t)(512 >> 4) << 32;             // stride byte offset: 512 B per 8 rows
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)4 << 61;                      // layout: 64-byte swizzle
     return d;
 }
 
@@ -155,14 +191,17 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
     float* l_s = reinterpret_cast<float*>(smem + Lay::kL);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
     uint64_t* q_full = bars;
-    uint64_t* c_full = bars + 1;    // [2]: a tile gathered (kGather arrivals)
-    uint64_t* c_empty = bars + 3;   // [2]: MMA2 done with the tile
-    uint64_t* s_full = bars + 5;    // [2]: MMA1 wrote S
-    uint64_t* p_full = bars + 7;    // P written (kSoft arrivals)
-    uint64_t* o_done = bars + 8;    // MMA2 of a tile complete
-    uint64_t* end_bar = bars + 9;   // every MMA issued has completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+    uint64_t* c_full = bars + 1;    // [kStages]: a tile gathered (kGather arrivals)
+    uint64_t* c_empty = bars + 4;   // [kStages]: MMA2 done with the tile
+    uint64_t* s_full = bars + 7;    // [2]: MMA1 wrote S
+    uint64_t* p_full = bars + 9;    // P written (kSoft arrivals)
+    uint64_t* o_done = bars + 10;   // MMA2 of a tile complete
+    uint64_t* end_bar = bars + 11;  // every MMA1 issued has completed
+    uint64_t* s_free = bars + 12;   // [2]: the softmax has read S (kSoft arrivals)
+    uint64_t* end_bar2 = bars + 14; // every MMA2 issued has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* seq_of_row = reinterpret_cast<int*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -170,12 +209,17 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
         for (int s = 0; s < kStages; ++s) {
             mbar_init(c_full + s, kGather);
             mbar_init(c_empty + s, 1);
-            mbar_init(s_full + s, 1);
         }
+        mbar_init(s_full, 1);
+        mbar_init(s_full + 1, 1);
         mbar_init(p_full, kSoft);
         mbar_init(o_done, 1);
         mbar_init(end_bar, 1);
+        mbar_init(s_free, kSoft);
+        mbar_init(s_free + 1, kSoft);
+        mbar_init(end_bar2, 1);
         *abort_flag = 0;
+        *seq_of_row = 0;
         fence_mbar_init();
     }
     if (warp == 1 && lane == 0) prefetch_tmap(&tmap_q);
@@ -192,15 +236,12 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
 
     // ---- this CTA's query row, its sequence, and its tiles
     const int t = blockIdx.x / n_split, sp = blockIdx.x % n_split;
-    int b = 0;
-    {
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(cu_q + mid) <= t) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-    }
+    // the sequence holding row t, found by all threads in one round of loads
+    // (no dependent chain as in a binary search)
+    for (int j = threadIdx.x; j < B; j += kThreads)
+        if (__ldg(cu_q + j) <= t && t < __ldg(cu_q + j + 1)) *seq_of_row = j;
+    __syncthreads();
+    const int b = *seq_of_row;
     const int64_t k0 = __ldg(cu_k + b);
     const int64_t len_k = (int64_t)__ldg(cu_k + b + 1) - k0;
     int32_t n_sel = __ldg(cnt + t);
@@ -227,18 +268,25 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
         return p >= 0 && p < len_k ? p : -1;
     };
 
+    constexpr uint32_t kI1 = idesc_bf16_f32(128, kTileRows);
+    constexpr uint32_t kI2 = idesc_bf16_f32(128, H) | (1u << 15);   // A is MN-major
     if (warp == 0) {
-        // ------------------------------------------------------------ MMA issuer
+        // ---------------------------------------------------- MMA1 issuer: S = Q . C^T
         if (lane == 0 && nt > 0) {
-            constexpr uint32_t kI1 = idesc_bf16_f32(128, kTileRows);
-            constexpr uint32_t kI2 = idesc_bf16_f32(128, H) | (1u << 15);   // A is MN-major
-            const uint32_t qa = smem_addr(q_s), ca = smem_addr(c_s), pa = smem_addr(p_s);
-            auto mma1 = [&](int i) -> bool {
-                const int s = i & 1;
-                if (!mbar_wait(c_full + s, (i >> 1) & 1, abort_flag, wait_ns)) {
+            const uint32_t qa = smem_addr(q_s), ca = smem_addr(c_s);
+            bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
+            if (!ok) give_up(20);
+            for (int i = 0; i < nt && ok; ++i) {
+                const int st = i % kStages, s = i & 1;
+                // tile i landed, and S buffer s read by the softmax of tile i-2
+                if (!mbar_wait(c_full + st, (i / kStages) & 1, abort_flag, wait_ns) ||
+                    (i >= 2 && !mbar_wait(s_free + s, ((i >> 1) - 1) & 1, abort_flag, wait_ns))) {
                     give_up(21);
-                    return false;
+                    break;
                 }
+                // the tile was written through cp.async (generic proxy); the MMA
+                // reads it through the async proxy
+                fence_proxy_async_smem();
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + Lay::kSCol + kTileRows * s;
 #pragma unroll 1
@@ -246,40 +294,41 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t a = smem_desc_sw128(qa + c * Lay::kQChunk + k * 32);
-                        const uint64_t bd = smem_desc_sw128(ca + s * kStageBytes + c * kChunkBytes + k * 32);
+                        const uint64_t bd = smem_desc_sw128(ca + st * kStageBytes + c * kChunkBytes + k * 32);
                         tc_mma_bf16(d, a, bd, kI1, (c | k) != 0 ? 1u : 0u);
                     }
                 tc_commit(s_full + s);
-                return true;
-            };
-            if (!mbar_wait(q_full, 0, abort_flag, wait_ns)) {
-                give_up(20);
-            } else if (mma1(0)) {
-                for (int i = 0; i < nt; ++i) {
-                    if (i + 1 < nt && !mma1(i + 1)) break;
-                    if (!mbar_wait(p_full, i & 1, abort_flag, wait_ns)) {
-                        give_up(22);
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t cbase = ca + (i & 1) * kStageBytes;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m)
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            // dims 128m .. 128m+127 = chunks 2m, 2m+1; rows 16k .. 16k+15
-                            const uint64_t a = smem_desc_sw128_mn(cbase + 2 * m * kChunkBytes + k * 2048,
-                                                                  kChunkBytes, 1024);
-                            const uint64_t bd = smem_desc_sw128(pa + k * 32);
-                            tc_mma_bf16(tmem_base + m * H, a, bd, kI2, (i > 0 || k > 0) ? 1u : 0u);
-                        }
-                    tc_commit(c_empty + (i & 1));
-                    tc_commit(o_done);
-                }
             }
-            // every MMA issued has completed before the CTA tears down
-            tc_commit(end_bar);
+            tc_commit(end_bar);   // every MMA1 issued has completed before teardown
             mbar_wait(end_bar, 0, nullptr, kMlaDrainNs);
+        }
+    } else if (warp == 9) {
+        // --------------------------------------------------- MMA2 issuer: O^T += C^T . P^T
+        if (lane == 0 && nt > 0) {
+            const uint32_t ca = smem_addr(c_s), pa = smem_addr(p_s);
+            for (int i = 0; i < nt; ++i) {
+                // P(i) written (the softmax of tile i saw S(i): MMA1(i) is complete)
+                if (!mbar_wait(p_full, i & 1, abort_flag, wait_ns)) {
+                    give_up(22);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t cbase = ca + (i % kStages) * kStageBytes;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        // dims 128m .. 128m+127 = chunks 2m, 2m+1; rows 16k .. 16k+15
+                        const uint64_t a = smem_desc_sw128_mn(cbase + 2 * m * kChunkBytes + k * 2048,
+                                                              kChunkBytes, 1024);
+                        const uint64_t bd = smem_desc_sw64(pa + k * 32);
+                        tc_mma_bf16(tmem_base + m * H, a, bd, kI2, (i > 0 || k > 0) ? 1u : 0u);
+                    }
+                tc_commit(c_empty + (i % kStages));
+                tc_commit(o_done);
+            }
+            tc_commit(end_bar2);
+            mbar_wait(end_bar2, 0, nullptr, kMlaDrainNs);
         }
     } else if (warp <= 4) {
         // ------------------------------------------------------------ gather
@@ -291,20 +340,35 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
             for (int c = 0; c < kChunks; ++c)
                 tma_load_2d(smem_addr(q_s + c * Lay::kQChunk), &tmap_q, q_full, c * 64, t * H);
         }
-        int issued = 0;
+        // Every write of a tile (rows, and zeros for rows left out) is a cp.async
+        // whose landing the tile's barrier tracks (arrive.noinc): the producer
+        // never waits for its own copies, only for a free stage. The rows
+        // kPrefetchTiles tiles ahead are requested into L2 meanwhile.
+        auto prefetch_tile = [&](int i) {
+            if (q4 != 0 || i >= nt) return;
+            const int32_t pp = position((tile0 + i) * kTileRows + r);
+            if (pp >= 0) prefetch_l2_bulk(cache + (k0 + pp) * kMlaDim, kMlaDim * 2);
+        };
+        {   // tiles 1 .. kPrefetchTiles-1: positions loaded together, then the requests
+            int32_t pp[kPrefetchTiles];
+#pragma unroll
+            for (int i = 1; i < kPrefetchTiles; ++i)
+                pp[i] = q4 == 0 && i < nt ? position((tile0 + i) * kTileRows + r) : -1;
+#pragma unroll
+            for (int i = 1; i < kPrefetchTiles; ++i)
+                if (pp[i] >= 0) prefetch_l2_bulk(cache + (k0 + pp[i]) * kMlaDim, kMlaDim * 2);
+        }
+        int32_t pos_next = nt > 0 ? position(tile0 * kTileRows + r) : -1;
         for (int i = 0; i < nt; ++i) {
-            const int s = i & 1;
-            if (i >= 1) {   // tile i-1 has landed: publish it before waiting for a free stage
-                cp_async_wait_all();
-                fence_proxy_async_smem();
-                mbar_arrive(c_full + ((i - 1) & 1));
-            }
-            if (i >= 2 && !mbar_wait(c_empty + s, ((i >> 1) - 1) & 1, abort_flag, wait_ns)) {
+            const int s = i % kStages;
+            // this row's position in tile i, loaded one iteration early
+            const int32_t pos = pos_next;
+            pos_next = i + 1 < nt ? position((tile0 + i + 1) * kTileRows + r) : -1;
+            if (i >= kStages && !mbar_wait(c_empty + s, (i / kStages - 1) & 1, abort_flag, wait_ns)) {
                 give_up(23);
                 break;
             }
             const int32_t j = (tile0 + i) * kTileRows + r;
-            const int32_t pos = position(j);
             if (j < n_sel && pos < 0 && q4 == 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
             const uint8_t* src =
                 pos >= 0 ? reinterpret_cast<const uint8_t*>(cache + (k0 + pos) * kMlaDim) : nullptr;
@@ -313,20 +377,16 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
             for (int m = 0; m < kChunks * 8 / 4; ++m) {
                 const int piece = q4 + 4 * m;            // 16-byte piece of the 1152-byte row
                 const int c = piece >> 3, jj = piece & 7;
-                uint8_t* dst = row_dst + c * kChunkBytes + ((jj ^ (r & 7)) << 4);
-                if (src) cp_async16(smem_addr(dst), src + c * 128 + jj * 16);
-                else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t dst = smem_addr(row_dst + c * kChunkBytes + ((jj ^ (r & 7)) << 4));
+                if (src) cp_async16(dst, src + c * 128 + jj * 16);
+                else cp_async16_zero(dst, cache);
             }
-            cp_async_commit();
-            issued = i + 1;
+            cp_async_arrive_noinc(c_full + s);
+            prefetch_tile(i + kPrefetchTiles);   // after the copies: its load does not delay them
         }
-        cp_async_wait_all();
-        if (issued == nt && nt > 0) {
-            fence_proxy_async_smem();
-            mbar_arrive(c_full + ((nt - 1) & 1));
-        }
+        cp_async_wait_all();   // nothing of this thread in flight when the CTA ends
         if (g == 0 && nt > 0) mbar_wait(q_full, 0, nullptr, kMlaDrainNs);   // Q landed before exit
-    } else {
+    } else if (warp <= 8) {
         // ------------------------------------------------------------ softmax
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;   // head = TMEM lane of S
@@ -348,6 +408,8 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
             uint32_t v[32];
             tmem_ld_x32(lane_base + Lay::kSCol + kTileRows * s, v);
             tmem_ld_wait(v);
+            tc_fence_before_sync();
+            mbar_arrive(s_free + s);   // MMA1 of tile i+2 may overwrite this buffer
             float tmax = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 32; ++c)
@@ -366,7 +428,7 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 p[c] = ((vmask >> c) & 1u) && m_used > -INFINITY
-                           ? exp2f(__uint_as_float(v[c]) * scale_log2 - m_used)
+                           ? ex2_fast(__uint_as_float(v[c]) * scale_log2 - m_used)
                            : 0.f;
                 psum += p[c];
             }
@@ -400,15 +462,15 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
                     }
                 tmem_st_wait();
             }
-            if (h < H) {   // P row h: 32 bf16 = four 16-byte pieces of the 128-byte swizzled row
-                uint8_t* prow = p_s + h * 128;
+            if (h < H) {   // P row h: 32 bf16 = four 16-byte pieces of a 64-byte swizzled row
+                uint8_t* prow = p_s + h * 64;
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const uint4 w = make_uint4(f32x2_to_bf16x2_rn(p[8 * jj + 0], p[8 * jj + 1]),
                                                f32x2_to_bf16x2_rn(p[8 * jj + 2], p[8 * jj + 3]),
                                                f32x2_to_bf16x2_rn(p[8 * jj + 4], p[8 * jj + 5]),
                                                f32x2_to_bf16x2_rn(p[8 * jj + 6], p[8 * jj + 7]));
-                    *reinterpret_cast<uint4*>(prow + ((jj ^ (h & 7)) << 4)) = w;
+                    *reinterpret_cast<uint4*>(prow + ((jj ^ ((h >> 1) & 3)) << 4)) = w;
                 }
             }
             fence_proxy_async_smem();
@@ -476,33 +538,59 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
 }
 
 // out[t,h,:] and lse[t,h] from the splits' (O, m, l): weights 2^(m_s - M)
-// with M the largest m among the splits that saw any row (l_s > 0).
+// with M the largest m among the splits that saw any row (l_s > 0). One block
+// per (t, h); the first warp finds the weights, then each thread sums one
+// float4 of dims over the splits with independent loads.
+constexpr int kMaxSplits = 32;
+
 __global__ void __launch_bounds__(128)
 sparse_mla_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int n_split,
                         int H, float* __restrict__ out, float* __restrict__ lse) {
+    __shared__ float wts[kMaxSplits];
+    __shared__ float inv_l;
     pdl_wait();
     pdl_launch_dependents();
     const int64_t th = blockIdx.x;   // t * H + h
     const int64_t t = th / H, h = th % H;
-    float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) {
-        const float* ml = part_ml + ((t * n_split + s) * H + h) * 2;
-        if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
-    }
-    float L = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-        const float* ml = part_ml + ((t * n_split + s) * H + h) * 2;
-        if (ml[1] > 0.f) L += exp2f(ml[0] - M) * ml[1];
-    }
-    for (int d = threadIdx.x; d < kMlaV; d += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < n_split; ++s) {
-            const float* ml = part_ml + ((t * n_split + s) * H + h) * 2;
-            if (ml[1] > 0.f) acc += exp2f(ml[0] - M) * part_o[((t * n_split + s) * H + h) * kMlaV + d];
+    if (threadIdx.x < 32) {
+        const int s = threadIdx.x;
+        float m = -INFINITY, l = 0.f;
+        if (s < n_split) {
+            const float2 ml = *reinterpret_cast<const float2*>(part_ml + ((t * n_split + s) * H + h) * 2);
+            if (ml.y > 0.f) {
+                m = ml.x;
+                l = ml.y;
+            }
         }
-        out[th * kMlaV + d] = L > 0.f ? acc / L : 0.f;
+        float M = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float w = l > 0.f ? exp2f(m - M) : 0.f;
+        float L = w * l;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        wts[s] = w;
+        if (s == 0) {
+            inv_l = L > 0.f ? 1.f / L : 0.f;
+            lse[th] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        }
     }
-    if (threadIdx.x == 0) lse[th] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    __syncthreads();
+    const int d4 = threadIdx.x;   // dims 4*d4 .. 4*d4+3
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s = 0; s < n_split; ++s) {
+        const float w = wts[s];
+        if (w != 0.f) {
+            const float4 o = *reinterpret_cast<const float4*>(part_o + ((t * n_split + s) * H + h) * kMlaV + 4 * d4);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+        }
+    }
+    const float il = inv_l;
+    *reinterpret_cast<float4*>(out + th * kMlaV + 4 * d4) = make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
 }
 
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
@@ -539,14 +627,25 @@ cudaError_t launch_h(const MlaArgs& a, const CUtensorMap& map, int tps, int n_sp
 
 }  // namespace
 
+// Splits per query row: the fewest that minimise waves x (tiles per split + 2),
+// one CTA per SM and about two tiles' worth of fixed cost per CTA (Q load,
+// pipeline fill, result write); at least two tiles per split.
 int mla_splits(int32_t T, int32_t topk) {
-    const int tiles = (topk + kTileRows - 1) / kTileRows;
-    const int sms = device_info().sm_count > 0 ? device_info().sm_count : 1;
+    const int64_t tiles = (topk + kTileRows - 1) / kTileRows;
+    const int64_t sms = device_info().sm_count > 0 ? device_info().sm_count : 1;
     if (T <= 0) return 1;
-    int s = (int)((sms + T - 1) / T);   // about one CTA per SM
-    const int cap = tiles / 2 > 0 ? tiles / 2 : 1;   // at least two tiles per split
-    s = s < 1 ? 1 : s > cap ? cap : s;
-    return s;
+    int64_t cap = tiles / 2 > 0 ? tiles / 2 : 1;
+    if (cap > kMaxSplits) cap = kMaxSplits;
+    int64_t best = 1, best_cost = INT64_MAX;
+    for (int64_t s = 1; s <= cap; ++s) {
+        const int64_t waves = ((int64_t)T * s + sms - 1) / sms;
+        const int64_t cost = waves * ((tiles + s - 1) / s + 2);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return (int)best;
 }
 
 size_t mla_partial_bytes(int32_t T, int32_t heads, int32_t topk) {
