@@ -12,16 +12,19 @@
 //
 // One CTA per (query row, range of 32-row tiles of its selection), on the
 // 5th-generation tensor cores:
-//   warp 0     TMEM allocation; one lane issues the MMAs:
-//                MMA1  S[128 heads (rows >= H unused), 32 rows] = Q . C^T, K = 576
-//                      (Q resident in shared memory, 128-byte swizzle, K-major)
-//                MMA2  O^T[512 dims, H] += C^T . P^T, K = 32 rows: the gathered
-//                      tile read a second time as an MN-major operand, P (bf16)
-//                      from shared memory; O^T stays in TMEM (4 x H columns)
+//   warp 0     TMEM allocation; one lane issues MMA1:
+//                S[128 heads (rows >= H unused), 32 rows] = Q . C^T, K = 576
+//                (Q resident in shared memory, 128-byte swizzle, K-major)
+//   warp 9     one lane issues MMA2:
+//                O^T[512 dims, H] += C^T . P^T, K = 32 rows: the gathered tile
+//                read a second time as an MN-major operand, P (bf16, 64-byte
+//                swizzle) from shared memory; O^T stays in TMEM (4 x H columns)
 //   warps 1-4  gather the selected rows with 16-byte cp.async into the swizzled
-//              tile layout (three stages), one lane also loads Q by TMA
+//              tile layout (three stages); each tile's barrier tracks the
+//              copies' landing (cp.async.mbarrier.arrive.noinc), rows 8 tiles
+//              ahead are bulk-prefetched into L2; one lane loads Q by TMA
 //   warps 5-8  softmax: a TMEM lane is a head, so each thread owns one row of S:
-//              running maximum in the log2 domain, P = exp2(S - m), sum l.
+//              running maximum in the log2 domain, P = 2^(S - m), sum l.
 //              O is rescaled (in TMEM) only when a head's maximum grows by more
 //              than 2^8, so the scale of O and l may lag the true maximum; both
 //              carry the same factor, and the result is unchanged.
