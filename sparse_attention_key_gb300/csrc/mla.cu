@@ -20,9 +20,10 @@
 //                read a second time as an MN-major operand, P (bf16, 64-byte
 //                swizzle) from shared memory; O^T stays in TMEM (4 x H columns)
 //   warps 1-4  gather the selected rows with 16-byte cp.async into the swizzled
-//              tile layout (three stages); each tile's barrier tracks the
-//              copies' landing (cp.async.mbarrier.arrive.noinc), rows 8 tiles
-//              ahead are bulk-prefetched into L2; one lane loads Q by TMA
+//              tile layout (three stages; 8 threads per row, so a warp copies
+//              4 rows x 128 contiguous bytes per instruction); each tile's
+//              barrier tracks the copies' landing (cp.async.mbarrier.arrive
+//              .noinc); one lane loads Q by TMA
 //   warps 5-8  softmax: a TMEM lane is a head, so each thread owns one row of S:
 //              running maximum in the log2 domain, P = 2^(S - m), sum l.
 //              O is rescaled (in TMEM) only when a head's maximum grows by more
@@ -52,7 +53,6 @@ constexpr int kTileRows = 32;                   // selected rows per tile
 constexpr int kChunkBytes = kTileRows * 128;    // one chunk of a tile
 constexpr int kStageBytes = kChunks * kChunkBytes;
 constexpr int kStages = 3;
-constexpr int kPrefetchTiles = 8;               // rows of the tile this far ahead go to L2 early
 constexpr int kThreads = 320;                   // warp 0 MMA1, 1-4 gather, 5-8 softmax, 9 MMA2
 constexpr int kGather = 128;                    // warps 1-4
 constexpr int kSoft = 128;                      // warps 5-8
@@ -97,12 +97,6 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // async proxy that tcgen05.mma reads operands through.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Ask L2 to fetch [p, p + bytes) ahead of the reads (16-byte aligned, bytes a
-// multiple of 16).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // 2^x by the hardware approximation (ex2.approx: relative error near 2^-22,
@@ -336,7 +330,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
     } else if (warp <= 4) {
         // ------------------------------------------------------------ gather
         const int g = threadIdx.x - 32;   // 0 .. 127
-        const int r = g >> 2, q4 = g & 3; // tile row, quarter of its 16-byte pieces
         if (g == 0 && nt > 0) {
             mbar_arrive_expect_tx(q_full, Lay::kQBytes);
 #pragma unroll 1
@@ -345,47 +338,39 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
         }
         // Every write of a tile (rows, and zeros for rows left out) is a cp.async
         // whose landing the tile's barrier tracks (arrive.noinc): the producer
-        // never waits for its own copies, only for a free stage. The rows
-        // kPrefetchTiles tiles ahead are requested into L2 meanwhile.
-        auto prefetch_tile = [&](int i) {
-            if (q4 != 0 || i >= nt) return;
-            const int32_t pp = position((tile0 + i) * kTileRows + r);
-            if (pp >= 0) prefetch_l2_bulk(cache + (k0 + pp) * kMlaDim, kMlaDim * 2);
-        };
-        {   // tiles 1 .. kPrefetchTiles-1: positions loaded together, then the requests
-            int32_t pp[kPrefetchTiles];
-#pragma unroll
-            for (int i = 1; i < kPrefetchTiles; ++i)
-                pp[i] = q4 == 0 && i < nt ? position((tile0 + i) * kTileRows + r) : -1;
-#pragma unroll
-            for (int i = 1; i < kPrefetchTiles; ++i)
-                if (pp[i] >= 0) prefetch_l2_bulk(cache + (k0 + pp[i]) * kMlaDim, kMlaDim * 2);
-        }
-        int32_t pos_next = nt > 0 ? position(tile0 * kTileRows + r) : -1;
+        // never waits for its own copies, only for a free stage. (Bulk L2
+        // prefetches of the rows of later tiles were measured slower: they
+        // compete with the gathers.)
+        // 8 threads per row: a warp copies 4 rows x 128 contiguous bytes per instruction
+        const int r8 = g >> 3, q8 = g & 7;   // rows r8 and r8 + 16
+        int32_t pn0 = nt > 0 ? position(tile0 * kTileRows + r8) : -1;
+        int32_t pn1 = nt > 0 ? position(tile0 * kTileRows + r8 + 16) : -1;
         for (int i = 0; i < nt; ++i) {
             const int s = i % kStages;
-            // this row's position in tile i, loaded one iteration early
-            const int32_t pos = pos_next;
-            pos_next = i + 1 < nt ? position((tile0 + i + 1) * kTileRows + r) : -1;
+            const int32_t p0 = pn0, p1 = pn1;
+            pn0 = i + 1 < nt ? position((tile0 + i + 1) * kTileRows + r8) : -1;
+            pn1 = i + 1 < nt ? position((tile0 + i + 1) * kTileRows + r8 + 16) : -1;
             if (i >= kStages && !mbar_wait(c_empty + s, (i / kStages - 1) & 1, abort_flag, wait_ns)) {
                 give_up(23);
                 break;
             }
-            const int32_t j = (tile0 + i) * kTileRows + r;
-            if (j < n_sel && pos < 0 && q4 == 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
-            const uint8_t* src =
-                pos >= 0 ? reinterpret_cast<const uint8_t*>(cache + (k0 + pos) * kMlaDim) : nullptr;
-            uint8_t* row_dst = c_s + s * kStageBytes + r * 128;
-#pragma unroll 6
-            for (int m = 0; m < kChunks * 8 / 4; ++m) {
-                const int piece = q4 + 4 * m;            // 16-byte piece of the 1152-byte row
-                const int c = piece >> 3, jj = piece & 7;
-                const uint32_t dst = smem_addr(row_dst + c * kChunkBytes + ((jj ^ (r & 7)) << 4));
-                if (src) cp_async16(dst, src + c * 128 + jj * 16);
-                else cp_async16_zero(dst, cache);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int rr = r8 + 16 * h2;
+                const int32_t pos = h2 == 0 ? p0 : p1;
+                const int32_t j = (tile0 + i) * kTileRows + rr;
+                if (j < n_sel && pos < 0 && q8 == 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
+                const uint8_t* src =
+                    pos >= 0 ? reinterpret_cast<const uint8_t*>(cache + (k0 + pos) * kMlaDim) : nullptr;
+                uint8_t* row_dst = c_s + s * kStageBytes + rr * 128;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const uint32_t dst = smem_addr(row_dst + c * kChunkBytes + ((q8 ^ (rr & 7)) << 4));
+                    if (src) cp_async16(dst, src + c * 128 + q8 * 16);
+                    else cp_async16_zero(dst, cache);
+                }
             }
             cp_async_arrive_noinc(c_full + s);
-            prefetch_tile(i + kPrefetchTiles);   // after the copies: its load does not delay them
         }
         cp_async_wait_all();   // nothing of this thread in flight when the CTA ends
         if (g == 0 && nt > 0) mbar_wait(q_full, 0, nullptr, kMlaDrainNs);   // Q landed before exit
