@@ -108,3 +108,41 @@ def test_concurrent_calls_from_several_host_threads(B):
     for i in range(4):
         assert torch.equal(outs[i], refs[i]), i
         assert B.get_status(ws_list[i]) == (0, 0)
+
+
+def test_sparse_mla_replays_in_a_cuda_graph(B):
+    """The attention over the selection (memset of the status word, attention,
+    merge) captured once and replayed, following new query values in place."""
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(811, [9000, 3000, 20000], q_per_seq=1)
+    dv = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a if dt is None else a.view(dt))).cuda()
+    dq, dc, di, dn, dcq, dck = dv(q, np.int16), dv(cache, np.int16), dv(idx), dv(cnt), dv(cu_q), dv(cu_k)
+    T, H = q.shape[0], q.shape[1]
+    out = torch.empty((T, H, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = B.workspace(B.sparse_mla_workspace_size(T, H, 2048), "cuda")
+    call = lambda: B.sparse_mla(dq, dc, di, dn, dcq, dck, 0.072, out=out, lse=lse, ws=ws)
+    call()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = out.clone(), lse.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    out.fill_(7.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    assert B.get_status(ws) == (0, 0)
+    q2 = wl.f32_to_bf16_bits(np.random.default_rng(812).standard_normal(q.shape).astype(np.float32))
+    dq.copy_(dv(q2, np.int16))
+    g.replay()
+    torch.cuda.synchronize()
+    got = out.clone()
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(got, out) and not torch.equal(got, ref_out)

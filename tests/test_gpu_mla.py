@@ -124,3 +124,31 @@ def test_mla_decode_batch_full_size(B):
     o, l = _run(B, q, cache, idx, cnt, cu_q, cu_k, scale)
     o_ref, l_ref = oracle.sparse_mla_batch(q, cache, idx, cnt, cu_q, cu_k, scale)
     _check(o, l, o_ref, l_ref, cache, idx, cnt, cu_q, cu_k, range(q.shape[0]))
+
+
+def test_mla_bad_counts_and_empty_sequences(B):
+    """A count above topk is reported (status, that row's output zero, lse
+    -inf); an empty sequence and an empty selection change nothing else."""
+    lens = [5000, 0, 3000, 2500]
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(71, [5000, 1, 3000, 2500], q_per_seq=1, topk=256)
+    cu_k = np.array([0, 5000, 5000, 8000, 10500], np.int32)   # sequence 1: no cached rows
+    cu_q = np.array([0, 1, 1, 2, 3], np.int32)                # ... and no query rows
+    q = q[[0, 2, 3]]
+    idx = idx[[0, 2, 3]]
+    cnt = cnt[[0, 2, 3]].copy()
+    cache = cache[:10500]
+    cnt[1] = 0          # an empty selection
+    cnt[2] = 300        # above topk = 256
+    dv = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a if dt is None else a.view(dt))).cuda()
+    ws = B.workspace(B.sparse_mla_workspace_size(3, 96, 256), "cuda")
+    out, lse = B.sparse_mla(dv(q, np.int16), dv(cache, np.int16), dv(idx), dv(cnt), dv(cu_q), dv(cu_k),
+                            0.07, ws=ws)
+    code, detail = B.get_status(ws)
+    assert code == 6 and detail == 2
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.all(o[1] == 0) and np.all(np.isneginf(l[1]))
+    assert np.all(o[2] == 0) and np.all(np.isneginf(l[2]))
+    o_ref, l_ref = oracle.sparse_mla(q[0], cache, idx[0, :cnt[0]], 0.07)
+    vmax = np.abs(oracle.bf16_bits_to_f64(cache[idx[0, :cnt[0]], :512])).max()
+    assert np.abs(o[0] - o_ref).max() <= 2.0 ** -8 * vmax
+    np.testing.assert_allclose(l[0], l_ref, atol=2e-4)
