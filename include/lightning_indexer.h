@@ -280,8 +280,9 @@ IDX_API uint64_t idx_kernel_launches(void);
 
 /*
  * Test hook for failure detection: sets the bound, in nanoseconds, of every
- * wait inside the tensor-core scorer (default 2,000,000,000) for launches
- * enqueued from now on, and returns the previous bound. When a wait runs out
+ * wait inside the tensor-core kernels (the scorer and the sparse MLA
+ * attention; default 2,000,000,000) for launches enqueued from now on, and
+ * returns the previous bound. When a wait runs out
  * the kernel records IDX_ERR_TIMEOUT in the status word, stops all its roles,
  * lets copies and tensor-core work already issued finish (within 100 ms),
  * frees its tensor memory and returns, leaving the CUDA context usable. The

@@ -96,8 +96,9 @@ struct ScoreArgs {
 // Tensor-core scorer (tcgen05/TMEM/TMA): a plan kernel, then the persistent
 // scorer. `plan_ws` holds tc_plan_bytes(B, T) bytes of device scratch.
 size_t tc_plan_bytes(int32_t B, int32_t T);
-// Bound of every wait in the tensor-core scorer, in ns; returns the previous one.
+// Bound of every wait in the tensor-core kernels, in ns; returns the previous one.
 uint64_t set_wait_limit_ns(uint64_t ns);
+uint64_t wait_limit_ns();
 
 // *hist_filled (may be NULL) tells whether a.row_hist was filled.
 cudaError_t launch_score_tc(const ScoreArgs& a, void* plan_ws, cudaStream_t stream,

@@ -59,7 +59,6 @@ constexpr int kSoft = 128;                      // warps 5-8
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftBar = 1;                     // named barrier of the softmax warps
 constexpr uint64_t kMlaDrainNs = 100000000ull;  // 100 ms to drain after an abort
-constexpr uint64_t kMlaWaitNs = 2000000000ull;  // no legitimate wait comes close
 
 template <int H>
 struct MlaLayout {
@@ -607,7 +606,7 @@ cudaError_t launch_h(const MlaArgs& a, const CUtensorMap& map, int tps, int n_sp
     const float scale_log2 = a.scale * 1.4426950408889634f;
     e = launch_kernel(kern, dim3((unsigned)((int64_t)a.T * n_split)), dim3(kThreads), (size_t)Lay::kBytes,
                       stream, 1, map, a.cache, a.cache_rows, a.idx, a.cnt, a.cu_q, a.cu_k, a.B, a.topk,
-                      scale_log2, tps, n_split, a.out, a.lse, part_o, part_ml, a.status, kMlaWaitNs);
+                      scale_log2, tps, n_split, a.out, a.lse, part_o, part_ml, a.status, wait_limit_ns());
     if (e != cudaSuccess || n_split == 1) return e;
     return launch_kernel(sparse_mla_merge_kernel, dim3((unsigned)((int64_t)a.T * H)), dim3(128), 0, stream, 1,
                          (const float*)part_o, (const float*)part_ml, n_split, H, a.out, a.lse);

@@ -429,6 +429,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s: no legitimate wait c
 static std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
 
 uint64_t set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms to drain after an abort
 
 // Walks the steps [beg, end) of a CTA: which group, which key tile.

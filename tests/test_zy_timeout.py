@@ -52,3 +52,30 @@ def test_zero_wait_bound_reports_timeout_and_context_survives(B, shape):
     ridx, rcnt, _ = oracle.score_topk(w.q, w.k, w.w, w.q_pos, w.cu_q, w.cu_k, K=2048, threads=8)
     assert np.array_equal(idx.cpu().numpy(), ridx)
     assert np.array_equal(cnt.cpu().numpy(), rcnt)
+
+
+def test_sparse_mla_zero_wait_bound_reports_timeout_and_context_survives(B):
+    """The same for the sparse MLA attention: every role leaves through its
+    bounded drain, the status word says IDX_ERR_TIMEOUT, and the context then
+    computes the oracle's result again."""
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(721, [9000, 3000, 20000], q_per_seq=1)
+    dv = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a if dt is None else a.view(dt))).cuda()
+    args = (dv(q, np.int16), dv(cache, np.int16), dv(idx), dv(cnt), dv(cu_q), dv(cu_k), 0.072)
+    ws = B.workspace(B.sparse_mla_workspace_size(q.shape[0], q.shape[1], 2048), "cuda")
+    old = B.set_wait_limit_ns(0)
+    try:
+        B.sparse_mla(*args, ws=ws)
+        code, _ = B.get_status(ws)
+    finally:
+        B.set_wait_limit_ns(old)
+    assert code == IDX_ERR_TIMEOUT
+    out, lse = B.sparse_mla(*args, ws=ws)
+    assert B.get_status(ws) == (0, 0)
+    o_ref, l_ref = oracle.sparse_mla_batch(q, cache, idx, cnt, cu_q, cu_k, 0.072)
+    lat = oracle.bf16_bits_to_f64(cache[:, :512])
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    for t in range(q.shape[0]):
+        b = t
+        vmax = np.abs(lat[cu_k[b] + idx[t, :cnt[t]]]).max()
+        assert np.abs(o[t] - o_ref[t]).max() <= 2.0 ** -8 * vmax
+        np.testing.assert_allclose(l[t], l_ref[t], atol=2e-4)
