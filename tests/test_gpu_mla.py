@@ -152,3 +152,39 @@ def test_mla_bad_counts_and_empty_sequences(B):
     vmax = np.abs(oracle.bf16_bits_to_f64(cache[idx[0, :cnt[0]], :512])).max()
     assert np.abs(o[0] - o_ref).max() <= 2.0 ** -8 * vmax
     np.testing.assert_allclose(l[0], l_ref, atol=2e-4)
+
+
+def test_mla_long_decode_full_size_sampled(B):
+    """64 queries over histories of 64K..128K rows (a 7 GB cache made on the
+    device from a seeded generator), 2048 selected rows each, 96 heads: the
+    launch configuration bench.py --mla long_decode times (two splits per
+    query). Three sampled queries against the oracle on their gathered rows."""
+    dev = torch.device("cuda", 0)
+    lens = np.random.default_rng(81).integers(65536, 131073, size=64).astype(np.int64)
+    T, H, K = 64, 96, 2048
+    gen = torch.Generator(device=dev).manual_seed(82)
+    L = int(lens.sum())
+    cache = torch.empty((L, 576), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, L, 1 << 20):
+        r1 = min(L, r0 + (1 << 20))
+        cache[r0:r1] = torch.randn((r1 - r0, 576), generator=gen, device=dev).to(torch.bfloat16)
+    q = torch.randn((T, H, 576), generator=gen, device=dev).to(torch.bfloat16)
+    idx = torch.stack([torch.randperm(int(n), generator=gen, device=dev)[:K].sort().values
+                       for n in lens]).to(torch.int32)
+    cnt = torch.full((T,), K, dtype=torch.int32, device=dev)
+    cu_k_h = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cu_k = torch.from_numpy(cu_k_h).to(dev)
+    cu_q = torch.arange(T + 1, dtype=torch.int32, device=dev)
+    scale = 1.0 / np.sqrt(192.0)
+    ws = B.workspace(B.sparse_mla_workspace_size(T, H, K), dev)
+    out, lse = B.sparse_mla(q, cache, idx, cnt, cu_q, cu_k, scale, ws=ws)
+    assert B.get_status(ws) == (0, 0)
+    for t in (0, 31, 63):
+        rows = int(cu_k_h[t]) + idx[t].long()
+        sel = cache[rows].view(torch.int16).cpu().numpy().view(np.uint16)      # [2048, 576]
+        qt = q[t].view(torch.int16).cpu().numpy().view(np.uint16)
+        o_ref, l_ref = oracle.sparse_mla(qt, sel, np.arange(K), scale)
+        vmax = np.abs(oracle.bf16_bits_to_f64(sel[:, :512])).max()
+        err = np.abs(out[t].cpu().numpy() - o_ref).max()
+        assert err <= 2.0 ** -8 * vmax, f"row {t}: |d out| {err}"
+        np.testing.assert_allclose(lse[t].cpu().numpy(), l_ref, atol=2e-4, err_msg=f"row {t}")
