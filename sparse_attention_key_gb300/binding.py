@@ -77,8 +77,12 @@ def lib():
             L.idx_version.restype = i32
             L.idx_kernel_launches.argtypes = []
             L.idx_kernel_launches.restype = ctypes.c_uint64
+            L.idx_sparse_mla_workspace_size.argtypes = [i32, i32, i32]
+            L.idx_sparse_mla_workspace_size.restype = sz
+            L.idx_sparse_mla.argtypes = [P, P, i64, P, P, P, P, i32, i32, i32, i32, ctypes.c_float, P,
+                                         P, P, sz, P]
             for name in ("idx_key_layernorm", "idx_score", "idx_topk", "idx_score_topk",
-                         "idx_get_status"):
+                         "idx_get_status", "idx_sparse_mla"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -361,11 +365,7 @@ MLA_VDIM = 512
 
 
 def sparse_mla_workspace_size(T: int, heads: int, topk: int) -> int:
-    L = lib()
-    fn = L.idx_sparse_mla_workspace_size
-    fn.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
-    fn.restype = ctypes.c_size_t
-    return int(fn(T, heads, topk))
+    return int(lib().idx_sparse_mla_workspace_size(T, heads, topk))
 
 
 def sparse_mla(q, cache, idx, cnt, cu_q, cu_k, scale: float, out: torch.Tensor | None = None,
@@ -400,12 +400,8 @@ def sparse_mla(q, cache, idx, cnt, cu_q, cu_k, scale: float, out: torch.Tensor |
     need = sparse_mla_workspace_size(T, H, topk)
     if ws is None:
         ws = workspace(need, q.device)
-    L = lib()
-    fn = L.idx_sparse_mla
-    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-    fn.argtypes = [P, P, i64, P, P, P, P, i32, i32, i32, i32, ctypes.c_float, P, P, P, ctypes.c_size_t, P]
-    fn.restype = ctypes.c_int
-    _check(fn(_ptr(q), _ptr(cache), int(cache.shape[0]), _ptr(idx), _ptr(cnt), _ptr(cu_q), _ptr(cu_k),
-              B, T, H, topk, float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream()),
+    _check(lib().idx_sparse_mla(_ptr(q), _ptr(cache), int(cache.shape[0]), _ptr(idx), _ptr(cnt),
+                                _ptr(cu_q), _ptr(cu_k), B, T, H, topk, float(scale), _ptr(out),
+                                _ptr(lse), _ptr(ws), ws.numel(), _stream()),
            "idx_sparse_mla")
     return out, lse
