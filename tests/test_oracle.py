@@ -487,3 +487,19 @@ def test_mla_batch_maps_positions_through_the_sequence_offsets():
     o1, l1 = oracle.sparse_mla(qb[1], c, [25, 59, 35], 0.05)
     assert np.array_equal(o[0], o0) and np.array_equal(o[1], o1)
     assert np.array_equal(lse[0], l0) and np.array_equal(lse[1], l1)
+
+
+def test_mla_inputs_follow_the_indexer_output_format():
+    """workloads.mla_case: each query keeps min(topk, its causal length)
+    distinct positions inside its sequence, ascending and -1 padded, as
+    idx_score_topk writes them; shapes of q and the 576-wide cache."""
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(3, [10, 5000, 2049], q_per_seq=2, heads=32, topk=2048)
+    assert q.shape == (6, 32, 576) and cache.shape == (int(cu_k[-1]), 576)
+    assert list(cu_q) == [0, 2, 4, 6] and list(cu_k) == [0, 10, 5010, 7059]
+    lens = [10, 5000, 2049]
+    for t in range(6):
+        n = lens[t // 2] - (1 - t % 2)                 # the query's causal length
+        assert cnt[t] == min(2048, n)
+        sel = idx[t, :cnt[t]]
+        assert np.all(np.diff(sel) > 0) and sel.min() >= 0 and sel.max() < n
+        assert np.all(idx[t, cnt[t]:] == -1)
