@@ -168,6 +168,7 @@ idx_status idx_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void
                              int ln_dtype, float eps, uint16_t* k_out, int64_t n_rows,
                              void* stream) {
     g_last_error[0] = 0;
+    TraceRange trace("idx_key_layernorm");
     if (n_rows < 0) return fail(IDX_ERR_INVALID_ARG, "n_rows must be >= 0");
     if (ln_dtype != IDX_PARAM_BF16 && ln_dtype != IDX_PARAM_F32)
         return fail(IDX_ERR_INVALID_ARG, "ln_dtype must be IDX_PARAM_BF16 or IDX_PARAM_F32");
@@ -187,6 +188,7 @@ idx_status idx_key_layernorm_append(const uint16_t* k_raw, const void* ln_w, con
                                     int ln_dtype, float eps, uint16_t* k_cache, int64_t cache_rows,
                                     const int64_t* slot, int64_t n_rows, void* stream) {
     g_last_error[0] = 0;
+    TraceRange trace("idx_key_layernorm_append");
     if (n_rows < 0 || cache_rows < 0) return fail(IDX_ERR_INVALID_ARG, "n_rows and cache_rows must be >= 0");
     if (ln_dtype != IDX_PARAM_BF16 && ln_dtype != IDX_PARAM_F32)
         return fail(IDX_ERR_INVALID_ARG, "ln_dtype must be IDX_PARAM_BF16 or IDX_PARAM_F32");
@@ -212,6 +214,7 @@ idx_status idx_score(const uint16_t* q, const uint16_t* k, const float* w, const
                      int64_t n_keys, int64_t max_len, float* scores, int64_t ld, void* ws,
                      size_t ws_bytes, void* stream) {
     g_last_error[0] = 0;
+    TraceRange trace("idx_score");
     if (idx_status st = check_batch(q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len)) return st;
     if (ld < max_len || ld % 4 != 0)
         return fail(IDX_ERR_INVALID_ARG, "ld must be >= max_len and a multiple of 4");
@@ -235,6 +238,7 @@ idx_status idx_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
                     int64_t max_len, int32_t topk, int32_t* idx, int32_t* cnt, void* ws,
                     size_t ws_bytes, void* stream) {
     g_last_error[0] = 0;
+    TraceRange trace("idx_topk");
     if (T < 0) return fail(IDX_ERR_INVALID_ARG, "T must be >= 0");
     if (topk < 1 || topk > IDX_TOPK_MAX)
         return fail(IDX_ERR_INVALID_ARG, "topk must be in [1, %d] (got %d)", IDX_TOPK_MAX, topk);
@@ -268,6 +272,7 @@ idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
                           int32_t B, int32_t T, int64_t n_keys, int64_t max_len, int32_t topk,
                           int32_t* idx, int32_t* cnt, void* ws, size_t ws_bytes, void* stream) {
     g_last_error[0] = 0;
+    TraceRange trace("idx_score_topk");
     if (idx_status st = check_batch(q, k, w, q_pos, cu_q, cu_k, B, T, n_keys, max_len)) return st;
     if (topk < 1 || topk > IDX_TOPK_MAX)
         return fail(IDX_ERR_INVALID_ARG, "topk must be in [1, %d] (got %d)", IDX_TOPK_MAX, topk);
@@ -331,6 +336,7 @@ idx_status idx_sparse_mla(const uint16_t* q, const uint16_t* cache, int64_t cach
                           float scale, float* out, float* lse, void* ws, size_t ws_bytes,
                           void* stream) {
     g_last_error[0] = 0;
+    TraceRange trace("idx_sparse_mla");
     if (B < 1) return fail(IDX_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
     if (T < 0) return fail(IDX_ERR_INVALID_ARG, "T must be >= 0 (got %d)", T);
     if (heads != 32 && heads != 64 && heads != 96)

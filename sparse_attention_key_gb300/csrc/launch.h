@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -14,6 +15,16 @@ struct DeviceInfo {
     int cc_major = 0, cc_minor = 0;
     int max_smem_optin = 0;   // bytes of shared memory a block may opt in to
     size_t l2_bytes = 0;
+};
+
+// A named NVTX range around one entry point's host work (argument checks and
+// launches), shown on Nsight timelines; NVTX does nothing when no tool is
+// attached.
+struct TraceRange {
+    explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange&) = delete;
+    TraceRange& operator=(const TraceRange&) = delete;
 };
 
 // Set the calling thread's idx_last_error() text.

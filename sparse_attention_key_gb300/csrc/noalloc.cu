@@ -90,6 +90,7 @@ extern "C" IDX_API idx_status idx_score_topk_noalloc(
     const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t T, int64_t n_keys,
     int64_t max_len, int32_t topk, int32_t* idx, int32_t* cnt, void* stream) {
     set_last_error_text("");
+    TraceRange trace("idx_score_topk_noalloc");
     if (B < 1 || T < 0) return noalloc_fail(IDX_ERR_INVALID_ARG, "B must be >= 1 and T >= 0");
     if (n_keys < 0 || n_keys > 0x7fffffffLL)
         return noalloc_fail(IDX_ERR_INVALID_ARG, "n_keys must be in [0, 2^31-1]");

@@ -147,6 +147,7 @@ idx_status idx_indexer_project(const uint16_t* x, const uint16_t* q_lora, const 
                                const int64_t* slot, float* w, void* ws, size_t ws_bytes,
                                void* stream) {
     set_last_error_text("");
+    TraceRange trace("idx_indexer_project");
     if (T < 0 || hidden < 8 || q_rank < 8 || hidden % 8 != 0 || q_rank % 8 != 0 || cache_rows < 0)
         return proj_fail(IDX_ERR_INVALID_ARG,
                          "T >= 0, hidden and q_rank positive multiples of 8, cache_rows >= 0");
