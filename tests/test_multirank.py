@@ -67,3 +67,15 @@ def test_reference_arm_works_on_rank_zero_only():
                        timeout=120)
     assert r.returncode == 0
     assert r.stdout.strip() == ""                      # no line, no work
+
+
+def test_bench_command_line_parses():
+    """bench.py imports and lists every mode without a GPU (its timed paths run
+    on the GPU; this catches a broken edit before that)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--help"], capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    for opt in ("--gpus", "--steps", "--warmup", "--workload", "--impl", "--ln-append", "--project",
+                "--mla", "--fused-only", "--record-traffic"):
+        assert opt in r.stdout, opt
