@@ -219,3 +219,55 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         binding.lib()
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "lightning_indexer.h"
+
+/* host buffers with the alignment the API asks of device pointers; the calls
+   below are rejected before anything is read from them */
+#define ALIGNED __attribute__((aligned(256)))
+static uint16_t qbuf[256] ALIGNED, kbuf[256] ALIGNED;
+static float wbuf[128] ALIGNED;
+static int32_t q_pos[1], cu[2] = {0, 1}, idx[IDX_TOPK_MAX];
+
+int main(void) {
+    size_t ws = idx_score_topk_workspace_size(1, 1, 1, IDX_TOPK_MAX);
+    idx_status s;
+    if (idx_version() < 100 || ws < 256 || ws % 256 != 0) return 1;
+    /* a misaligned query array: an argument error */
+    s = idx_score_topk(qbuf + 1, kbuf, wbuf, q_pos, cu, cu, 1, 1, 1, 1, IDX_TOPK_MAX, idx, NULL,
+                       NULL, ws, NULL);
+    if (s != IDX_ERR_INVALID_ARG || idx_last_error() == NULL || strlen(idx_last_error()) == 0) return 2;
+    /* a null workspace: a workspace error */
+    s = idx_score_topk(qbuf, kbuf, wbuf, q_pos, cu, cu, 1, 1, 1, 1, IDX_TOPK_MAX, idx, NULL,
+                       NULL, ws, NULL);
+    if (s != IDX_ERR_WORKSPACE || strlen(idx_last_error()) == 0) return 3;
+    printf("ok %d %zu\n", (int)idx_version(), ws);
+    return 0;
+}
+"""
+
+
+@pytest.mark.parametrize("lang", ["c99", "c++17"])
+def test_plain_c_client_compiles_links_and_runs(tmp_path, lang):
+    """The header is valid C and C++ on its own, and a program built with the
+    host compiler (no CUDA headers, no torch) links the library and calls it."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c99" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    path = lib_build.build()
+    src = tmp_path / ("client.c" if lang == "c99" else "client.cpp")
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    flags = ["-std=" + lang, "-Wall", "-Wextra", "-pedantic", "-Werror"]
+    subprocess.run([cc, *flags, "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                    path, "-Wl,-rpath," + os.path.dirname(path)], check=True, capture_output=True,
+                   text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.startswith("ok ")
