@@ -66,6 +66,19 @@ def test_mla_peaked_softmax_rescales_across_tiles(B):
         _check(o, l, o_ref, l_ref, cache, idx, cnt, cu_q, cu_k, range(q.shape[0]))
 
 
+@pytest.mark.parametrize("topk", [1, 33])
+def test_mla_short_index_rows(B, topk):
+    """idx rows of stride 1 and 33: selections shorter than one tile, and a
+    second tile holding one row."""
+    lens = [1, 50, 700, 33]
+    q, cache, idx, cnt, cu_q, cu_k = wl.mla_case(25 + topk, lens, q_per_seq=1, heads=64, topk=topk)
+    assert idx.shape == (4, topk) and list(cnt) == [1, min(topk, 50), min(topk, 700), min(topk, 33)]
+    scale = 1.0 / np.sqrt(192.0)
+    o, l = _run(B, q, cache, idx, cnt, cu_q, cu_k, scale)
+    o_ref, l_ref = oracle.sparse_mla_batch(q, cache, idx, cnt, cu_q, cu_k, scale)
+    _check(o, l, o_ref, l_ref, cache, idx, cnt, cu_q, cu_k, range(q.shape[0]))
+
+
 def test_mla_many_rows_single_split(B):
     """T >= the SM count: one CTA per query row writes the result directly."""
     lens = [3000] * 40
