@@ -2,13 +2,19 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
 
-One step = one pass of the whole indexer over one batch of the named workload:
-key LayerNorm (when the workload chains it), head scores with the relu/head-
-weighted epilogue, and the exact top-2048 with the tie/order rule. Inputs are
-resident in HBM when the timed region starts; between timed steps L2 is
-flushed by writing a 256 MB buffer and then reading another 256 MB buffer (so
-that every step starts with a cold L2 that holds no dirty lines of the
-flush). Rank 0 prints one JSON line.
+One step = one idx_score_topk call over one batch of the named workload (the
+agentic chunk by default, the largest single-GPU workload): head scores with
+the relu / head-weighted epilogue and the exact top-2048 with the tie/order
+rule. The key LayerNorm runs once per key at cache fill and is timed on its
+own where the workload chains it (decode batch). Inputs are resident in HBM
+when the timed region starts; between timed steps L2 is flushed by writing a
+256 MB buffer and then reading another 256 MB buffer (so that every step
+starts with a cold L2 that holds no dirty lines of the flush). Rank 0 prints
+one JSON line. Per-kernel times come from the same fused call: the library
+records CUDA events between its launches (idx_set_kernel_events). The line
+also carries a by_workload block with the fused-call time, per-kernel times
+and rooflines of the decode batch, prefill ties, long decode and speculative
+verification workloads.
 
 --impl reference times the CPU oracle (the plain fp64 definition) on the host's
 cores on a bounded row sample of the same workload, as the reference arm.
@@ -35,7 +41,7 @@ from sparse_attention_key_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "indexer query-key pairs/s (score+exact top-2048); % of HBM / tensor roofline"
 UNIT = "pairs/s"
-DEFAULT_WORKLOAD = 2   # the decode batch: 8 sequences, one query each, 8K-64K keys
+DEFAULT_WORKLOAD = 4   # the agentic chunk: 4 x (50,000 cached keys + 800 new queries)
 
 
 E2E_CHUNKS = 4   # row chunks (and streams) for the keys' host-to-device copy in the e2e step
@@ -210,27 +216,207 @@ def whole_job_value(pairs_per_step: int, world: int, steps: int, max_ms: float) 
 
 
 # ---------------------------------------------------------------------------
-# algorithmic work per launch
+# algorithmic work per call (the scorer's contraction, its key/query bytes, the
+# selection's outputs; staged fp32 scores are overhead of the two-kernel design)
 # ---------------------------------------------------------------------------
 
 def algorithmic(w: wl.Workload):
-    """Per-call algorithmic work: flops, HBM bytes for score (unique keys, q, w, out) and LN."""
+    """Per-call algorithmic work of idx_score_topk and of the key LayerNorm."""
     unique_keys = 0
     for b in range(w.B):
         q0, q1 = int(w.cu_q[b]), int(w.cu_q[b + 1])
         if q1 > q0:
             unique_keys += int(w.q_pos[q0:q1].max()) + 1
     score_bytes = unique_keys * 256 + w.T * (32 * 128 * 2 + 32 * 4)
-    # the selection's own minimum: one read of its fp32 score rows, its outputs
-    topk_bytes = 4 * w.pairs + w.T * w.topk * 4 + w.T * 4
-    ln_bytes = (w.k_raw.shape[0] * 512 + 2 * 128 * 2) if (w.k is None and w.k_raw is not None) else 0
+    topk_bytes = w.T * (w.topk * 4 + 4)                 # idx and cnt written
+    staged_bytes = 4 * w.pairs                          # fp32 scores: written once, read back
+    ln_bytes = (w.k_raw.shape[0] * 512 + 2 * 128 * 2) if w.k_raw is not None else 0
     return {"flops": 8192.0 * w.pairs, "score_bytes": score_bytes, "topk_bytes": topk_bytes,
+            "call_bytes": score_bytes + topk_bytes, "staged_bytes": staged_bytes,
             "ln_bytes": ln_bytes, "unique_keys": unique_keys}
+
+
+def tensor_bound(w: wl.Workload) -> bool:
+    """Many queries per sequence share each key tile: the contraction dominates
+    (8,192 flop per pair against 256 B per key, shared by the sequence's queries)."""
+    return w.T > 4 * w.B
+
+
+def _roof(bound, amount, ms, pk):
+    if ms is None or ms <= 0:
+        return None
+    if bound == "tensor":
+        ach = amount / (ms / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"], "flops": amount, "ms": ms}
+    ach = amount / (ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / pk["hbm_gbs"], "bytes": amount, "ms": ms}
+
+
+def rooflines(w: wl.Workload, kernels_ms: dict, fused_ms: float, pk: dict):
+    """Per-kernel and whole-call rooflines of one idx_score_topk call."""
+    alg = algorithmic(w)
+    tb = tensor_bound(w)
+    out = {}
+    if "score" in kernels_ms:
+        out["score"] = (_roof("tensor", alg["flops"], kernels_ms["score"], pk) if tb else
+                        _roof("hbm", alg["score_bytes"], kernels_ms["score"], pk))
+    if "topk" in kernels_ms:
+        r = _roof("hbm", alg["topk_bytes"], kernels_ms["topk"], pk)
+        if r is not None:
+            # its read of the staged scores is overhead of the two-kernel design
+            r["overhead_bytes"] = alg["staged_bytes"]
+            r["overhead_gbs"] = alg["staged_bytes"] / (kernels_ms["topk"] / 1e3) / 1e9
+        out["topk"] = r
+    if "plan" in kernels_ms:
+        out["plan"] = {"bound": "latency", "ms": kernels_ms["plan"]}
+    call = (_roof("tensor", alg["flops"], fused_ms, pk) if tb else
+            _roof("hbm", alg["call_bytes"], fused_ms, pk))
+    return out, call
 
 
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+
+PHASES = ("plan", "score", "topk")   # kernels of one fused call, in launch order
+
+
+class Bench:
+    """Device state shared by the timed loops of one process."""
+
+    def __init__(self, dev):
+        import torch
+        self.torch = torch
+        self.dev = dev
+        self.flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+        self.flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def flush_l2(self):
+        self.flush_w.zero_()        # evicts everything the step could reuse
+        self.flush_r.max()          # writes the flush's dirty lines back before the step
+
+    def up(self, a, dt=None):
+        x = self.torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(dt) if dt is not None else x).to(self.dev)
+
+    def event(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+
+class FusedCase:
+    """One workload resident in HBM with its outputs and workspace."""
+
+    def __init__(self, bn: Bench, w: wl.Workload):
+        import torch
+        from sparse_attention_key_gb300 import binding as B
+        self.B, self.w, self.bn = B, w, bn
+        self.q, self.wt, self.q_pos = bn.up(w.q, torch.int16), bn.up(w.w), bn.up(w.q_pos)
+        self.cu_q, self.cu_k = bn.up(w.cu_q), bn.up(w.cu_k)
+        self.chained_ln = w.k is None
+        if self.chained_ln:
+            self.k_raw = bn.up(w.k_raw, torch.int16)
+            self.ln_w, self.ln_b = bn.up(w.ln_w, torch.int16), bn.up(w.ln_b, torch.int16)
+            self.k = torch.empty_like(self.k_raw)
+            B.key_layernorm(self.k_raw, self.ln_w, self.ln_b, w.eps, out=self.k)
+        else:
+            self.k = bn.up(w.k, torch.int16)
+        T, K = w.T, w.topk
+        self.idx = torch.empty((T, K), dtype=torch.int32, device=bn.dev)
+        self.cnt = torch.empty((T,), dtype=torch.int32, device=bn.dev)
+        self.ws = B.workspace(B.score_topk_workspace_size(w.B, T, w.max_len, K), bn.dev)
+
+    def call(self):
+        w = self.w
+        self.B.score_topk(self.q, self.k, self.wt, self.q_pos, self.cu_q, self.cu_k, w.max_len,
+                          w.topk, idx=self.idx, cnt=self.cnt, ws=self.ws)
+
+    def ln(self):
+        self.B.key_layernorm(self.k_raw, self.ln_w, self.ln_b, self.w.eps, out=self.k)
+
+    def warm(self, n):
+        for _ in range(max(n, 3)):
+            self.call()
+        self.bn.torch.cuda.synchronize()
+        code, detail = self.B.get_status(self.ws)
+        if code != 0:
+            raise RuntimeError(f"device status {code} (detail {detail}) after warm-up")
+
+    def time_calls(self, steps):
+        """Per-step ms of the fused call, L2 flushed before each."""
+        bn = self.bn
+        st = [bn.event() for _ in range(steps)]
+        en = [bn.event() for _ in range(steps)]
+        for i in range(steps):
+            bn.flush_l2()
+            st[i].record(bn.stream)
+            self.call()
+            en[i].record(bn.stream)
+        bn.torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(st, en)]
+
+    def time_kernels(self, steps):
+        """Mean ms of each kernel of the fused call, from events the library
+        records between its launches (idx_set_kernel_events)."""
+        bn, B = self.bn, self.B
+        n0 = B.kernel_launches()
+        self.call()
+        bn.torch.cuda.synchronize()
+        per_call = B.kernel_launches() - n0
+        rows = []
+        for _ in range(steps):
+            ev = [bn.event() for _ in range(per_call + 1)]
+            for e in ev:                 # creates the CUDA events
+                e.record(bn.stream)
+            bn.flush_l2()
+            ev[0].record(bn.stream)
+            B.set_kernel_events(ev[1:])
+            self.call()
+            B.set_kernel_events([])
+            rows.append(ev)
+        bn.torch.cuda.synchronize()
+        gaps = np.array([[ev[i].elapsed_time(ev[i + 1]) for i in range(per_call)] for ev in rows])
+        mean = gaps.mean(axis=0)
+        out = {"plan": float(mean[0]), "score": float(mean[1]), "topk": float(mean[2:].sum())}
+        return out, int(per_call)
+
+    def time_ln(self, steps):
+        bn = self.bn
+        ms = []
+        for _ in range(steps):
+            bn.flush_l2()
+            a, e = bn.event(), bn.event()
+            a.record(bn.stream)
+            self.ln()
+            e.record(bn.stream)
+            ms.append((a, e))
+        bn.torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(e) for a, e in ms]))
+
+
+def workload_block(bn: Bench, w: wl.Workload, steps: int, warmup: int, pk: dict):
+    """Fused-call time, per-kernel times and rooflines of one workload."""
+    fc = FusedCase(bn, w)
+    fc.warm(warmup)
+    ms = fc.time_calls(steps)
+    kern, per_call = fc.time_kernels(steps)
+    fused_ms = float(np.mean(ms))
+    per_kernel, call = rooflines(w, kern, fused_ms, pk)
+    block = {"B": w.B, "T": w.T, "pairs": w.pairs, "max_len": w.max_len,
+             "fused_ms": fused_ms, "fused_ms_median": float(np.median(ms)),
+             "pairs_per_s": w.pairs / (fused_ms / 1e3), "kernels_per_call": per_call,
+             "kernels_ms": kern, "kernel_rooflines": per_kernel, "call_roofline": call,
+             "bound": "tensor" if tensor_bound(w) else "hbm", "steps": steps}
+    if fc.chained_ln:
+        ln_ms = fc.time_ln(steps)
+        alg = algorithmic(w)
+        block["key_layernorm"] = _roof("hbm", alg["ln_bytes"], ln_ms, pk)
+    del fc
+    bn.torch.cuda.empty_cache()
+    return block
+
 
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -243,78 +429,30 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    bn = Bench(dev)
     w = wl.by_index(args.workload)
-    chained_ln = w.k is None
-
-    def up(a, dt=None):
-        x = torch.from_numpy(np.ascontiguousarray(a))
-        return (x.view(dt) if dt is not None else x).to(dev)
-
-    q, wt, q_pos = up(w.q, torch.int16), up(w.w), up(w.q_pos)
-    cu_q, cu_k = up(w.cu_q), up(w.cu_k)
-    if chained_ln:
-        k_raw, ln_w, ln_b = up(w.k_raw, torch.int16), up(w.ln_w, torch.int16), up(w.ln_b, torch.int16)
-        k = torch.empty_like(k_raw)
-    else:
-        k = up(w.k, torch.int16)
-    T, K, max_len = w.T, w.topk, w.max_len
-    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
-    cnt = torch.empty((T,), dtype=torch.int32, device=dev)
-    ws = B.workspace(B.score_topk_workspace_size(w.B, T, max_len, K), dev)
-    ld = (max_len + 3) // 4 * 4
-    scores = torch.empty((T, ld), dtype=torch.float32, device=dev)
-    ws_small = B.workspace(max(B.score_workspace_size(w.B, T, max_len),
-                               B.topk_workspace_size(T, max_len, K)), dev)
-    flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
-    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
-
-    def flush_l2():
-        flush_w.zero_()        # evicts everything the step could reuse
-        flush_r.max()          # writes the flush's dirty lines back before the step
-    stream = torch.cuda.current_stream()
-
-    def step():
-        if chained_ln:
-            B.key_layernorm(k_raw, ln_w, ln_b, w.eps, out=k)
-        B.score_topk(q, k, wt, q_pos, cu_q, cu_k, max_len, K, idx=idx, cnt=cnt, ws=ws)
-
-    def step_split(ev):
-        ev[0].record(stream)
-        if chained_ln:
-            B.key_layernorm(k_raw, ln_w, ln_b, w.eps, out=k)
-        ev[1].record(stream)
-        B.score(q, k, wt, q_pos, cu_q, cu_k, max_len, ld=ld, out=scores, ws=ws_small)
-        ev[2].record(stream)
-        B.topk(scores, q_pos_plus1, max_len, K, idx=idx, cnt=cnt, ws=ws_small)
-        ev[3].record(stream)
-
-    q_pos_plus1 = q_pos + 1
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    code, detail = B.get_status(ws)
-    if code != 0:
-        raise RuntimeError(f"device status {code} (detail {detail}) after warm-up")
+    T, K = w.T, w.topk
+    fc = FusedCase(bn, w)
+    fc.warm(args.warmup)
 
     cvd = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x]
     clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else str(local_rank))
     clocks.start()
     time.sleep(0.3)
 
-    # ---- timed region: K steps of the fused call (plus the chained LayerNorm)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # ---- timed region: K steps of the fused call
+    starts = [bn.event() for _ in range(args.steps)]
+    ends = [bn.event() for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = B.kernel_launches()
     t_wall0 = time.time()
     for i in range(args.steps):
-        flush_l2()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
+        bn.flush_l2()
+        starts[i].record(bn.stream)
+        fc.call()
+        ends[i].record(bn.stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     launches = B.kernel_launches() - launches0
@@ -331,21 +469,16 @@ def run_ours(args, rank, world, local_rank):
                   flush=True)
         return
 
-    # ---- per-kernel durations: the same kernels through the split entry points
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush_l2()
-        step_split(evs[i])
-    torch.cuda.synchronize()
+    # ---- per-kernel durations inside the same fused call (events between its launches)
+    kern, per_call = fc.time_kernels(args.steps)
+    ln_ms = fc.time_ln(args.steps) if fc.chained_ln else None
     t_wall2 = time.time()
     clocks.stop()
-    ln_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    score_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
-    topk_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
 
     # ---- end to end through the public API with host buffers
     def pinned(a):
         return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    chained_ln = fc.chained_ln
     h_in = {"q": pinned(w.q.view(np.int16)), "w": pinned(w.w), "q_pos": pinned(w.q_pos),
             "cu_q": pinned(w.cu_q), "cu_k": pinned(w.cu_k)}
     if chained_ln:
@@ -370,6 +503,7 @@ def run_ours(args, rank, world, local_rank):
     side = [torch.cuda.Stream(device=dev) for _ in range(E2E_CHUNKS)]
     go = torch.cuda.Event()
     done = [torch.cuda.Event() for _ in range(E2E_CHUNKS)]
+    stream = bn.stream
 
     def e2e_step():
         go.record(stream)
@@ -382,29 +516,39 @@ def run_ours(args, rank, world, local_rank):
                 side[c].wait_event(go)
                 d_in[big][r0:r1].copy_(h_in[big][r0:r1], non_blocking=True)
                 if chained_ln and r1 > r0:
-                    B.key_layernorm(d_in["k_raw"][r0:r1], ln_w, ln_b, w.eps, out=k[r0:r1])
+                    B.key_layernorm(d_in["k_raw"][r0:r1], fc.ln_w, fc.ln_b, w.eps, out=fc.k[r0:r1])
                 done[c].record(side[c])
         for c in range(E2E_CHUNKS):
             stream.wait_event(done[c])
-        kk = k if chained_ln else d_in["k"]
-        B.score_topk(d_in["q"], kk, d_in["w"], d_in["q_pos"], d_in["cu_q"], d_in["cu_k"], max_len,
-                     K, idx=idx, cnt=cnt, ws=ws)
-        h_idx.copy_(idx, non_blocking=True)
-        h_cnt.copy_(cnt, non_blocking=True)
+        kk = fc.k if chained_ln else d_in["k"]
+        B.score_topk(d_in["q"], kk, d_in["w"], d_in["q_pos"], d_in["cu_q"], d_in["cu_k"],
+                     w.max_len, K, idx=fc.idx, cnt=fc.cnt, ws=fc.ws)
+        h_idx.copy_(fc.idx, non_blocking=True)
+        h_cnt.copy_(fc.cnt, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_start = [bn.event() for _ in range(args.steps)]
+    e_end = [bn.event() for _ in range(args.steps)]
     for i in range(args.steps):
-        flush_l2()
+        bn.flush_l2()
         e_start[i].record(stream)
         e2e_step()
         e_end[i].record(stream)
     torch.cuda.synchronize()
     e2e_ms = float(sum(s.elapsed_time(e) for s, e in zip(e_start, e_end)))
-    ok = np.array_equal(h_idx.numpy(), idx.cpu().numpy())
+    ok = np.array_equal(h_idx.numpy(), fc.idx.cpu().numpy())
+    del fc, d_in, h_in
+    torch.cuda.empty_cache()
+
+    # ---- the other full-size workloads, each with its own fused-call rooflines
+    pk = peaks()
+    by_workload = {}
+    if args.by_workload and world == 1:
+        for i in [x for x in (2, 3, 5, 6) if x != args.workload]:
+            by_workload[wl.NAMES[i]] = workload_block(bn, wl.by_index(i), args.other_steps,
+                                                      args.warmup, pk)
 
     total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], world, dev)
     if rank != 0:
@@ -413,54 +557,47 @@ def run_ours(args, rank, world, local_rank):
     pairs = w.pairs
     value = whole_job_value(pairs, world, args.steps, total_ms)
     e2e_value = whole_job_value(pairs, world, args.steps, e2e_ms)
-    pk = peaks()
-    alg = algorithmic(w)
-    kernels = {
-        "key_layernorm": {"ms": ln_ms, "bytes": alg["ln_bytes"]},
-        "score": {"ms": score_ms, "bytes": alg["score_bytes"], "flops": alg["flops"]},
-        "topk": {"ms": topk_ms, "bytes": alg["topk_bytes"]},
-    }
-    tensor_bound = w.T > w.B * 4   # many queries per sequence: the contraction dominates
-
-    def roofline_of(name):
-        kv = kernels[name]
-        if kv["ms"] <= 0:
-            return None
-        if name == "score" and tensor_bound:
-            ach = alg["flops"] / (kv["ms"] / 1e3) / 1e12
-            return {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "ms": kv["ms"]}
-        ach = kv["bytes"] / (kv["ms"] / 1e3) / 1e9
-        return {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / pk["hbm_gbs"], "ms": kv["ms"]}
-
-    per_kernel = {k_: roofline_of(k_) for k_ in kernels if kernels[k_]["ms"] > 0}
-    dominant = max(per_kernel, key=lambda k_: per_kernel[k_]["ms"])
-    roof = dict(per_kernel[dominant])
-    roof.pop("ms")
-    roof.update({"kernel": dominant, "traffic": dram_traffic(args.workload, dominant),
-                 "peak_source": pk["source"]})
+    fused_ms = total_ms / args.steps
+    per_kernel, call_roof = rooflines(w, kern, fused_ms, pk)
+    timed = {k_: v for k_, v in per_kernel.items() if v is not None and "frac" in v}
+    dominant = max(timed, key=lambda k_: timed[k_]["ms"])
+    roof = {k_: v for k_, v in timed[dominant].items() if k_ in ("bound", "achieved", "peak", "unit", "frac")}
+    roof.update({"kernel": dominant, "ms": timed[dominant]["ms"],
+                 "traffic": dram_traffic(args.workload, dominant),
+                 "peak_source": pk["source"],
+                 "units": ("8,192 flop per (query, causal key) pair" if roof["bound"] == "tensor"
+                           else "bytes: 256 per (sequence, key) read + 8,320 per query (q, w)")})
+    if ln_ms is not None:
+        per_kernel["key_layernorm"] = _roof("hbm", algorithmic(w)["ln_bytes"], ln_ms, pk)
 
     ck = clocks.summary(t_wall0, t_wall2)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": fused_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": wl.NAMES[args.workload], "B": w.B, "T": T, "L": w.L,
-                   "pairs_per_step": pairs, "topk": K, "max_len": max_len,
-                   "layernorm_in_step": chained_ln, "l2": "flushed between steps: 256 MB written, then 256 MB read (cold, clean)",
+                   "pairs_per_step": pairs, "topk": K, "max_len": w.max_len,
+                   "step": "one idx_score_topk call (score + exact top-2048); the key "
+                           "LayerNorm is timed on its own",
+                   "l2": "flushed between steps: 256 MB written, then 256 MB read (cold, clean)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "matches_device_result": bool(ok),
                 "copies": f"pinned host buffers; keys in {E2E_CHUNKS} row chunks on {E2E_CHUNKS} streams"
                           + (", each LayerNormed as it lands" if chained_ln else "")},
         "gpu_launches": int(launches),
-        "kernels_ms": {k_: v["ms"] for k_, v in kernels.items()},
+        "kernels_per_call": per_call,
+        "kernels_ms": kern,
+        "kernels_source": "events recorded by the library between the kernels of the fused "
+                          "call (idx_set_kernel_events), mean over the steps",
         "roofline": roof,
+        "call_roofline": call_roof,
         "kernel_rooflines": per_kernel,
         "clocks": ck,
     }
+    if by_workload:
+        line["by_workload"] = by_workload
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args)
     print(json.dumps(line), flush=True)
@@ -671,22 +808,33 @@ def _oracle_inputs(w: wl.Workload):
     return w.k
 
 
-def cpu_baseline(w: wl.Workload, args):
+def _oracle_rate(w, k, rows, threads):
     import oracle
+    t0 = time.time()
+    oracle.score_topk(w.q, k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, rows=rows, threads=threads)
+    return time.time() - t0
+
+
+def cpu_baseline(w: wl.Workload, args):
+    """The fp64 oracle, as it stands, on the host: single-threaded and on all
+    cores (one thread per query row), each on a bounded row sample."""
     cores = os.cpu_count() or 1
     k = _oracle_inputs(w)
-    # calibrate: ~0.2 s single-row probe, then size the sample to ~10-20 s of work
-    rows, tot = _oracle_sample(w, 20_000)
-    t0 = time.time()
-    oracle.score_topk(w.q, k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, rows=rows, threads=cores)
-    rate = tot / max(time.time() - t0, 1e-6)
-    rows, tot = _oracle_sample(w, int(rate * args.cpu_seconds))
-    t0 = time.time()
-    oracle.score_topk(w.q, k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, rows=rows, threads=cores)
-    dt = time.time() - t0
-    return {"value": tot / dt, "unit": UNIT, "cores": min(cores, len(rows)), "kind": "oracle",
-            "sample": f"{len(rows)} of {w.T} query rows ({tot} pairs) of {wl.NAMES[args.workload]}, "
-                      f"fp64 C oracle, one thread per row, {dt:.1f} s"}
+    rows, tot = _oracle_sample(w, 20_000)          # calibration: a few ms of work
+    rate1 = tot / max(_oracle_rate(w, k, rows, 1), 1e-6)
+    # single thread: about a third of the budget
+    rows1, tot1 = _oracle_sample(w, int(rate1 * args.cpu_seconds / 3))
+    dt1 = _oracle_rate(w, k, rows1, 1)
+    # all cores: the rest, on enough rows to keep every core busy
+    rows_n, tot_n = _oracle_sample(w, max(int(rate1 * cores * args.cpu_seconds * 2 / 3), 1))
+    dt_n = _oracle_rate(w, k, rows_n, cores)
+    used = min(cores, len(rows_n))
+    return {"value": tot_n / dt_n, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"{len(rows_n)} of {w.T} query rows ({tot_n} pairs) of {wl.NAMES[args.workload]}, "
+                      f"fp64 C oracle, one thread per row on {used} of {cores} host cores, {dt_n:.1f} s",
+            "single_thread": {"value": tot1 / dt1, "unit": UNIT, "cores": 1,
+                              "sample": f"{len(rows1)} query rows ({tot1} pairs), {dt1:.1f} s"},
+            "host_cores": cores}
 
 
 def run_reference(args, rank, world):
@@ -735,6 +883,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-by-workload", dest="by_workload", action="store_false",
+                    help="skip timing the other full-size workloads (by_workload block)")
+    ap.add_argument("--other-steps", type=int, default=20,
+                    help="timed fused calls per workload in the by_workload block")
     ap.add_argument("--ln-append", type=int, metavar="ROWS", default=0,
                     help="time the key LayerNorm fused into the key-cache append of ROWS new keys "
                          "(random distinct slots of a 4*ROWS-row cache) against LayerNorm into a "

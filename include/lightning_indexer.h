@@ -185,7 +185,9 @@ IDX_API size_t idx_topk_workspace_size(int32_t T, int64_t max_len, int32_t topk)
 /*
  * The whole indexer in one call: idx_score followed by idx_topk with
  * n_valid[t] = q_pos[t] + 1, staging the fp32 scores inside the workspace.
- * Arguments as for idx_score and idx_topk.
+ * Arguments as for idx_score and idx_topk. When a bounded wait inside the
+ * scorer gives up (IDX_ERR_TIMEOUT in the status word) no row is selected
+ * from the incomplete scores: every row gets idx -1 and cnt 0.
  */
 IDX_API idx_status idx_score_topk(const uint16_t* q, const uint16_t* k, const float* w,
                           const int32_t* q_pos, const int32_t* cu_q, const int32_t* cu_k,
@@ -214,9 +216,15 @@ IDX_API size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_l
  *             unordered host threads) race on it and must be serialised.
  *   Set-up    the first call on each device looks up the array's device address
  *             (cudaGetSymbolAddress, with that device current); make that first
- *             call before any stream capture.
- *   Errors    host checks as idx_score_topk; a row skipped for a device-side
- *             argument error shows cnt[t] == 0 and idx -1 (no status word).
+ *             call before any stream capture. The address is kept per device and
+ *             CUDA context, so the first call in a new context of a device
+ *             (after cudaDeviceReset, say) looks it up again.
+ *   Errors    host checks as idx_score_topk. There is no status word to read: a
+ *             row skipped for a device-side argument error shows cnt[t] == 0 and
+ *             idx -1, and when a bounded wait inside the scorer gives up (the
+ *             workspace entry point's IDX_ERR_TIMEOUT) every row of the call is
+ *             written that way. A valid row keeps at least one position, so
+ *             cnt[t] == 0 always marks a failed row.
  */
 IDX_API idx_status idx_score_topk_noalloc(const uint16_t* q, const uint16_t* k, const float* w,
                                           const int32_t* q_pos, const int32_t* cu_q,
@@ -286,11 +294,25 @@ IDX_API uint64_t idx_kernel_launches(void);
  * the kernel records IDX_ERR_TIMEOUT in the status word, stops all its roles,
  * lets copies and tensor-core work already issued finish (within 100 ms),
  * frees its tensor memory and returns, leaving the CUDA context usable. The
- * call's later kernels still run on the partly written scores: idx and cnt are
- * then meaningless, but every write stays inside its buffer. A bound of 0 makes
+ * selection kernels of the same fused call then select nothing from the
+ * partly written scores: every row gets idx -1 and cnt 0. A bound of 0 makes
  * the first wait that is not already satisfied give up.
  */
 IDX_API uint64_t idx_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Measurement hook (no counterpart in the port notes): arms n CUDA events
+ * (cudaEvent_t handles passed as void*, created by the caller, n <= 16) for
+ * the calling thread. The next n kernels that any entry point enqueues from
+ * this thread each get events[i] recorded on their stream right after the
+ * i-th of them, so that a benchmark can time every kernel of one real fused
+ * call (event i-1 to event i). A recorded event sits between two kernels
+ * that would otherwise overlap their start-up (programmatic dependent
+ * launch), so the per-kernel times add up to a little more than the call
+ * alone. n = 0 disarms. Returns n, or -1 for n outside [0, 16] or NULL
+ * events (message in idx_last_error). The events are not owned.
+ */
+IDX_API int32_t idx_set_kernel_events(void* const* events, int32_t n);
 
 #ifdef __cplusplus
 }

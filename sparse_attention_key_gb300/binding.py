@@ -35,7 +35,7 @@ EXPORTS = ("idx_key_layernorm", "idx_score", "idx_score_workspace_size", "idx_to
            "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches",
            "idx_score_topk_noalloc", "idx_set_wait_limit_ns", "idx_key_layernorm_append",
            "idx_indexer_project", "idx_indexer_project_workspace_size", "idx_sparse_mla",
-           "idx_sparse_mla_workspace_size")
+           "idx_sparse_mla_workspace_size", "idx_set_kernel_events")
 
 
 class IndexerError(RuntimeError):
@@ -358,6 +358,21 @@ def set_wait_limit_ns(limit_ns: int) -> int:
     fn.argtypes = [ctypes.c_uint64]
     fn.restype = ctypes.c_uint64
     return int(fn(int(limit_ns)))
+
+
+def set_kernel_events(events) -> int:
+    """Measurement hook: record ``events`` (torch.cuda.Event with timing, each
+    recorded once before so that it exists) right after each of the next
+    len(events) kernels this thread enqueues through the library; [] disarms."""
+    handles = [ctypes.c_void_p(int(e.cuda_event)) for e in events]
+    arr = (ctypes.c_void_p * max(len(handles), 1))(*handles)
+    fn = lib().idx_set_kernel_events
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    fn.restype = ctypes.c_int32
+    r = int(fn(arr if handles else None, len(handles)))
+    if r < 0:
+        raise IndexerError(1, "idx_set_kernel_events", lib().idx_last_error().decode(errors="replace"))
+    return r
 
 
 MLA_DIM = 576    # MLA cache row: 512-wide latent + 64 key dims

@@ -34,6 +34,17 @@ static std::atomic<uint64_t> g_launches{0};
 
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+// Measurement events of the calling thread (idx_set_kernel_events).
+constexpr int kMaxKernelEvents = 16;
+static thread_local cudaEvent_t g_kernel_events[kMaxKernelEvents];
+static thread_local int g_kernel_events_n = 0;
+static thread_local int g_kernel_events_next = 0;
+
+void after_launch(cudaStream_t stream) {
+    if (g_kernel_events_next < g_kernel_events_n)
+        cudaEventRecord(g_kernel_events[g_kernel_events_next++], stream);
+}
+
 static constexpr int kMaxDevices = 64;
 
 const DeviceInfo& device_info() {
@@ -163,6 +174,18 @@ const char* idx_last_error(void) { return g_last_error; }
 uint64_t idx_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 uint64_t idx_set_wait_limit_ns(uint64_t limit_ns) { return set_wait_limit_ns(limit_ns); }
+
+int32_t idx_set_kernel_events(void* const* events, int32_t n) {
+    if (n < 0 || n > kMaxKernelEvents || (n > 0 && events == nullptr)) {
+        fail(IDX_ERR_INVALID_ARG, "idx_set_kernel_events: n must be in [0, %d] with non-NULL events",
+             kMaxKernelEvents);
+        return -1;
+    }
+    for (int i = 0; i < n; ++i) g_kernel_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_kernel_events_n = n;
+    g_kernel_events_next = 0;
+    return n;
+}
 
 idx_status idx_key_layernorm(const uint16_t* k_raw, const void* ln_w, const void* ln_b,
                              int ln_dtype, float eps, uint16_t* k_out, int64_t n_rows,

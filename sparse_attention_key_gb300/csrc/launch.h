@@ -33,6 +33,10 @@ void set_last_error_text(const char* msg);
 // Count one kernel launch (reported by idx_kernel_launches).
 void count_launch(int n = 1);
 
+// After a kernel was enqueued on `stream`: record the calling thread's next
+// measurement event there, if idx_set_kernel_events armed any.
+void after_launch(cudaStream_t stream);
+
 // Properties of the current device (cached per device).
 const DeviceInfo& device_info();
 
@@ -69,7 +73,9 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     cfg.attrs = attr;
     cfg.numAttrs = n;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess) after_launch(stream);
+    return e;
 }
 
 // slot == NULL: row r of k_raw -> row r of k_out. Otherwise row r -> row

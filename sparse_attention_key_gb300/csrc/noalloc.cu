@@ -22,9 +22,16 @@
 //     different host threads without ordering) race on it. Serialise them.
 //   - The first call on each device looks up the array's device address with
 //     cudaGetSymbolAddress (with that device current); make that first call
-//     before any stream capture.
-//   - Device-side argument errors are not reported through a status word: a
-//     skipped row shows cnt[t] == 0 and an idx row of -1.
+//     before any stream capture. The address is cached per device and CUDA
+//     context: the first call in a new context of a device (after
+//     cudaDeviceReset, say) looks it up again.
+//   - There is no status word to read back. A row skipped for a device-side
+//     argument error shows cnt[t] == 0 and an idx row of -1; when a bounded
+//     wait inside the scorer gives up (IDX_ERR_TIMEOUT in the workspace entry
+//     point), every row of the call is written that way. A valid row always
+//     keeps at least one position, so cnt[t] == 0 marks the failure.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -52,20 +59,51 @@ idx_status noalloc_fail(idx_status code, const char* msg) {
     return code;
 }
 
-// Device address of the scratch array on the current device (looked up once
-// per device, with that device current). Returns nullptr and fills `err` on
-// failure.
+// Id of the calling thread's current CUDA context (unique for the life of
+// the process; a context made after cudaDeviceReset gets a new one), or 0
+// when there is none or the driver does not say.
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of the scratch array in the current device's context. It is
+// looked up with cudaGetSymbolAddress, with that device current, the first
+// time a context calls, and cached per device together with the context's id:
+// a later context on the same device (the module is loaded again there, for
+// instance after cudaDeviceReset) looks it up anew instead of using a stale
+// address. Returns nullptr and fills `err` on failure.
 void* noalloc_scratch(cudaError_t* err) {
     static std::mutex mu;
     static void* addr[kNoAllocMaxDevices] = {};
+    static unsigned long long ctx_of[kNoAllocMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
         *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
         return nullptr;
     }
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    if (addr[dev] == nullptr || ctx == 0 || ctx != ctx_of[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) {
@@ -73,6 +111,7 @@ void* noalloc_scratch(cudaError_t* err) {
             return nullptr;
         }
         addr[dev] = p;
+        ctx_of[dev] = current_context_id();   // the lookup made the context current if needed
     }
     *err = cudaSuccess;
     return addr[dev];

@@ -270,8 +270,17 @@ __device__ __forceinline__ void emit_ordered(S& sh, const uint32_t* above, const
     }
 }
 
+// True when a bounded wait of the scorer that ran before this kernel in the
+// same call gave up: its staged scores are then incomplete, and every row of
+// the call is written as skipped (-1s, cnt 0) instead of being selected from
+// them. Read after pdl_wait(), when the scorer has completed.
+__device__ __forceinline__ bool scorer_gave_up(const DeviceStatus* status) {
+    return *reinterpret_cast<const volatile int32_t*>(&status->code) == IDX_ERR_TIMEOUT;
+}
+
 // Row checks shared by both kernels. Returns the row length, or -1 after
-// writing the output of a bad row (-1s, cnt 0, status) or of a row that keeps
+// writing the output of a bad row (-1s, cnt 0, status), of every row of a
+// call whose scorer gave up (-1s, cnt 0; `gave_up`), or of a row that keeps
 // every position (n <= K).
 template <int THREADS>
 __device__ __forceinline__ int64_t row_prologue(int t, const int32_t* __restrict__ n_valid,
@@ -279,7 +288,13 @@ __device__ __forceinline__ int64_t row_prologue(int t, const int32_t* __restrict
                                                 int K, int32_t* out, int32_t* __restrict__ cnt,
                                                 DeviceStatus* status,
                                                 const int32_t* __restrict__ cu_q,
-                                                const int32_t* __restrict__ cu_k, int B) {
+                                                const int32_t* __restrict__ cu_k, int B,
+                                                bool gave_up) {
+    if (gave_up) {
+        for (int i = threadIdx.x; i < K; i += THREADS) out[i] = -1;
+        if (cnt && threadIdx.x == 0) cnt[t] = 0;
+        return -1;
+    }
     const int64_t n = (int64_t)__ldg(n_valid + t) + (n_from_pos ? 1 : 0);
     bool bad = n < 0 || n > max_len || n > ld;
     if (cu_q != nullptr) {  // fused call: the row must lie inside its sequence
@@ -316,6 +331,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
                    const int32_t* __restrict__ cu_k, int B, int32_t stage_cap) {
     pdl_wait();
     pdl_launch_dependents();
+    const bool gave_up = scorer_gave_up(status);
     constexpr int D1 = 11;                      // digits: bits 31..21, 20..10, 9..0
     constexpr int kD1Shift = 32 - D1;
     using S = TopkSmem<THREADS, D1>;
@@ -330,7 +346,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         int32_t* out = idx + (int64_t)t * K;
         const int64_t n64 = row_prologue<THREADS>(t, n_valid, n_from_pos, max_len, ld, K, out, cnt,
-                                                  status, cu_q, cu_k, B);
+                                                  status, cu_q, cu_k, B, gave_up);
         if (n64 < 0) continue;
         const int32_t n = (int32_t)n64;
         const int32_t nvec = n >> 2, tail0 = nvec << 2;
@@ -433,6 +449,7 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
                    uint32_t* __restrict__ gbits, int32_t list_cap) {
     pdl_wait();
     pdl_launch_dependents();
+    const bool gave_up = scorer_gave_up(status);
     constexpr int D1 = 12;                      // digits: bits 31..20, 19..10, 9..0
     constexpr int kD1Shift = 32 - D1;
     using S = TopkSmem<THREADS, D1>;
@@ -447,7 +464,7 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         int32_t* out = idx + (int64_t)t * K;
         const int64_t n64 = row_prologue<THREADS>(t, n_valid, n_from_pos, max_len, ld, K, out, cnt,
-                                                  status, cu_q, cu_k, B);
+                                                  status, cu_q, cu_k, B, gave_up);
         if (n64 < 0) continue;
         const int32_t n = (int32_t)n64;
         const int32_t nvec = n >> 2, tail0 = nvec << 2;
@@ -828,7 +845,8 @@ topk_split_finish_kernel(const float* __restrict__ scores, int64_t ld,
     const int t = blockIdx.x;
     int32_t* out = idx + (int64_t)t * K;
     const int64_t n64 = row_prologue<kFinishThreads>(t, n_valid, n_from_pos, max_len, ld, K, out,
-                                                     cnt, status, cu_q, cu_k, B);
+                                                     cnt, status, cu_q, cu_k, B,
+                                                     scorer_gave_up(status));
     if (n64 < 0) return;
     const int32_t n = (int32_t)n64;
     const int32_t nw = (n + 31) >> 5;
@@ -1035,9 +1053,11 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
     const int64_t n64 = selecting_row(t, n_valid, n_from_pos, max_len, ld, K, cu_q, cu_k, B);
     pdl_wait();
     pdl_launch_dependents();
-    if (n64 < 0) {   // the whole cluster returns, before any cluster barrier
+    // (the same in every CTA: only the scorer before this kernel writes a timeout)
+    const bool gave_up = scorer_gave_up(status);
+    if (n64 < 0 || gave_up) {   // the whole cluster returns, before any cluster barrier
         if (r == 0) row_prologue<kClThreads>(t, n_valid, n_from_pos, max_len, ld, K, out, cnt, status,
-                                             cu_q, cu_k, B);
+                                             cu_q, cu_k, B, gave_up);
         return;
     }
     if (hist1 != nullptr) {   // the row's first-digit histogram, from the scorer

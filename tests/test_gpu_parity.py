@@ -16,8 +16,10 @@ The stages are compared on identical inputs: a 1-ulp LayerNorm difference in one
 key element moves a score by ~1e-3 relative, so the scoring of the decode batch
 takes the oracle's post-LayerNorm keys on both sides, and the GPU-chained path is
 checked for consistency with its own scores.
-Full-size workloads are checked on sampled rows the oracle computes one by one.
+Full-size workloads are checked on every row against the oracle (run on all
+host cores), plus quick variants on sampled rows.
 """
+import os
 import zlib
 
 import numpy as np
@@ -31,7 +33,7 @@ from tests._util import (bf16_ulp_distance, bits_of, rule_order_ok, scores_close
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-ORACLE_THREADS = 8
+ORACLE_THREADS = max(os.cpu_count() or 1, 1)
 
 
 @pytest.fixture(scope="module")
@@ -326,6 +328,17 @@ def test_indexer_prefill_ties_full_size_sampled(B):
     _check_exact(B, w, rows=rows)
 
 
+def test_indexer_prefill_ties_full_size_all_rows(B):
+    # every one of the 8,192 rows bit-exact, tie order included (integer inputs)
+    w = workload(3)
+    d = to_device(w)
+    idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len)
+    ridx, rcnt, _ = oracle_rows(w, None, want_scores=False)
+    got_idx, got_cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    bad = np.flatnonzero((got_idx != ridx).any(axis=1) | (got_cnt != rcnt))
+    assert bad.size == 0, f"{bad.size} rows differ, first {bad[:8].tolist()}"
+
+
 def _check_tolerance(B, w, rows, d=None, k_oracle=None):
     d = to_device(w) if d is None else d
     idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len)
@@ -369,6 +382,23 @@ def test_indexer_agentic_chunk_sampled(B):
     w = workload(4)
     rows = [0, 1, 399, 799, 800, 1600, 2401, 3199]
     _check_tolerance(B, w, rows)
+
+
+def test_indexer_agentic_chunk_all_rows(B):
+    # all 3,200 rows: scores within tolerance, sets within the threshold rule,
+    # and the GPU output the rule-ordered top-K of its own scores
+    w = workload(4)
+    _check_tolerance(B, w, list(range(w.T)))
+
+
+def test_indexer_long_decode_all_rows(B):
+    w = workload(5)
+    _check_tolerance(B, w, list(range(w.T)))
+
+
+def test_indexer_spec_verify_all_rows(B):
+    w = workload(6)
+    _check_tolerance(B, w, list(range(w.T)))
 
 
 def test_indexer_long_decode_sampled(B):

@@ -40,11 +40,14 @@ def test_zero_wait_bound_reports_timeout_and_context_survives(B, shape):
     ws = B.workspace(B.score_topk_workspace_size(w.B, w.T, w.max_len), "cuda")
     old = B.set_wait_limit_ns(0)
     try:
-        B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len, ws=ws)
+        idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"],
+                                w.max_len, ws=ws)
         code, _ = B.get_status(ws)          # synchronises: the kernel returned
     finally:
         B.set_wait_limit_ns(old)
     assert code == IDX_ERR_TIMEOUT
+    # nothing is selected from the incomplete scores: every row is skipped
+    assert (cnt.cpu().numpy() == 0).all() and (idx.cpu().numpy() == -1).all()
     # same context, normal bound: a correct result again
     idx, cnt = B.score_topk(d["q"], d["k"], d["w"], d["q_pos"], d["cu_q"], d["cu_k"], w.max_len,
                             ws=ws)

@@ -5,15 +5,19 @@ device memory of its own (a serving engine with a fixed memory plan that bans
 cudaMalloc on its request path, or a plugin handed only its input and output
 buffers). Its scratch is a fixed array inside the library, shared by every
 call, so this test makes two different calls in a row and checks both against
-the workspace entry point. It lives in its own file, collected last, so that a
-run stopping at the first failure has already run every other test; it also
-passes on its own in a fresh process.
+the workspace entry point, then checks a call that fills the 32 MiB of staged
+scores against the CPU oracle itself, and a call whose scorer gives up. It
+lives in its own file, collected last, so that a run stopping at the first
+failure has already run every other test; it also passes on its own in a
+fresh process.
 """
 import ctypes
+import os
 
 import numpy as np
 import pytest
 
+import oracle
 from sparse_attention_key_gb300 import workloads as wl
 from tests._util import to_device
 
@@ -83,3 +87,42 @@ def test_noalloc_rejects_calls_beyond_its_scratch(L):
                                   2048, _p(idx), None, stream)
     assert rc == 3
     assert b"32 MiB" in L.idx_last_error()
+
+
+def test_noalloc_at_its_scratch_limit_matches_the_oracle(L):
+    # 64 queries at the end of one 131,072-key history: 64 * 131,072 * 4 bytes
+    # of staged scores, exactly the 32 MiB the library holds. Integer inputs
+    # with heavy ties: indices and counts bit-exact against the oracle.
+    n, T = 131_072, 64
+    w = wl.custom(904, q_counts=[T], k_lens=[n], kind="int2")
+    assert w.T * ((w.max_len + 3) // 4 * 4) * 4 == 32 << 20
+    d = to_device(w)
+    idx, cnt = _noalloc(L, d, w.T, w.B, w.max_len, w.topk)
+    torch.cuda.synchronize()
+    ridx, rcnt, _ = oracle.score_topk(w.q, w.k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk,
+                                      threads=os.cpu_count() or 8)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+
+
+def test_noalloc_scorer_timeout_leaves_every_row_skipped_then_recovers(L):
+    # With the wait bound at 0 the scorer gives up; the call has no status word
+    # to read, so every row must come back as skipped (cnt 0, idx -1) instead
+    # of a selection from half-written scores. The next call, with the normal
+    # bound, reuses the same scratch and must match the oracle again.
+    from sparse_attention_key_gb300 import binding
+    w = wl.custom(905, q_counts=[1, 1, 1], k_lens=[30000, 9000, 20000], kind="int2")
+    d = to_device(w)
+    old = binding.set_wait_limit_ns(0)
+    try:
+        idx, cnt = _noalloc(L, d, w.T, w.B, w.max_len, w.topk)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_wait_limit_ns(old)
+    assert (cnt.cpu().numpy() == 0).all()
+    assert (idx.cpu().numpy() == -1).all()
+    idx, cnt = _noalloc(L, d, w.T, w.B, w.max_len, w.topk)
+    torch.cuda.synchronize()
+    ridx, rcnt, _ = oracle.score_topk(w.q, w.k, w.w, w.q_pos, w.cu_q, w.cu_k, K=w.topk, threads=3)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
