@@ -380,6 +380,7 @@ class FusedCase:
         gaps = np.array([[ev[i].elapsed_time(ev[i + 1]) for i in range(per_call)] for ev in rows])
         mean = gaps.mean(axis=0)
         out = {"plan": float(mean[0]), "score": float(mean[1]), "topk": float(mean[2:].sum())}
+        self.launch_ms = [float(x) for x in mean]   # every launch of the call, in order
         return out, int(per_call)
 
     def time_ln(self, steps):
@@ -407,7 +408,8 @@ def workload_block(bn: Bench, w: wl.Workload, steps: int, warmup: int, pk: dict)
     block = {"B": w.B, "T": w.T, "pairs": w.pairs, "max_len": w.max_len,
              "fused_ms": fused_ms, "fused_ms_median": float(np.median(ms)),
              "pairs_per_s": w.pairs / (fused_ms / 1e3), "kernels_per_call": per_call,
-             "kernels_ms": kern, "kernel_rooflines": per_kernel, "call_roofline": call,
+             "kernels_ms": kern, "launch_ms": fc.launch_ms, "kernel_rooflines": per_kernel,
+             "call_roofline": call,
              "bound": "tensor" if tensor_bound(w) else "hbm", "steps": steps}
     if fc.chained_ln:
         ln_ms = fc.time_ln(steps)
@@ -471,6 +473,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- per-kernel durations inside the same fused call (events between its launches)
     kern, per_call = fc.time_kernels(args.steps)
+    launch_ms = fc.launch_ms
     ln_ms = fc.time_ln(args.steps) if fc.chained_ln else None
     t_wall2 = time.time()
     clocks.stop()
@@ -589,6 +592,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "kernels_per_call": per_call,
         "kernels_ms": kern,
+        "launch_ms": launch_ms,
         "kernels_source": "events recorded by the library between the kernels of the fused "
                           "call (idx_set_kernel_events), mean over the steps",
         "roofline": roof,

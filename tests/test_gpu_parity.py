@@ -454,6 +454,29 @@ def test_indexer_spec_verify_shapes_exact(B):
     _check_exact(B, w)
 
 
+def test_indexer_many_rows_long_histories_integer_ties_exact(B):
+    # more than 128 rows of more than 32,768 keys: the streamed selection reads
+    # the scorer's segment maxima; with integer inputs the tie groups at the
+    # bound overflow its candidate list on some rows (general path) and not on
+    # others. Bit-exact.
+    w = wl.custom(405, q_counts=[140, 20], k_lens=[40000, 33000], kind="int2")
+    _check_exact(B, w)
+
+
+@pytest.mark.parametrize("kind", ["int4s3", "int2"])
+def test_indexer_many_rows_mixed_lengths_exact(B, kind):
+    # random query positions: rows that keep everything, rows too short for
+    # the segment bound (fewer than 2,048 segments of 16) and rows that use it,
+    # in one call
+    w = wl.custom(406, q_counts=[100, 60], k_lens=[60000, 34000], kind=kind, positions="random")
+    _check_exact(B, w)
+
+
+def test_indexer_many_rows_long_histories_real_values(B):
+    w = wl.custom(407, q_counts=[90, 50], k_lens=[45000, 70000], kind="normal")
+    _check_tolerance(B, w, list(range(w.T)))
+
+
 def test_indexer_decode_integer_ties_long_histories(B):
     # one query per sequence (the scorer histograms the first digit itself) on
     # integer inputs: tie groups far larger than the selection's candidate list
