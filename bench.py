@@ -693,6 +693,26 @@ def run_project(args):
         torch.cuda.synchronize()
         ms.append(a.elapsed_time(e))
     us = float(np.median(ms)) * 1e3
+    # each launch of one call, from events the library records between them
+    n0 = B.kernel_launches()
+    call()
+    torch.cuda.synchronize()
+    per_call = B.kernel_launches() - n0
+    rows = []
+    for _ in range(args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(per_call + 1)]
+        for e in ev:
+            e.record()
+        flush_w.zero_()
+        flush_r.max()
+        ev[0].record()
+        B.set_kernel_events(ev[1:])
+        call()
+        B.set_kernel_events([])
+        rows.append(ev)
+    torch.cuda.synchronize()
+    launch_us = [float(x) * 1e3 for x in np.mean([[ev[i].elapsed_time(ev[i + 1]) for i in range(per_call)]
+                                                 for ev in rows], axis=0)]
     flops = 2.0 * T * (4096 * R + 128 * H + 32 * H)
     weight_bytes = 2.0 * (4096 * R + 128 * H + 32 * H)
     io_bytes = 2.0 * T * (H + R + 4096 + 128 * 2) + 4.0 * T * 32
@@ -704,8 +724,9 @@ def run_project(args):
              "frac": tflops / pk["bf16_tflops"]} if bound == "tensor" else
             {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"]})
     print(json.dumps({"mode": "project", "T": T, "hidden": H, "q_rank": R, "steps": args.steps,
-                      "us_per_call": us, "tflops": tflops, "bytes_per_call": weight_bytes + io_bytes,
-                      "roofline": roof, "gemm": "cuBLASLt (bf16 in, fp32 accumulate)",
+                      "us_per_call": us, "launch_us": launch_us, "tflops": tflops,
+                      "bytes_per_call": weight_bytes + io_bytes,
+                      "roofline": roof, "gemm": "library tcgen05 GEMM (bf16 in, fp32 accumulate)",
                       "l2": "flushed between calls: 256 MB written, then 256 MB read"}), flush=True)
 
 

@@ -125,13 +125,19 @@ IDX_API idx_status idx_key_layernorm_append(const uint16_t* k_raw, const void* l
  *   k_pre[t]         = W_k . x[t]        W_k [128, hidden]     -> bf16 (workspace)
  *   k_cache[slot[t]] = LayerNorm(k_pre[t]) as idx_key_layernorm_append
  *   w[t]             = W_w . x[t]        W_w [32, hidden]      -> w fp32 [T,32]
- * Any scale of the per-head weights is part of W_w. The three products are
- * plain GEMMs run by cuBLASLt inside the caller's workspace (ws: 256-byte
- * aligned, idx_indexer_project_workspace_size(T) bytes); the library
- * allocates nothing. x [T,hidden] and q_lora [T,q_rank] are bf16 row-major;
- * hidden and q_rank are multiples of 8; matrices 16-byte aligned. slot and
- * the LayerNorm parameters are as for idx_key_layernorm_append. The first
- * call creates the process's cuBLASLt handle (host state only).
+ * Any scale of the per-head weights is part of W_w. The products run on the
+ * library's own tensor-core GEMM (the key and weight products in one pass over
+ * x); with few tokens K is split over the SMs and the fp32 partial sums are
+ * added by a second kernel, which for the key also rounds k_pre to bf16 and
+ * appends its LayerNorm to the cache (bit-identical to
+ * idx_key_layernorm_append). ws: 256-byte aligned, at least
+ * idx_indexer_project_workspace_size(T) bytes (a size that depends on the
+ * current device's SM count); it holds the status word (idx_get_status reads
+ * it: IDX_ERR_TIMEOUT if a bounded wait of the GEMM gave up) and the partial
+ * sums. The library allocates nothing. x [T,hidden] and q_lora
+ * [T,q_rank] are bf16 row-major; hidden and q_rank are multiples of 8;
+ * matrices 16-byte aligned. slot and the LayerNorm parameters are as for
+ * idx_key_layernorm_append.
  */
 IDX_API size_t idx_indexer_project_workspace_size(int32_t T);
 IDX_API idx_status idx_indexer_project(const uint16_t* x, const uint16_t* q_lora,
@@ -288,7 +294,7 @@ IDX_API uint64_t idx_kernel_launches(void);
 
 /*
  * Test hook for failure detection: sets the bound, in nanoseconds, of every
- * wait inside the tensor-core kernels (the scorer and the sparse MLA
+ * wait inside the tensor-core kernels (the scorer, the projection GEMM and the sparse MLA
  * attention; default 2,000,000,000) for launches enqueued from now on, and
  * returns the previous bound. When a wait runs out
  * the kernel records IDX_ERR_TIMEOUT in the status word, stops all its roles,

@@ -73,7 +73,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, err in results:
             sys.stderr.write(err)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcublasLt"]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

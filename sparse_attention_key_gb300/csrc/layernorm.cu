@@ -15,6 +15,7 @@
 // low enough that the kernel is bound by memory rather than issue.
 #include "common.cuh"
 #include "launch.h"
+#include "ln_row.cuh"
 
 namespace lidx {
 
@@ -34,19 +35,7 @@ key_layernorm_kernel(const uint4* x, const void* __restrict__ ln_w, const void* 
     const int half = lane >> 4;          // which row of the pair
     const int hl = lane & 15;            // lane within the half-warp: features 8*hl .. 8*hl+7
     float2 g[4], b[4];   // features 8*hl + 2k, 8*hl + 2k + 1
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int d = hl * 8 + 2 * k;
-        if (kF32Params) {
-            g[k] = make_float2(static_cast<const float*>(ln_w)[d], static_cast<const float*>(ln_w)[d + 1]);
-            b[k] = make_float2(static_cast<const float*>(ln_b)[d], static_cast<const float*>(ln_b)[d + 1]);
-        } else {
-            const uint16_t* w16 = static_cast<const uint16_t*>(ln_w);
-            const uint16_t* b16 = static_cast<const uint16_t*>(ln_b);
-            g[k] = make_float2(__uint_as_float(uint32_t(w16[d]) << 16), __uint_as_float(uint32_t(w16[d + 1]) << 16));
-            b[k] = make_float2(__uint_as_float(uint32_t(b16[d]) << 16), __uint_as_float(uint32_t(b16[d + 1]) << 16));
-        }
-    }
+    ln_params_half_warp(ln_w, ln_b, kF32Params, hl, g, b);
     const int64_t warp_id = (int64_t)blockIdx.x * kLnWarpsPerBlock + (threadIdx.x >> 5);
     const int64_t n_warps = (int64_t)gridDim.x * kLnWarpsPerBlock;
     constexpr int kRowsPerIter = 2 * kLnRowsInFlight;
@@ -68,35 +57,8 @@ key_layernorm_kernel(const uint4* x, const void* __restrict__ ln_w, const void* 
 #pragma unroll
         for (int i = 0; i < kLnRowsInFlight; ++i) {
             const int64_t row = r0 + 2 * i + half;
-            // packed pairs of features (2k, 2k+1): the two bf16 halves of one word
-            const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-            float2 f[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) f[k] = make_float2(bf16_lo(wv[k]), bf16_hi(wv[k]));
-            const float2 s2 = __fadd2_rn(__fadd2_rn(f[0], f[1]), __fadd2_rn(f[2], f[3]));
-            float s = s2.x + s2.y;
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            const float mean = s * (1.0f / kDim);
-            const float2 nm = make_float2(-mean, -mean);
-            float2 c[4];
-            float2 q = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                c[k] = __fadd2_rn(f[k], nm);
-                q = __ffma2_rn(c[k], c[k], q);
-            }
-            float ss = q.x + q.y;
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float inv = rsqrtf(fmaf(ss, 1.0f / kDim, eps));
-            const float2 inv2 = make_float2(inv, inv);
             uint32_t o16[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 o = __ffma2_rn(__fmul2_rn(c[k], inv2), g[k], b[k]);
-                o16[k] = f32x2_to_bf16x2_rn(o.x, o.y);
-            }
+            ln_row_half_warp(v[i], g, b, eps, o16);
             if (row < n_rows && dst[i] >= 0) y[dst[i] * 16 + hl] = make_uint4(o16[0], o16[1], o16[2], o16[3]);
         }
     }

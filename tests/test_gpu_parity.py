@@ -266,6 +266,37 @@ def test_indexer_project_integer_inputs_exact(B):
     assert (cache[untouched] == 0).all()
 
 
+def _proj_check_exact(B, seed, T, hidden, rank, cache_rows):
+    x, ql, wq, wk, ww, g, b = _proj_inputs(seed, T, hidden, rank, integer=True)
+    slot = np.random.default_rng(seed).permutation(cache_rows)[:T].astype(np.int64)
+    q, w, cache = _proj_run(B, x, ql, wq, wk, ww, g, b, cache_rows, slot)
+    rq, rk, rw, rk_pre = oracle.indexer_project(x, ql, wq, wk, ww, oracle.bf16_bits_to_f64(g),
+                                                oracle.bf16_bits_to_f64(b), float(np.float32(1e-6)))
+    assert np.array_equal(q, rq)
+    assert np.array_equal(w, rw.astype(np.float32))
+    beta = oracle.bf16_bits_to_f64(b)
+    _, y = oracle.key_layernorm(rk_pre, oracle.bf16_bits_to_f64(g), beta, float(np.float32(1e-6)))
+    got = cache[slot]
+    dist = bf16_ulp_distance(got, rk)
+    err = np.abs(oracle.bf16_bits_to_f64(got) - y)
+    bound = 2.0 ** -17 * (np.abs(y - beta[None, :]) + np.abs(beta[None, :]))
+    assert not ((dist > 1) & (err > bound)).any()
+
+
+def test_indexer_project_many_tokens_exact(B):
+    # 1,300 tokens: 11 row tiles (6 pairs, the last with a tile past the end)
+    # x 16 column tiles of q, enough work without splitting K (bf16 written
+    # straight from the accumulators); the key/weight product splits K.
+    # Integer inputs: exact.
+    _proj_check_exact(B, 43, 1300, 7168, 1536, 1400)
+
+
+def test_indexer_project_ragged_k_and_rows_exact(B):
+    # hidden and q_rank not multiples of the 64-wide K block (the last block
+    # reads zeros past the matrix), and a second row tile with 2 valid rows
+    _proj_check_exact(B, 44, 130, 1000, 520, 200)
+
+
 def test_indexer_project_real_valued(B):
     T, hidden, rank = 64, 1024, 512
     x, ql, wq, wk, ww, g, b = _proj_inputs(42, T, hidden, rank, integer=False)

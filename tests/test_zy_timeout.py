@@ -82,3 +82,34 @@ def test_sparse_mla_zero_wait_bound_reports_timeout_and_context_survives(B):
         vmax = np.abs(lat[cu_k[b] + idx[t, :cnt[t]]]).max()
         assert np.abs(o[t] - o_ref[t]).max() <= 2.0 ** -8 * vmax
         np.testing.assert_allclose(l[t], l_ref[t], atol=2e-4)
+
+
+def test_projection_gemm_zero_wait_bound_reports_timeout_and_context_survives(B):
+    """The projection GEMM's waits are bounded too: with a bound of 0 the call
+    reports IDX_ERR_TIMEOUT in its workspace's status word, and the same context
+    then computes the exact projections again."""
+    rng = np.random.default_rng(731)
+    T, hidden, rank = 40, 512, 256
+    mk = lambda shape: wl.f32_to_bf16_bits(rng.integers(-2, 3, size=shape).astype(np.float32))
+    x, ql = mk((T, hidden)), mk((T, rank))
+    wq, wk, ww = mk((4096, rank)), mk((128, hidden)), mk((32, hidden))
+    g = wl.f32_to_bf16_bits(np.ones(128, np.float32))
+    b = wl.f32_to_bf16_bits(np.zeros(128, np.float32))
+    dv = lambda a: torch.from_numpy(a.view(np.int16)).cuda()
+    args = (dv(x), dv(ql), dv(wq), dv(wk), dv(ww), dv(g), dv(b), 1e-6)
+    cache = torch.zeros((T, 128), dtype=torch.int16, device="cuda")
+    slot = torch.arange(T, dtype=torch.int64, device="cuda")
+    from sparse_attention_key_gb300 import binding
+    ws = B.workspace(int(binding.lib().idx_indexer_project_workspace_size(T)), "cuda")
+    old = B.set_wait_limit_ns(0)
+    try:
+        B.indexer_project(*args, cache, slot, ws=ws)
+        code, _ = B.get_status(ws)
+    finally:
+        B.set_wait_limit_ns(old)
+    assert code == IDX_ERR_TIMEOUT
+    q, w = B.indexer_project(*args, cache, slot, ws=ws)
+    assert B.get_status(ws) == (0, 0)
+    rq, _, rw, _ = oracle.indexer_project(x, ql, wq, wk, ww, np.ones(128), np.zeros(128), 1e-6)
+    assert np.array_equal(q.view(torch.int16).cpu().numpy().view(np.uint16), rq)
+    assert np.array_equal(w.cpu().numpy(), rw.astype(np.float32))
