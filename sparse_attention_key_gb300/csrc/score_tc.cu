@@ -108,6 +108,36 @@ __device__ __forceinline__ void write_empty_descs(const TcPlan& plan, int grid) 
     }
 }
 
+// Extra cost of starting a group, in key tiles, for the scorers with several
+// queries per group: loading the group's queries (one buffer: the MMAs wait)
+// and the epilogue's per-group set-up.
+constexpr int kGroupStartCost = 2;
+
+// First step of scorer CTA c of `grid` when the CTAs share the steps by cost:
+// a step costs 1, and the first step of a group kGroupStartCost more. CTA c
+// starts at the first step s whose cost before it, s + kGroupStartCost * (group
+// starts before s), reaches total_cost * c / grid. sb[0..n_groups] are the
+// groups' first steps (sb[n_groups] = total).
+__device__ __forceinline__ int32_t cost_boundary(const int32_t* sb, int n_groups, int64_t total,
+                                                 int grid, int c) {
+    if (c >= grid) return (int32_t)total;
+    const int64_t total_cost = total + (int64_t)kGroupStartCost * n_groups;
+    const int64_t target = total_cost * c / grid;
+    // the last group g whose first step's cost-before (sb[g] + K*g) is <= target
+    int lo = 0, hi = n_groups - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)sb[mid] + (int64_t)kGroupStartCost * mid <= target) lo = mid; else hi = mid - 1;
+    }
+    const int64_t at = (int64_t)sb[lo] + (int64_t)kGroupStartCost * lo;
+    if (target <= at) return sb[lo];
+    // inside group lo the step sb[lo] + j (j >= 1) has cost-before at + K + j
+    int64_t j = target - at - kGroupStartCost;
+    if (j < 1) j = 1;
+    const int64_t s = (int64_t)sb[lo] + j;
+    return (int32_t)(s < sb[lo + 1] ? s : sb[lo + 1]);
+}
+
 constexpr int kPlanThreads = 1024;
 
 __device__ __forceinline__ int block_exclusive_sum(int v, int* warp_sums, int* total) {
@@ -242,6 +272,11 @@ tc_plan_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu
         return;
     }
     __syncthreads();   // step_begin and groups are complete
+    if (GQ > 4) {   // several queries per group: CTA c's first step, steps shared uniformly
+        for (int c = threadIdx.x; c < grid; c += kPlanThreads)
+            plan.cta_desc[2 * c].x = (int32_t)((int64_t)carry * c / grid);
+        return;
+    }
     for (int c = threadIdx.x; c < grid; c += kPlanThreads)
         write_cta_desc(plan, plan.step_begin, n_groups, carry, grid, c);
 }
@@ -377,6 +412,15 @@ tc_plan_fast_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict
         return;
     }
     __syncthreads();   // step offsets and groups are complete
+    if (GQ > 4) {
+        // several queries per group: [2c].x = the first step of CTA c, the
+        // steps shared by cost (uniform when the group starts are not in
+        // shared memory)
+        for (int c = threadIdx.x; c < grid; c += kPlanThreads)
+            plan.cta_desc[2 * c].x = sb_shared ? cost_boundary(s_sb, n_groups, total, grid, c)
+                                               : (int32_t)((int64_t)total * c / grid);
+        return;
+    }
     for (int c = threadIdx.x; c < grid; c += kPlanThreads)
         write_cta_desc(plan, sb_shared ? s_sb : plan.step_begin, n_groups, total, grid, c);
 }
@@ -557,8 +601,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
     } else {
         n_groups = plan.hdr->n_groups;
         const int64_t total = plan.hdr->total_steps;
-        beg = (int32_t)(total * blockIdx.x / gridDim.x);
-        end = (int32_t)(total * (blockIdx.x + 1) / gridDim.x);
+        // the plan's cost-weighted boundaries (see cost_boundary)
+        beg = plan.cta_desc[2 * blockIdx.x].x;
+        end = blockIdx.x + 1 < gridDim.x ? plan.cta_desc[2 * (blockIdx.x + 1)].x : (int32_t)total;
     }
     auto start_cursor = [&](StepCursor& c) {
         if (C::GQ <= 4) c.init(start, start_group);
