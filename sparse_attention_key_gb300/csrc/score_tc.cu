@@ -85,32 +85,12 @@ static TcPlan plan_layout(void* base, int32_t B, int32_t T) {
     return pl;
 }
 
-// CTA c of `grid` scorer CTAs takes the steps [total*c/grid, total*(c+1)/grid).
-// Descriptor of scorer CTA c, whose first step is found by binary search in
+// Descriptor of scorer CTA c of `grid`, which takes the steps between its
+// boundary and the next CTA's; its first group is found by binary search in
 // sb[0..n_groups] (shared or global memory; sb[n_groups] == total > 0).
-__device__ __forceinline__ void write_cta_desc(const TcPlan& plan, const int32_t* sb, int n_groups,
-                                               int64_t total, int grid, int c) {
-    const int64_t beg = total * c / grid, end = total * (c + 1) / grid;
-    int lo = 0, hi = n_groups - 1;   // the last group whose first step is <= beg
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (sb[mid] <= beg) lo = mid; else hi = mid - 1;
-    }
-    plan.cta_desc[2 * c] = make_int4(lo, (int)(beg - sb[lo]), sb[lo + 1], (int)end);
-    plan.cta_desc[2 * c + 1] = plan.groups[lo];
-}
-
-// Descriptors of a plan with no steps: every CTA has an empty range.
-__device__ __forceinline__ void write_empty_descs(const TcPlan& plan, int grid) {
-    for (int c = threadIdx.x; c < grid; c += blockDim.x) {
-        plan.cta_desc[2 * c] = make_int4(0, 0, 0, 0);
-        plan.cta_desc[2 * c + 1] = make_int4(0, 0, 0, 0);
-    }
-}
-
-// Extra cost of starting a group, in key tiles, for the scorers with several
-// queries per group: loading the group's queries (one buffer: the MMAs wait)
-// and the epilogue's per-group set-up.
+// Extra cost of starting a group, in key tiles, for the scorers: loading the
+// group's queries (one buffer: the MMAs wait) and the epilogue's per-group
+// set-up (and, with one query per group, its first-digit histogram flush).
 constexpr int kGroupStartCost = 2;
 
 // First step of scorer CTA c of `grid` when the CTAs share the steps by cost:
@@ -136,6 +116,29 @@ __device__ __forceinline__ int32_t cost_boundary(const int32_t* sb, int n_groups
     if (j < 1) j = 1;
     const int64_t s = (int64_t)sb[lo] + j;
     return (int32_t)(s < sb[lo + 1] ? s : sb[lo + 1]);
+}
+
+
+// by_cost: boundaries by cost (sb in shared memory), else uniform in steps.
+__device__ __forceinline__ void write_cta_desc(const TcPlan& plan, const int32_t* sb, int n_groups,
+                                               int64_t total, int grid, int c, bool by_cost) {
+    const int64_t beg = by_cost ? cost_boundary(sb, n_groups, total, grid, c) : total * c / grid;
+    const int64_t end = by_cost ? cost_boundary(sb, n_groups, total, grid, c + 1) : total * (c + 1) / grid;
+    int lo = 0, hi = n_groups - 1;   // the last group whose first step is <= beg
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sb[mid] <= beg) lo = mid; else hi = mid - 1;
+    }
+    plan.cta_desc[2 * c] = make_int4(lo, (int)(beg - sb[lo]), sb[lo + 1], (int)end);
+    plan.cta_desc[2 * c + 1] = plan.groups[lo];
+}
+
+// Descriptors of a plan with no steps: every CTA has an empty range.
+__device__ __forceinline__ void write_empty_descs(const TcPlan& plan, int grid) {
+    for (int c = threadIdx.x; c < grid; c += blockDim.x) {
+        plan.cta_desc[2 * c] = make_int4(0, 0, 0, 0);
+        plan.cta_desc[2 * c + 1] = make_int4(0, 0, 0, 0);
+    }
 }
 
 constexpr int kPlanThreads = 1024;
@@ -278,7 +281,7 @@ tc_plan_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu
         return;
     }
     for (int c = threadIdx.x; c < grid; c += kPlanThreads)
-        write_cta_desc(plan, plan.step_begin, n_groups, carry, grid, c);
+        write_cta_desc(plan, plan.step_begin, n_groups, carry, grid, c, false);
 }
 
 // Fast plan for up to kPlanSeqs sequences: one thread per sequence reads its
@@ -422,7 +425,7 @@ tc_plan_fast_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict
         return;
     }
     for (int c = threadIdx.x; c < grid; c += kPlanThreads)
-        write_cta_desc(plan, sb_shared ? s_sb : plan.step_begin, n_groups, total, grid, c);
+        write_cta_desc(plan, sb_shared ? s_sb : plan.step_begin, n_groups, total, grid, c, sb_shared);
 }
 
 // ---------------------------------------------------------------------------
