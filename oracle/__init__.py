@@ -67,6 +67,10 @@ def _load():
             lib.oracle_score_topk.restype = ctypes.c_int
             lib.oracle_sparse_mla.argtypes = [P, P, P, i64, i32, ctypes.c_double, P, P]
             lib.oracle_sparse_mla.restype = None
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = ctypes.c_double
+            lib.oracle_sparse_mla_fp8.argtypes = [P, P, P, P, i64, i32, ctypes.c_double, P, P]
+            lib.oracle_sparse_mla_fp8.restype = None
             _lib = lib
     return _lib
 
@@ -254,4 +258,54 @@ def sparse_mla_batch(q_bits, cache_bits, idx, cnt, cu_q, cu_k, scale: float, row
         b = int(np.searchsorted(cq, t, side="right")) - 1
         pos = np.asarray(idx[t][:int(cnt[t])], dtype=np.int64)
         o[t], lse[t] = sparse_mla(q[t], cache_bits, ck[b] + pos, scale)
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) MLA cache rows
+# ---------------------------------------------------------------------------
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Exact values of E4M3 codes (uint8), as float64 (NaN for the NaN codes)."""
+    lib = _load()
+    table = np.array([lib.oracle_e4m3_to_double(b) for b in range(256)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def sparse_mla_fp8(q_t_bits, cache8, row_scale, rows, scale: float):
+    """sparse_mla over FP8 rows: row r's value is row_scale[r] x e4m3(cache8[r]).
+
+    TokenSpeed's K3 post (section 2, MLA) stores the MLA cache in FP8; a row
+    holds 576 E4M3 codes and one scale. ``cache8`` uint8 [L, 576], ``row_scale``
+    [L] (any float dtype, used exactly), ``rows`` absolute row numbers, q [H, 576]
+    bf16 bits. Returns (o [H, 512], lse [H]) in fp64.
+    """
+    lib = _load()
+    q = _c(q_t_bits, np.uint16).reshape(-1, MLA_DIM)
+    c = _c(cache8, np.uint8).reshape(-1, MLA_DIM)
+    sc = _c(row_scale, np.float64).reshape(-1)
+    r = _c(rows, np.int64).reshape(-1)
+    assert r.size == 0 or (r.min() >= 0 and r.max() < c.shape[0])
+    H = q.shape[0]
+    o = np.empty((H, MLA_VDIM), dtype=np.float64)
+    lse = np.empty(H, dtype=np.float64)
+    lib.oracle_sparse_mla_fp8(_ptr(q), _ptr(c), _ptr(sc), _ptr(r), r.size, H, float(scale), _ptr(o),
+                              _ptr(lse))
+    return o, lse
+
+
+def sparse_mla_fp8_batch(q_bits, cache8, row_scale, idx, cnt, cu_q, cu_k, scale: float, rows=None):
+    """sparse_mla_fp8 for each query row t of a packed ragged batch (see
+    sparse_mla_batch). Returns (o [T, H, 512], lse [T, H]); rows outside
+    ``rows`` (when given) are left NaN."""
+    q = _c(q_bits, np.uint16)
+    T, H = q.shape[0], q.shape[1]
+    cq = np.asarray(cu_q).reshape(-1)
+    ck = np.asarray(cu_k).reshape(-1)
+    o = np.full((T, H, MLA_VDIM), np.nan)
+    lse = np.full((T, H), np.nan)
+    for t in (range(T) if rows is None else rows):
+        b = int(np.searchsorted(cq, t, side="right")) - 1
+        pos = np.asarray(idx[t][:int(cnt[t])], dtype=np.int64)
+        o[t], lse[t] = sparse_mla_fp8(q[t], cache8, row_scale, ck[b] + pos, scale)
     return o, lse

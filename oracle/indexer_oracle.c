@@ -31,6 +31,10 @@
  *     a zero query (o = the mean latent, lse = log n), a large scale (o tends
  *     to the top-logit row), order of the selected rows, and the result
  *     against scipy's softmax/logsumexp over a numpy matmul of the rows.
+ *   - oracle_e4m3_to_double: hand-derived codes (zero, subnormals, 1.0, the
+ *     largest finite 448, NaN) and every code against torch's float8_e4m3fn.
+ *   - oracle_sparse_mla_fp8: equal to oracle_sparse_mla on rows whose
+ *     dequantised values are exact bf16 values; one selected row.
  */
 #include <math.h>
 #include <stdint.h>
@@ -290,6 +294,65 @@ void oracle_sparse_mla(const uint16_t* q_t, const uint16_t* cache, const int64_t
             const double p = exp(logit[j] - m) / sum;
             const uint16_t* c = cache + rows[j] * MLA_DIM;
             for (int d = 0; d < MLA_VDIM; ++d) oh[d] += p * oracle_bf16_to_double(c[d]);
+        }
+        lse[h] = m + log(sum);
+    }
+    free(logit);
+}
+
+/* ---------------------------------------------------------------------------
+ * FP8 (E4M3) cache rows for the sparse MLA attention.
+ * "Kimi K3 on AMD Instinct GPUs with TokenSpeed", section 2 (MLA), stores the
+ * MLA cache in FP8. Reading: each cached row is 576 E4M3 codes and one scale
+ * (a row's value is scale x the code's value); the pages give no scale
+ * granularity, and per row is the plainest. E4M3 as commonly defined (OCP
+ * 8-bit floating point): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits; exponent 0 holds the subnormals m/8 x 2^-6; the pattern with all
+ * exponent and mantissa bits set is NaN; there is no infinity.
+ * ------------------------------------------------------------------------- */
+
+double oracle_e4m3_to_double(uint8_t b) {
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9)               /* m/8 x 2^(1-7) */
+                              : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/*
+ * The attention of oracle_sparse_mla over FP8 rows: c_j[d] = scale_row[rows[j]]
+ * x e4m3(cache8[rows[j] * 576 + d]), in fp64; the same softmax, output and
+ * log-sum-exp.
+ */
+void oracle_sparse_mla_fp8(const uint16_t* q_t, const uint8_t* cache8, const double* row_scale,
+                           const int64_t* rows, int64_t n, int32_t heads, double scale, double* o,
+                           double* lse) {
+    double* logit = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    for (int32_t h = 0; h < heads; ++h) {
+        const uint16_t* qh = q_t + (int64_t)h * MLA_DIM;
+        double* oh = o + (int64_t)h * MLA_VDIM;
+        for (int d = 0; d < MLA_VDIM; ++d) oh[d] = 0.0;
+        if (n <= 0) {
+            lse[h] = -INFINITY;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < n; ++j) {
+            const uint8_t* c = cache8 + rows[j] * MLA_DIM;
+            const double sr = row_scale[rows[j]];
+            double dot = 0.0;
+            for (int d = 0; d < MLA_DIM; ++d)
+                dot += oracle_bf16_to_double(qh[d]) * (sr * oracle_e4m3_to_double(c[d]));
+            logit[j] = scale * dot;
+            if (logit[j] > m) m = logit[j];
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < n; ++j) sum += exp(logit[j] - m);
+        for (int64_t j = 0; j < n; ++j) {
+            const double p = exp(logit[j] - m) / sum;
+            const uint8_t* c = cache8 + rows[j] * MLA_DIM;
+            const double sr = row_scale[rows[j]];
+            for (int d = 0; d < MLA_VDIM; ++d) oh[d] += p * (sr * oracle_e4m3_to_double(c[d]));
         }
         lse[h] = m + log(sum);
     }

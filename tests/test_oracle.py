@@ -503,3 +503,62 @@ def test_mla_inputs_follow_the_indexer_output_format():
         sel = idx[t, :cnt[t]]
         assert np.all(np.diff(sel) > 0) and sel.min() >= 0 and sel.max() < n
         assert np.all(idx[t, cnt[t]:] == -1)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) MLA cache rows
+# ---------------------------------------------------------------------------
+
+def test_e4m3_hand_derived_codes():
+    # sign | exponent (4 bits, bias 7) | mantissa (3 bits); exponent 0: m/8 x 2^-6
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x38: 1.0, 0x39: 1.125, 0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    got = oracle.e4m3_to_f64(list(cases))
+    assert np.array_equal(got, np.array(list(cases.values())))
+    assert np.signbit(oracle.e4m3_to_f64([0x80]))[0]
+    assert np.isnan(oracle.e4m3_to_f64([0x7F, 0xFF])).all()
+
+
+def test_e4m3_every_code_against_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def _bf16_exact_fp8_rows(rng, n, pow2_scales=True):
+    # codes with |value| <= 8 and power-of-two row scales: every dequantised
+    # value is an exact bf16 value (<= 4 significant bits)
+    codes = rng.integers(0, 256, size=(n, 576)).astype(np.uint8)
+    codes[(codes & 0x7F) >= 0x58] &= 0x47          # keep exponents small (|v| < 2^4), no NaN
+    scale = 2.0 ** rng.integers(-3, 2, size=n).astype(np.float64)
+    return codes, scale
+
+
+def test_mla_fp8_equals_bf16_attention_on_exact_rows():
+    rng = np.random.default_rng(31)
+    codes, scale = _bf16_exact_fp8_rows(rng, 40)
+    vals = scale[:, None] * oracle.e4m3_to_f64(codes)
+    bits = oracle.f64_to_bf16_bits(vals)
+    assert np.array_equal(oracle.bf16_bits_to_f64(bits), vals)   # exact in bf16
+    q = wl.f32_to_bf16_bits(rng.standard_normal((6, 576)).astype(np.float32) * 0.1)
+    rows = np.array([3, 17, 0, 39, 22, 5])
+    o8, l8 = oracle.sparse_mla_fp8(q, codes, scale, rows, 0.07)
+    ob, lb = oracle.sparse_mla(q, bits, rows, 0.07)
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
+
+
+def test_mla_fp8_single_row_returns_its_dequantised_latent():
+    rng = np.random.default_rng(32)
+    codes, scale = _bf16_exact_fp8_rows(rng, 5)
+    scale[2] = 0.3                                   # any real scale
+    q = wl.f32_to_bf16_bits(rng.standard_normal((4, 576)).astype(np.float32))
+    o, lse = oracle.sparse_mla_fp8(q, codes, scale, np.array([2]), 0.05)
+    c = 0.3 * oracle.e4m3_to_f64(codes[2])
+    assert np.allclose(o, np.broadcast_to(c[:512], o.shape), rtol=0, atol=1e-15)
+    assert np.allclose(lse, 0.05 * (oracle.bf16_bits_to_f64(q) @ c), rtol=1e-14, atol=1e-14)
