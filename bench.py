@@ -751,10 +751,19 @@ def run_mla(args):
     H, K = 96, 2048
     T, L = len(lens), int(sum(lens))
     gen = torch.Generator(device=dev).manual_seed(17)
-    cache = torch.empty((L, 576), dtype=torch.bfloat16, device=dev)
-    for r0 in range(0, L, 1 << 20):   # N(0,1) rows, in chunks
-        r1 = min(L, r0 + (1 << 20))
-        cache[r0:r1] = torch.randn((r1 - r0, 576), generator=gen, device=dev).to(torch.bfloat16)
+    if args.fp8:   # E4M3 codes (random bytes, NaN codes moved to 0) and fp32 row scales
+        cache = torch.empty((L, 576), dtype=torch.uint8, device=dev)
+        for r0 in range(0, L, 1 << 18):
+            r1 = min(L, r0 + (1 << 18))
+            blk = torch.randint(0, 256, (r1 - r0, 576), generator=gen, device=dev, dtype=torch.int32)
+            blk = torch.where((blk & 0x7F) == 0x7F, torch.zeros_like(blk), blk)
+            cache[r0:r1] = blk.to(torch.uint8)
+        row_scale = torch.exp2(torch.rand((L,), generator=gen, device=dev) * -8.0).float()
+    else:
+        cache = torch.empty((L, 576), dtype=torch.bfloat16, device=dev)
+        for r0 in range(0, L, 1 << 20):   # N(0,1) rows, in chunks
+            r1 = min(L, r0 + (1 << 20))
+            cache[r0:r1] = torch.randn((r1 - r0, 576), generator=gen, device=dev).to(torch.bfloat16)
     q = torch.randn((T, H, 576), generator=gen, device=dev).to(torch.bfloat16)
     idx = torch.full((T, K), -1, dtype=torch.int32, device=dev)
     for t, n in enumerate(lens):   # distinct positions, ascending, as the indexer emits them
@@ -768,7 +777,11 @@ def run_mla(args):
     ws = B.workspace(B.sparse_mla_workspace_size(T, H, K), dev)
     flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
     flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
-    call = lambda: B.sparse_mla(q, cache, idx, cnt, cu_q, cu_k, scale, out=out, lse=lse, ws=ws)
+    if args.fp8:
+        call = lambda: B.sparse_mla_fp8(q, cache, row_scale, idx, cnt, cu_q, cu_k, scale, out=out, lse=lse,
+                                        ws=ws)
+    else:
+        call = lambda: B.sparse_mla(q, cache, idx, cnt, cu_q, cu_k, scale, out=out, lse=lse, ws=ws)
     for _ in range(max(args.warmup, 3)):
         call()
     torch.cuda.synchronize()
@@ -787,7 +800,8 @@ def run_mla(args):
     launches = (B.kernel_launches() - n0) // max(args.steps, 1)
     us = float(np.median(ms)) * 1e3
     pairs = T * K
-    bytes_alg = pairs * 576 * 2 + T * H * 576 * 2 + T * H * 512 * 4 + T * H * 4 + T * K * 4
+    row_bytes = 576 + 4 if args.fp8 else 576 * 2   # a selected row (FP8: codes + its scale)
+    bytes_alg = pairs * row_bytes + T * H * 576 * 2 + T * H * 512 * 4 + T * H * 4 + T * K * 4
     flops = 2.0 * pairs * H * (576 + 512)
     pk = peaks()
     gbs = bytes_alg / (us * 1e-6) / 1e9
@@ -796,9 +810,11 @@ def run_mla(args):
         "mode": "sparse_mla", "metric": "sparse MLA (query, selected position) pairs/s",
         "value": pairs / (us * 1e-6), "unit": "pairs/s", "higher_is_better": True,
         "config": {"workload": args.mla, "queries": T, "heads": H, "topk": K, "cache_rows": L,
-                   "row": "576 bf16 (512 latent + 64 key dims)", "scale": "1/sqrt(192)"},
+                   "row": ("576 E4M3 codes + an fp32 scale" if args.fp8 else "576 bf16")
+                   + " (512 latent + 64 key dims)", "scale": "1/sqrt(192)"},
         "steps": args.steps, "us_per_call": us, "gpu_launches_per_call": launches,
-        "dtype": "bf16 in, fp32 accumulate and out",
+        "dtype": ("e4m3 cache, bf16 q and MMA operands" if args.fp8 else "bf16 in")
+        + ", fp32 accumulate and out",
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / pk["hbm_gbs"], "bytes_per_call": bytes_alg},
         "tensor": {"achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
@@ -925,6 +941,8 @@ def main():
     ap.add_argument("--mla", choices=["decode_batch", "long_decode"], default=None,
                     help="time the sparse MLA attention over 2048 selected positions per query "
                          "(96 heads) on that workload's shapes; prints its own JSON line")
+    ap.add_argument("--fp8", action="store_true",
+                    help="--mla: FP8 (E4M3) cache rows with an fp32 scale each")
     ap.add_argument("--fused-only", action="store_true",
                     help="time only the fused steps (for profiler captures); prints a short line")
     ap.add_argument("--record-traffic", metavar="CSV",

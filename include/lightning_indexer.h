@@ -272,6 +272,27 @@ IDX_API idx_status idx_sparse_mla(const uint16_t* q, const uint16_t* cache, int6
                                   size_t ws_bytes, void* stream);
 
 /*
+ * idx_sparse_mla over an FP8 cache. The TokenSpeed post on Kimi K3 (section 2,
+ * MLA, and the TL;DR's precision list) keeps the MLA cache in FP8; here a
+ * cache row is 576 E4M3 codes (OCP FP8: 1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, subnormals, one NaN code per sign, no infinities) and one
+ * fp32 scale, and stands for the row
+ *   c_s[d] = row_scale[s] * e4m3(cache8[s, d]).
+ * The result is that of idx_sparse_mla on these rows. Arguments as there, but:
+ *   cache8     uint8 [cache_rows, 576], 16-byte aligned (rows packed by
+ *              sequence as cu_k says); codes 0x7F and 0xFF (NaN) make the row's
+ *              contributions NaN
+ *   row_scale  fp32 [cache_rows], finite, 4-byte aligned
+ * The workspace is idx_sparse_mla_workspace_size(T, heads, topk) bytes.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+IDX_API idx_status idx_sparse_mla_fp8(const uint16_t* q, const uint8_t* cache8, const float* row_scale,
+                                      int64_t cache_rows, const int32_t* idx, const int32_t* cnt,
+                                      const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t T,
+                                      int32_t heads, int32_t topk, float scale, float* out, float* lse,
+                                      void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Device status word of a workspace, written by the kernels of the last call
  * that used it: IDX_OK, IDX_ERR_DEVICE_ARG or IDX_ERR_TIMEOUT. Synchronises
  * `stream` (a blocking read of 8 bytes). *detail (may be NULL) receives the

@@ -35,7 +35,7 @@ EXPORTS = ("idx_key_layernorm", "idx_score", "idx_score_workspace_size", "idx_to
            "idx_get_status", "idx_last_error", "idx_version", "idx_kernel_launches",
            "idx_score_topk_noalloc", "idx_set_wait_limit_ns", "idx_key_layernorm_append",
            "idx_indexer_project", "idx_indexer_project_workspace_size", "idx_sparse_mla",
-           "idx_sparse_mla_workspace_size", "idx_set_kernel_events")
+           "idx_sparse_mla_workspace_size", "idx_sparse_mla_fp8", "idx_set_kernel_events")
 
 
 class IndexerError(RuntimeError):
@@ -81,8 +81,10 @@ def lib():
             L.idx_sparse_mla_workspace_size.restype = sz
             L.idx_sparse_mla.argtypes = [P, P, i64, P, P, P, P, i32, i32, i32, i32, ctypes.c_float, P,
                                          P, P, sz, P]
+            L.idx_sparse_mla_fp8.argtypes = [P, P, P, i64, P, P, P, P, i32, i32, i32, i32,
+                                             ctypes.c_float, P, P, P, sz, P]
             for name in ("idx_key_layernorm", "idx_score", "idx_topk", "idx_score_topk",
-                         "idx_get_status", "idx_sparse_mla"):
+                         "idx_get_status", "idx_sparse_mla", "idx_sparse_mla_fp8"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -419,4 +421,46 @@ def sparse_mla(q, cache, idx, cnt, cu_q, cu_k, scale: float, out: torch.Tensor |
                                 _ptr(cu_q), _ptr(cu_k), B, T, H, topk, float(scale), _ptr(out),
                                 _ptr(lse), _ptr(ws), ws.numel(), _stream()),
            "idx_sparse_mla")
+    return out, lse
+
+
+def sparse_mla_fp8(q, cache8, row_scale, idx, cnt, cu_q, cu_k, scale: float,
+                   out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                   ws: torch.Tensor | None = None):
+    """Sparse MLA attention over an FP8 cache -> (out [T,H,512] fp32, lse [T,H] fp32).
+
+    cache8 uint8 (or float8_e4m3fn) [rows, 576] of E4M3 codes, row_scale fp32 [rows]:
+    row s stands for row_scale[s] * e4m3(cache8[s]). Other arguments as sparse_mla.
+    """
+    _dev(q, "q", _BF16)
+    _dev(cache8, "cache8", (torch.uint8, torch.float8_e4m3fn))
+    _dev(idx, "idx", _I32)
+    _dev(cnt, "cnt", _I32)
+    _dev(cu_q, "cu_q", _I32)
+    _dev(cu_k, "cu_k", _I32)
+    if q.dim() != 3 or q.shape[2] != MLA_DIM:
+        raise ValueError("q must be [T, heads, 576]")
+    if cache8.dim() != 2 or cache8.shape[1] != MLA_DIM:
+        raise ValueError("cache8 must be [rows, 576]")
+    _dev(row_scale, "row_scale", _F32, (int(cache8.shape[0]),))
+    T, H = int(q.shape[0]), int(q.shape[1])
+    if idx.dim() != 2 or idx.shape[0] != T:
+        raise ValueError("idx must be [T, topk]")
+    topk = int(idx.shape[1])
+    _dev(cnt, "cnt", _I32, (T,))
+    B = int(cu_q.numel()) - 1
+    if out is None:
+        out = torch.empty((T, H, MLA_VDIM), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    _dev(out, "out", _F32, (T, H, MLA_VDIM))
+    _dev(lse, "lse", _F32, (T, H))
+    need = sparse_mla_workspace_size(T, H, topk)
+    if ws is None:
+        ws = workspace(need, q.device)
+    _check(lib().idx_sparse_mla_fp8(_ptr(q), _ptr(cache8), _ptr(row_scale), int(cache8.shape[0]),
+                                    _ptr(idx), _ptr(cnt), _ptr(cu_q), _ptr(cu_k), B, T, H, topk,
+                                    float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream()),
+           "idx_sparse_mla_fp8")
     return out, lse

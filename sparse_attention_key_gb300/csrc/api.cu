@@ -353,6 +353,12 @@ size_t idx_sparse_mla_workspace_size(int32_t T, int32_t heads, int32_t topk) {
     return kWsHeader + mla_partial_bytes(T, heads, topk);
 }
 
+static idx_status sparse_mla_common(const uint16_t* q, const uint16_t* cache, const uint8_t* cache8,
+                                    const float* row_scale, int64_t cache_rows, const int32_t* idx,
+                                    const int32_t* cnt, const int32_t* cu_q, const int32_t* cu_k,
+                                    int32_t B, int32_t T, int32_t heads, int32_t topk, float scale,
+                                    float* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+
 idx_status idx_sparse_mla(const uint16_t* q, const uint16_t* cache, int64_t cache_rows,
                           const int32_t* idx, const int32_t* cnt, const int32_t* cu_q,
                           const int32_t* cu_k, int32_t B, int32_t T, int32_t heads, int32_t topk,
@@ -360,6 +366,32 @@ idx_status idx_sparse_mla(const uint16_t* q, const uint16_t* cache, int64_t cach
                           void* stream) {
     g_last_error[0] = 0;
     TraceRange trace("idx_sparse_mla");
+    if (T > 0 && cache_rows > 0 && !cache) return fail(IDX_ERR_INVALID_ARG, "cache must not be NULL");
+    if (!aligned(cache, 16)) return fail(IDX_ERR_INVALID_ARG, "cache must be 16-byte aligned");
+    return sparse_mla_common(q, cache, nullptr, nullptr, cache_rows, idx, cnt, cu_q, cu_k, B, T, heads,
+                             topk, scale, out, lse, ws, ws_bytes, stream);
+}
+
+idx_status idx_sparse_mla_fp8(const uint16_t* q, const uint8_t* cache8, const float* row_scale,
+                              int64_t cache_rows, const int32_t* idx, const int32_t* cnt,
+                              const int32_t* cu_q, const int32_t* cu_k, int32_t B, int32_t T,
+                              int32_t heads, int32_t topk, float scale, float* out, float* lse,
+                              void* ws, size_t ws_bytes, void* stream) {
+    g_last_error[0] = 0;
+    TraceRange trace("idx_sparse_mla_fp8");
+    if (T > 0 && cache_rows > 0 && (!cache8 || !row_scale))
+        return fail(IDX_ERR_INVALID_ARG, "cache8 and row_scale must not be NULL");
+    if (!aligned(cache8, 16) || !aligned(row_scale, 4))
+        return fail(IDX_ERR_INVALID_ARG, "cache8 must be 16-byte aligned, row_scale 4-byte");
+    return sparse_mla_common(q, nullptr, cache8, row_scale, cache_rows, idx, cnt, cu_q, cu_k, B, T,
+                             heads, topk, scale, out, lse, ws, ws_bytes, stream);
+}
+
+static idx_status sparse_mla_common(const uint16_t* q, const uint16_t* cache, const uint8_t* cache8,
+                                    const float* row_scale, int64_t cache_rows, const int32_t* idx,
+                                    const int32_t* cnt, const int32_t* cu_q, const int32_t* cu_k,
+                                    int32_t B, int32_t T, int32_t heads, int32_t topk, float scale,
+                                    float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
     if (B < 1) return fail(IDX_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
     if (T < 0) return fail(IDX_ERR_INVALID_ARG, "T must be >= 0 (got %d)", T);
     if (heads != 32 && heads != 64 && heads != 96)
@@ -370,9 +402,9 @@ idx_status idx_sparse_mla(const uint16_t* q, const uint16_t* cache, int64_t cach
         return fail(IDX_ERR_INVALID_ARG, "scale must be finite and > 0");
     if (cache_rows < 0) return fail(IDX_ERR_INVALID_ARG, "cache_rows must be >= 0");
     if (!cu_q || !cu_k) return fail(IDX_ERR_INVALID_ARG, "cu_q / cu_k must not be NULL");
-    if (T > 0 && (!q || !idx || !cnt || !out || !lse || (cache_rows > 0 && !cache)))
-        return fail(IDX_ERR_INVALID_ARG, "q, cache, idx, cnt, out and lse must not be NULL");
-    if (!aligned(q, 16) || !aligned(cache, 16) || !aligned(idx, 4) || !aligned(cnt, 4) ||
+    if (T > 0 && (!q || !idx || !cnt || !out || !lse))
+        return fail(IDX_ERR_INVALID_ARG, "q, idx, cnt, out and lse must not be NULL");
+    if (!aligned(q, 16) || !aligned(idx, 4) || !aligned(cnt, 4) ||
         !aligned(out, 16) || !aligned(lse, 4) || !aligned(cu_q, 4) || !aligned(cu_k, 4))
         return fail(IDX_ERR_INVALID_ARG,
                     "q, cache and out must be 16-byte aligned; int32 and lse arrays 4-byte");
@@ -385,6 +417,8 @@ idx_status idx_sparse_mla(const uint16_t* q, const uint16_t* cache, int64_t cach
     if (T == 0) return IDX_OK;
     MlaArgs a{q, cache, cache_rows, idx, cnt, cu_q, cu_k, B, T, heads, topk, scale, out, lse,
               (DeviceStatus*)ws};
+    a.cache8 = cache8;
+    a.row_scale = row_scale;
     cudaError_t e = launch_sparse_mla(a, (char*)ws + kWsHeader, s);
     return e == cudaSuccess ? IDX_OK : cuda_fail(e, "sparse_mla launch");
 }

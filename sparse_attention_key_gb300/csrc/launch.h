@@ -170,6 +170,10 @@ struct MlaArgs {
     float* out;              // fp32 [T, heads, 512]
     float* lse;              // fp32 [T, heads]
     DeviceStatus* status;
+    // FP8 cache (instead of `cache`): E4M3 codes [cache_rows, 576] and one
+    // fp32 scale per row; NULL for the bf16 cache.
+    const uint8_t* cache8 = nullptr;
+    const float* row_scale = nullptr;
 };
 
 // Key splits per query row (1: the kernel writes out/lse itself).

@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -58,25 +59,33 @@ constexpr int kGather = 128;                    // warps 1-4
 constexpr int kSoft = 128;                      // warps 5-8
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftBar = 1;                     // named barrier of the softmax warps
+constexpr int kGatherBar = 2;                   // named barrier of the gather warps (FP8)
 constexpr uint64_t kMlaDrainNs = 100000000ull;  // 100 ms to drain after an abort
 
-template <int H>
+constexpr int kRow8 = kMlaDim;                  // an FP8 cache row: 576 bytes
+constexpr int kStage8 = kTileRows * kRow8;      // FP8 staging of a tile (row-major)
+
+template <int H, bool kFp8 = false>
 struct MlaLayout {
+    // swizzled bf16 tile stages (FP8: two, the staging takes the third's room)
+    static constexpr int kNStages = kFp8 ? 2 : kStages;
     static constexpr int kQChunk = H * 128;     // a 64-dim chunk of Q (H rows)
     static constexpr int kQBytes = kChunks * kQChunk;
     static constexpr int kC = kQBytes;          // 1024-byte aligned since H % 8 == 0
-    static constexpr int kP = kC + kStages * kStageBytes;   // 1024-byte aligned
+    static constexpr int kS8 = kC + kNStages * kStageBytes;   // FP8 staging [2][32 rows][576 B]
+    static constexpr int kP = kS8 + (kFp8 ? 2 * kStage8 : 0);   // 1024-byte aligned
     static constexpr int kPBytes = H * 64;      // P: a 64-byte row (32 bf16) per head, 64-byte swizzle
     static constexpr int kF = kP + kPBytes;     // per-head rescale factors [2][128]
     static constexpr int kM = kF + 1024;        // per-head m [128]
     static constexpr int kL = kM + 512;         // per-head l [128]
     static constexpr int kBar = kL + 512;
-    static constexpr int kBytes = kBar + 16 * 8 + 16;   // 15 barriers, TMEM slot, flags
+    static constexpr int kBytes = kBar + 24 * 8 + 16;   // barriers, TMEM slot, flags, masks
     static constexpr uint32_t kOCols = 4 * H;   // O^T: 4 tiles of 128 dims, H columns each
     static constexpr uint32_t kSCol = kOCols;   // S: two buffers of 32 columns
     static_assert(H % 32 == 0 && H >= 32 && H <= 96, "heads: 32, 64 or 96");
     static_assert(kOCols + 2 * kTileRows <= kTmemCols, "TMEM columns");
     static_assert(kBytes <= 227 * 1024, "shared memory");
+    static_assert(kP % 1024 == 0 && kS8 % 16 == 0, "alignment");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -96,6 +105,24 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // async proxy that tcgen05.mma reads operands through.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One untiled bulk copy global -> shared (TMA engine), completion counted in
+// bytes on `bar`; addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(ptx::smem_addr(bar))
+                 : "memory");
+}
+
+// Two E4M3 codes (low byte first) -> two bf16 values (low half first), exactly:
+// every E4M3 value is an fp16 and a bf16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_codes));
+    const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+    const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+    return f32x2_to_bf16x2_rn(lo, hi);
 }
 
 // 2^x by the hardware approximation (ex2.approx: relative error near 2^-22,
@@ -163,16 +190,25 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <int H>
+// kFp8: the cache rows are 576 E4M3 codes (cache8) with one fp32 scale each
+// (row_scale); the row is c = row_scale x e4m3(code). Each selected row is
+// fetched by one 576-byte bulk copy (TMA engine) into a row-major staging
+// tile; the gather warps convert the codes to bf16 (exact) into the swizzled
+// tile the MMAs read, and the softmax applies the row scale in fp32: to the
+// logits (scale x row_scale x q.e) and to P before its bf16 rounding
+// (O accumulates p x row_scale x e; l sums p).
+template <int H, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __restrict__ cache,
+                  const uint8_t* __restrict__ cache8, const float* __restrict__ row_scale,
                   int64_t cache_rows, const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt,
                   const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B, int topk,
                   float scale_log2, int tiles_per_split, int n_split, float* __restrict__ out,
                   float* __restrict__ lse, float* __restrict__ part_o, float* __restrict__ part_ml,
                   DeviceStatus* status, uint64_t wait_ns) {
     using namespace ptx;
-    using Lay = MlaLayout<H>;
+    using Lay = MlaLayout<H, kFp8>;
+    constexpr int NST = Lay::kNStages;
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_addr(smem) & 1023u) != 0) {   // the swizzled tiles need 1024-byte alignment
         pdl_wait();
@@ -195,17 +231,21 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
     uint64_t* end_bar = bars + 11;  // every MMA1 issued has completed
     uint64_t* s_free = bars + 12;   // [2]: the softmax has read S (kSoft arrivals)
     uint64_t* end_bar2 = bars + 14; // every MMA2 issued has completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+    uint64_t* g_full = bars + 15;   // [2] (FP8): a tile's bulk copies landed in staging
+    uint32_t* vmask8 = reinterpret_cast<uint32_t*>(bars + 17);   // [2] (FP8): staged rows present
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* seq_of_row = reinterpret_cast<int*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(c_full + s, kGather);
             mbar_init(c_empty + s, 1);
         }
+        mbar_init(g_full, 1);
+        mbar_init(g_full + 1, 1);
         mbar_init(s_full, 1);
         mbar_init(s_full + 1, 1);
         mbar_init(p_full, kSoft);
@@ -273,9 +313,9 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
             bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
             if (!ok) give_up(20);
             for (int i = 0; i < nt && ok; ++i) {
-                const int st = i % kStages, s = i & 1;
+                const int st = i % NST, s = i & 1;
                 // tile i landed, and S buffer s read by the softmax of tile i-2
-                if (!mbar_wait(c_full + st, (i / kStages) & 1, abort_flag, wait_ns) ||
+                if (!mbar_wait(c_full + st, (i / NST) & 1, abort_flag, wait_ns) ||
                     (i >= 2 && !mbar_wait(s_free + s, ((i >> 1) - 1) & 1, abort_flag, wait_ns))) {
                     give_up(21);
                     break;
@@ -309,7 +349,7 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t cbase = ca + (i % kStages) * kStageBytes;
+                const uint32_t cbase = ca + (i % NST) * kStageBytes;
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
 #pragma unroll
@@ -320,12 +360,78 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
                         const uint64_t bd = smem_desc_sw64(pa + k * 32);
                         tc_mma_bf16(tmem_base + m * H, a, bd, kI2, (i > 0 || k > 0) ? 1u : 0u);
                     }
-                tc_commit(c_empty + (i % kStages));
+                tc_commit(c_empty + (i % NST));
                 tc_commit(o_done);
             }
             tc_commit(end_bar2);
             mbar_wait(end_bar2, 0, nullptr, kMlaDrainNs);
         }
+    } else if (warp <= 4 && kFp8) {
+        // ------------------------------------------------- gather (FP8 rows)
+        // Tile i: warp 1 (a lane per row) issues the rows' bulk copies into
+        // staging buffer i & 1; then all four warps convert tile i-1 from its
+        // staging buffer into swizzled stage (i-1) % NST. A barrier of the four
+        // warps after each conversion frees its staging buffer for tile i+1.
+        const int g = threadIdx.x - 32;   // 0 .. 127
+        if (g == 0 && nt > 0) {
+            mbar_arrive_expect_tx(q_full, Lay::kQBytes);
+#pragma unroll 1
+            for (int c = 0; c < kChunks; ++c)
+                tma_load_2d(smem_addr(q_s + c * Lay::kQChunk), &tmap_q, q_full, c * 64, t * H);
+        }
+        uint8_t* st8 = smem + Lay::kS8;
+        int issued = 0, waited = 0;   // tiles whose copies were issued / seen landed
+        for (int i = 0; i <= nt; ++i) {
+            if (i < nt && warp == 1) {
+                const int f = i & 1;
+                const int32_t j = (tile0 + i) * kTileRows + lane;
+                const int32_t pos = position(j);
+                if (j < n_sel && pos < 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
+                const uint32_t vm = __ballot_sync(0xffffffffu, pos >= 0);
+                if (lane == 0) {
+                    vmask8[f] = vm;
+                    mbar_arrive_expect_tx(g_full + f, (uint32_t)__popc(vm) * kRow8);
+                }
+                __syncwarp();
+                if (pos >= 0)
+                    bulk_copy_g2s(smem_addr(st8 + f * kStage8 + lane * kRow8), cache8 + (k0 + pos) * kRow8,
+                                  kRow8, g_full + f);
+            }
+            if (i < nt) issued = i + 1;
+            if (i == 0) continue;
+            const int k = i - 1, f = k & 1, st = k % NST;
+            bool ok = mbar_wait(g_full + f, (k >> 1) & 1, abort_flag, wait_ns);
+            if (ok) waited = k + 1;
+            if (ok && k >= NST) ok = mbar_wait(c_empty + st, (k / NST - 1) & 1, abort_flag, wait_ns);
+            // every thread of the group agrees on the outcome before the barriers below
+            if (bar_red_or(kGatherBar, kGather, !ok)) {
+                give_up(27);
+                break;
+            }
+            const uint32_t vm = vmask8[f];
+            const uint8_t* src = st8 + f * kStage8;
+            uint8_t* dst = c_s + st * kStageBytes;
+            // 32 rows x 72 pieces (8 codes -> 16 bytes of bf16); thread g takes
+            // pieces g, g + 128, ...
+#pragma unroll 2
+            for (int pc = g; pc < kTileRows * 72; pc += kGather) {
+                const int r = pc / 72, w = pc - r * 72, c = w >> 3, q8 = w & 7;
+                uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                if ((vm >> r) & 1u) {
+                    const uint2 in = *reinterpret_cast<const uint2*>(src + r * kRow8 + w * 8);
+                    o = make_uint4(e4m3x2_to_bf16x2(in.x & 0xFFFFu), e4m3x2_to_bf16x2(in.x >> 16),
+                                   e4m3x2_to_bf16x2(in.y & 0xFFFFu), e4m3x2_to_bf16x2(in.y >> 16));
+                }
+                *reinterpret_cast<uint4*>(dst + c * kChunkBytes + r * 128 + ((q8 ^ (r & 7)) << 4)) = o;
+            }
+            fence_proxy_async_smem();   // the MMAs read the tile through the async proxy
+            mbar_arrive(c_full + st);
+            named_bar_sync(kGatherBar, kGather);   // staging buffer f is free again
+        }
+        // copies issued but not seen landing (after an abort) land before exit
+        if (warp == 1 && lane == 0)
+            for (int k = waited; k < issued; ++k) mbar_wait(g_full + (k & 1), (k >> 1) & 1, nullptr, kMlaDrainNs);
+        if (g == 0 && nt > 0) mbar_wait(q_full, 0, nullptr, kMlaDrainNs);   // Q landed before exit
     } else if (warp <= 4) {
         // ------------------------------------------------------------ gather
         const int g = threadIdx.x - 32;   // 0 .. 127
@@ -345,11 +451,11 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
         int32_t pn0 = nt > 0 ? position(tile0 * kTileRows + r8) : -1;
         int32_t pn1 = nt > 0 ? position(tile0 * kTileRows + r8 + 16) : -1;
         for (int i = 0; i < nt; ++i) {
-            const int s = i % kStages;
+            const int s = i % NST;
             const int32_t p0 = pn0, p1 = pn1;
             pn0 = i + 1 < nt ? position((tile0 + i + 1) * kTileRows + r8) : -1;
             pn1 = i + 1 < nt ? position((tile0 + i + 1) * kTileRows + r8 + 16) : -1;
-            if (i >= kStages && !mbar_wait(c_empty + s, (i / kStages - 1) & 1, abort_flag, wait_ns)) {
+            if (i >= NST && !mbar_wait(c_empty + s, (i / NST - 1) & 1, abort_flag, wait_ns)) {
                 give_up(23);
                 break;
             }
@@ -380,9 +486,25 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         float m_used = -INFINITY, l = 0.f;
         int done = 0;
+        // FP8: the row scale of row `lane` of the current tile, loaded a tile
+        // ahead (its position two tiles ahead)
+        auto scale_of = [&](int32_t pos) -> float { return pos >= 0 ? __ldg(row_scale + k0 + pos) : 0.f; };
+        int32_t pos_cur = 0, pos_next = 0;
+        float sc_cur = 0.f;
+        if (kFp8 && nt > 0) {
+            pos_cur = position(tile0 * kTileRows + lane);
+            sc_cur = scale_of(pos_cur);
+            pos_next = position((tile0 + 1) * kTileRows + lane);
+        }
         for (int i = 0; i < nt; ++i) {
             const int s = i & 1;
-            const bool vc = position((tile0 + i) * kTileRows + lane) >= 0;
+            float sc_next = 0.f;
+            int32_t pos_after = -1;
+            if (kFp8) {
+                sc_next = i + 1 < nt ? scale_of(pos_next) : 0.f;
+                pos_after = i + 2 < nt ? position((tile0 + i + 2) * kTileRows + lane) : -1;
+            }
+            const bool vc = kFp8 ? pos_cur >= 0 : position((tile0 + i) * kTileRows + lane) >= 0;
             const uint32_t vmask = __ballot_sync(0xffffffffu, vc);
             // every wait's outcome is agreed by the whole group (bar.red.or),
             // so the group's barriers always see all of its threads
@@ -397,10 +519,17 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
             tmem_ld_wait(v);
             tc_fence_before_sync();
             mbar_arrive(s_free + s);   // MMA1 of tile i+2 may overwrite this buffer
+            // logits in the log2 domain (FP8: times the row's scale)
+            float sc[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                sc[c] = kFp8 ? __shfl_sync(0xffffffffu, sc_cur, c) : 1.f;
+                v[c] = __float_as_uint(__uint_as_float(v[c]) * scale_log2 * sc[c]);
+            }
             float tmax = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-                if ((vmask >> c) & 1u) tmax = fmaxf(tmax, __uint_as_float(v[c]) * scale_log2);
+                if ((vmask >> c) & 1u) tmax = fmaxf(tmax, __uint_as_float(v[c]));
             // new reference maximum: the first finite one, or one that grew past 2^8
             bool need = false;
             float f = 1.f;
@@ -415,11 +544,17 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 p[c] = ((vmask >> c) & 1u) && m_used > -INFINITY
-                           ? ex2_fast(__uint_as_float(v[c]) * scale_log2 - m_used)
+                           ? ex2_fast(__uint_as_float(v[c]) - m_used)
                            : 0.f;
                 psum += p[c];
+                if (kFp8) p[c] *= sc[c];   // O gathers p x row scale x code; l sums p
             }
             l += psum;
+            if (kFp8) {
+                pos_cur = pos_next;
+                sc_cur = sc_next;
+                pos_next = pos_after;
+            }
             // factors of tile i in buffer i & 1: the barrier of tile i+1 lies
             // between this tile's reads and the next writes of the same buffer
             float* fac_i = fac + 128 * (i & 1);
@@ -596,17 +731,18 @@ EncodeTiledFn mla_encode_fn() {
     return fn;
 }
 
-template <int H>
+template <int H, bool kFp8>
 cudaError_t launch_h(const MlaArgs& a, const CUtensorMap& map, int tps, int n_split, float* part_o,
                      float* part_ml, cudaStream_t stream) {
-    using Lay = MlaLayout<H>;
-    auto kern = sparse_mla_kernel<H>;
+    using Lay = MlaLayout<H, kFp8>;
+    auto kern = sparse_mla_kernel<H, kFp8>;
     cudaError_t e = ensure_smem_optin((const void*)kern, Lay::kBytes);
     if (e != cudaSuccess) return e;
     const float scale_log2 = a.scale * 1.4426950408889634f;
     e = launch_kernel(kern, dim3((unsigned)((int64_t)a.T * n_split)), dim3(kThreads), (size_t)Lay::kBytes,
-                      stream, 1, map, a.cache, a.cache_rows, a.idx, a.cnt, a.cu_q, a.cu_k, a.B, a.topk,
-                      scale_log2, tps, n_split, a.out, a.lse, part_o, part_ml, a.status, wait_limit_ns());
+                      stream, 1, map, a.cache, a.cache8, a.row_scale, a.cache_rows, a.idx, a.cnt, a.cu_q,
+                      a.cu_k, a.B, a.topk, scale_log2, tps, n_split, a.out, a.lse, part_o, part_ml, a.status,
+                      wait_limit_ns());
     if (e != cudaSuccess || n_split == 1) return e;
     return launch_kernel(sparse_mla_merge_kernel, dim3((unsigned)((int64_t)a.T * H)), dim3(128), 0, stream, 1,
                          (const float*)part_o, (const float*)part_ml, n_split, H, a.out, a.lse);
@@ -664,10 +800,14 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, void* partials, cudaStream_t str
         part_ml = reinterpret_cast<float*>(static_cast<char*>(partials) +
                                            align_up((size_t)a.T * n_split * a.heads * kMlaV * 4, 256));
     }
+    const bool fp8 = a.cache8 != nullptr;
     switch (a.heads) {
-        case 32: return launch_h<32>(a, map, tps, n_split, part_o, part_ml, stream);
-        case 64: return launch_h<64>(a, map, tps, n_split, part_o, part_ml, stream);
-        case 96: return launch_h<96>(a, map, tps, n_split, part_o, part_ml, stream);
+        case 32: return fp8 ? launch_h<32, true>(a, map, tps, n_split, part_o, part_ml, stream)
+                            : launch_h<32, false>(a, map, tps, n_split, part_o, part_ml, stream);
+        case 64: return fp8 ? launch_h<64, true>(a, map, tps, n_split, part_o, part_ml, stream)
+                            : launch_h<64, false>(a, map, tps, n_split, part_o, part_ml, stream);
+        case 96: return fp8 ? launch_h<96, true>(a, map, tps, n_split, part_o, part_ml, stream)
+                            : launch_h<96, false>(a, map, tps, n_split, part_o, part_ml, stream);
         default: return cudaErrorInvalidValue;
     }
 }

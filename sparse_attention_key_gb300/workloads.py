@@ -310,11 +310,42 @@ def mla_case(seed: int, k_lens, q_per_seq: int = 1, heads: int = MLA_HEADS, topk
     """
     rng = np.random.default_rng(seed)
     k_lens = np.asarray(k_lens, dtype=np.int64)
+    cache = _normal_bf16(rng, (int(k_lens.sum()), MLA_DIM))
+    return _mla_queries(rng, cache, k_lens, q_per_seq, heads, topk, n_sel, qscale)
+
+
+def fp8_codes(rng, shape) -> np.ndarray:
+    """E4M3 code bytes with a bell-shaped spread of magnitudes: random sign,
+    exponent field 7 + round(N(0, 1.5)) clipped to 0..15 (so mostly values of
+    2^-2 .. 2^3, with some subnormals and some near the top of the range),
+    uniform mantissa; the two NaN codes are never drawn (mantissa 7 of the top
+    exponent becomes 6)."""
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8)
+    expo = np.clip(np.rint(7 + 1.5 * rng.standard_normal(shape)), 0, 15).astype(np.uint8)
+    mant = rng.integers(0, 8, size=shape, dtype=np.uint8)
+    mant = np.where((expo == 15) & (mant == 7), np.uint8(6), mant)
+    return ((sign << 7) | (expo << 3) | mant).astype(np.uint8)
+
+
+def mla_fp8_case(seed: int, k_lens, q_per_seq: int = 1, heads: int = MLA_HEADS, topk: int = 2048,
+                 n_sel=None, qscale: float = 1.0):
+    """mla_case over an FP8 cache: rows of 576 E4M3 codes (fp8_codes) with
+    one fp32 scale each, 2^U(-3, 0). Returns (q bits, cache8 [L,576] uint8,
+    row_scale [L] fp32, idx, cnt, cu_q, cu_k)."""
+    rng = np.random.default_rng(seed)
+    k_lens = np.asarray(k_lens, dtype=np.int64)
+    L = int(k_lens.sum())
+    cache8 = fp8_codes(rng, (L, MLA_DIM))
+    row_scale = np.exp2(rng.uniform(-3.0, 0.0, size=L)).astype(np.float32)
+    q, _, idx, cnt, cu_q, cu_k = _mla_queries(rng, cache8, k_lens, q_per_seq, heads, topk, n_sel, qscale)
+    return q, cache8, row_scale, idx, cnt, cu_q, cu_k
+
+
+def _mla_queries(rng, cache, k_lens, q_per_seq, heads, topk, n_sel, qscale):
     B = k_lens.size
     cu_k = np.concatenate([[0], np.cumsum(k_lens)]).astype(np.int32)
     cu_q = (np.arange(B + 1) * q_per_seq).astype(np.int32)
     T = B * q_per_seq
-    cache = _normal_bf16(rng, (int(cu_k[-1]), MLA_DIM))
     q = f32_to_bf16_bits((qscale * rng.standard_normal((T, heads, MLA_DIM))).astype(np.float32))
     idx = np.full((T, topk), -1, dtype=np.int32)
     cnt = np.zeros(T, dtype=np.int32)
