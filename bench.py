@@ -751,14 +751,17 @@ def run_mla(args):
     H, K = 96, 2048
     T, L = len(lens), int(sum(lens))
     gen = torch.Generator(device=dev).manual_seed(17)
-    if args.fp8:   # E4M3 codes (random bytes, NaN codes moved to 0) and fp32 row scales
+    if args.fp8:   # E4M3 codes spread like workloads.fp8_codes, fp32 row scales 2^U(-3,0)
         cache = torch.empty((L, 576), dtype=torch.uint8, device=dev)
         for r0 in range(0, L, 1 << 18):
             r1 = min(L, r0 + (1 << 18))
-            blk = torch.randint(0, 256, (r1 - r0, 576), generator=gen, device=dev, dtype=torch.int32)
-            blk = torch.where((blk & 0x7F) == 0x7F, torch.zeros_like(blk), blk)
-            cache[r0:r1] = blk.to(torch.uint8)
-        row_scale = torch.exp2(torch.rand((L,), generator=gen, device=dev) * -8.0).float()
+            shape = (r1 - r0, 576)
+            sign = torch.randint(0, 2, shape, generator=gen, device=dev, dtype=torch.int32)
+            expo = (7 + 1.5 * torch.randn(shape, generator=gen, device=dev)).round().clamp(0, 15).int()
+            mant = torch.randint(0, 8, shape, generator=gen, device=dev, dtype=torch.int32)
+            mant = torch.where((expo == 15) & (mant == 7), torch.full_like(mant, 6), mant)
+            cache[r0:r1] = ((sign << 7) | (expo << 3) | mant).to(torch.uint8)
+        row_scale = torch.exp2(torch.rand((L,), generator=gen, device=dev) * -3.0).float()
     else:
         cache = torch.empty((L, 576), dtype=torch.bfloat16, device=dev)
         for r0 in range(0, L, 1 << 20):   # N(0,1) rows, in chunks

@@ -27,8 +27,10 @@
 //   warps 5-8  softmax: a TMEM lane is a head, so each thread owns one row of S:
 //              running maximum in the log2 domain, P = 2^(S - m), sum l.
 //              O is rescaled (in TMEM) only when a head's maximum grows by more
-//              than 2^8, so the scale of O and l may lag the true maximum; both
-//              carry the same factor, and the result is unchanged.
+//              than 2^kRescaleLog2 (2^20), so the scale of O and l may lag the
+//              true maximum; both carry the same factor, and the result is
+//              unchanged. Weights stay below 2^20, so O stays finite for cache
+//              values below about 1e29 (fp32 sums of 2048 weighted rows).
 // With one CTA per query row the kernel writes out/lse; with several it writes
 // (O, m, l) partials that sparse_mla_merge_kernel combines.
 // Every wait is bounded; a timeout or an out-of-range position is recorded in
@@ -59,33 +61,36 @@ constexpr int kGather = 128;                    // warps 1-4
 constexpr int kSoft = 128;                      // warps 5-8
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftBar = 1;                     // named barrier of the softmax warps
-constexpr int kGatherBar = 2;                   // named barrier of the gather warps (FP8)
 constexpr uint64_t kMlaDrainNs = 100000000ull;  // 100 ms to drain after an abort
+// A head's reference maximum (log2 domain) moves, and O and l are rescaled,
+// only when the tile maximum exceeds it by more than this. Measured: a
+// threshold of 8 rescaled on most tiles of rows whose logits spread widely,
+// at up to a few microseconds per rescale.
+constexpr float kRescaleLog2 = 20.f;
 
 constexpr int kRow8 = kMlaDim;                  // an FP8 cache row: 576 bytes
-constexpr int kStage8 = kTileRows * kRow8;      // FP8 staging of a tile (row-major)
 
 template <int H, bool kFp8 = false>
 struct MlaLayout {
-    // swizzled bf16 tile stages (FP8: two, the staging takes the third's room)
-    static constexpr int kNStages = kFp8 ? 2 : kStages;
+    // swizzled bf16 tile stages (the FP8 path converts into the same stages)
+    static constexpr int kNStages = kStages;
     static constexpr int kQChunk = H * 128;     // a 64-dim chunk of Q (H rows)
     static constexpr int kQBytes = kChunks * kQChunk;
     static constexpr int kC = kQBytes;          // 1024-byte aligned since H % 8 == 0
-    static constexpr int kS8 = kC + kNStages * kStageBytes;   // FP8 staging [2][32 rows][576 B]
-    static constexpr int kP = kS8 + (kFp8 ? 2 * kStage8 : 0);   // 1024-byte aligned
+    static constexpr int kP = kC + kNStages * kStageBytes;   // 1024-byte aligned
     static constexpr int kPBytes = H * 64;      // P: a 64-byte row (32 bf16) per head, 64-byte swizzle
     static constexpr int kF = kP + kPBytes;     // per-head rescale factors [2][128]
     static constexpr int kM = kF + 1024;        // per-head m [128]
     static constexpr int kL = kM + 512;         // per-head l [128]
-    static constexpr int kBar = kL + 512;
+    static constexpr int kSc = kL + 512;        // FP8: row scales of each stage's tile [kNStages][32]
+    static constexpr int kBar = kSc + kNStages * kTileRows * 4;
     static constexpr int kBytes = kBar + 24 * 8 + 16;   // barriers, TMEM slot, flags, masks
     static constexpr uint32_t kOCols = 4 * H;   // O^T: 4 tiles of 128 dims, H columns each
     static constexpr uint32_t kSCol = kOCols;   // S: two buffers of 32 columns
     static_assert(H % 32 == 0 && H >= 32 && H <= 96, "heads: 32, 64 or 96");
     static_assert(kOCols + 2 * kTileRows <= kTmemCols, "TMEM columns");
     static_assert(kBytes <= 227 * 1024, "shared memory");
-    static_assert(kP % 1024 == 0 && kS8 % 16 == 0, "alignment");
+    static_assert(kP % 1024 == 0, "alignment");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -107,12 +112,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// One untiled bulk copy global -> shared (TMA engine), completion counted in
-// bytes on `bar`; addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(ptx::smem_addr(bar))
-                 : "memory");
+// 16 bytes from global memory, read-only, not kept in L1 (rows are read once).
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 // Two E4M3 codes (low byte first) -> two bf16 values (low half first), exactly:
@@ -191,10 +197,9 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // kFp8: the cache rows are 576 E4M3 codes (cache8) with one fp32 scale each
-// (row_scale); the row is c = row_scale x e4m3(code). Each selected row is
-// fetched by one 576-byte bulk copy (TMA engine) into a row-major staging
-// tile; the gather warps convert the codes to bf16 (exact) into the swizzled
-// tile the MMAs read, and the softmax applies the row scale in fp32: to the
+// (row_scale); the row is c = row_scale x e4m3(code). The gather warps load
+// the selected rows' codes into registers and convert them to bf16 (exact)
+// into the swizzled tile the MMAs read, and the softmax applies the row scale in fp32: to the
 // logits (scale x row_scale x q.e) and to P before its bf16 rounding
 // (O accumulates p x row_scale x e; l sums p).
 template <int H, bool kFp8>
@@ -221,6 +226,7 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
     float* fac = reinterpret_cast<float*>(smem + Lay::kF);
     float* m_s = reinterpret_cast<float*>(smem + Lay::kM);
     float* l_s = reinterpret_cast<float*>(smem + Lay::kL);
+    float* sc_s = reinterpret_cast<float*>(smem + Lay::kSc);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
     uint64_t* q_full = bars;
     uint64_t* c_full = bars + 1;    // [kStages]: a tile gathered (kGather arrivals)
@@ -231,8 +237,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
     uint64_t* end_bar = bars + 11;  // every MMA1 issued has completed
     uint64_t* s_free = bars + 12;   // [2]: the softmax has read S (kSoft arrivals)
     uint64_t* end_bar2 = bars + 14; // every MMA2 issued has completed
-    uint64_t* g_full = bars + 15;   // [2] (FP8): a tile's bulk copies landed in staging
-    uint32_t* vmask8 = reinterpret_cast<uint32_t*>(bars + 17);   // [2] (FP8): staged rows present
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* seq_of_row = reinterpret_cast<int*>(tmem_slot + 2);
@@ -244,8 +248,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
             mbar_init(c_full + s, kGather);
             mbar_init(c_empty + s, 1);
         }
-        mbar_init(g_full, 1);
-        mbar_init(g_full + 1, 1);
         mbar_init(s_full, 1);
         mbar_init(s_full + 1, 1);
         mbar_init(p_full, kSoft);
@@ -368,10 +370,12 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
         }
     } else if (warp <= 4 && kFp8) {
         // ------------------------------------------------- gather (FP8 rows)
-        // Tile i: warp 1 (a lane per row) issues the rows' bulk copies into
-        // staging buffer i & 1; then all four warps convert tile i-1 from its
-        // staging buffer into swizzled stage (i-1) % NST. A barrier of the four
-        // warps after each conversion frees its staging buffer for tile i+1.
+        // Each thread owns 9 of a tile's 32 x 36 16-byte pieces of codes. It
+        // loads them into registers two tiles ahead (tile i+1 in flight while
+        // tile i is converted), converts 16 codes into two 16-byte bf16 pieces
+        // (exact) and stores them at their swizzled places in stage i % NST;
+        // rows left out load nothing and convert to zeros. No shared-memory
+        // staging: the three bf16 stages of the bf16 path fit beside Q.
         const int g = threadIdx.x - 32;   // 0 .. 127
         if (g == 0 && nt > 0) {
             mbar_arrive_expect_tx(q_full, Lay::kQBytes);
@@ -379,58 +383,71 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
             for (int c = 0; c < kChunks; ++c)
                 tma_load_2d(smem_addr(q_s + c * Lay::kQChunk), &tmap_q, q_full, c * 64, t * H);
         }
-        uint8_t* st8 = smem + Lay::kS8;
-        int issued = 0, waited = 0;   // tiles whose copies were issued / seen landed
-        for (int i = 0; i <= nt; ++i) {
-            if (i < nt && warp == 1) {
-                const int f = i & 1;
-                const int32_t j = (tile0 + i) * kTileRows + lane;
-                const int32_t pos = position(j);
-                if (j < n_sel && pos < 0) report_error(status, IDX_ERR_DEVICE_ARG, t);
-                const uint32_t vm = __ballot_sync(0xffffffffu, pos >= 0);
-                if (lane == 0) {
-                    vmask8[f] = vm;
-                    mbar_arrive_expect_tx(g_full + f, (uint32_t)__popc(vm) * kRow8);
-                }
-                __syncwarp();
-                if (pos >= 0)
-                    bulk_copy_g2s(smem_addr(st8 + f * kStage8 + lane * kRow8), cache8 + (k0 + pos) * kRow8,
-                                  kRow8, g_full + f);
+        constexpr int kPcs = kRow8 / 16;                        // 36 pieces per row
+        constexpr int kPer = kTileRows * kPcs / kGather;        // 9 pieces per thread
+        static_assert(kTileRows * kPcs % kGather == 0, "pieces per thread");
+        // positions of this thread's rows, fetched two tiles ahead: pe for the
+        // even tiles, po for the odd ones
+        int32_t pe[kPer], po[kPer];
+        auto fetch_positions = [&](int i, int32_t (&P)[kPer]) {
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                P[j] = i < nt ? position((tile0 + i) * kTileRows + (g + kGather * j) / kPcs) : -1;
+        };
+        // issue the loads of tile i (positions in P; the thread holding a row's
+        // first piece also loads that row's scale), then fetch the positions
+        // of tile i+2 into P
+        auto load_tile = [&](int i, int32_t (&P)[kPer], uint4 (&R)[kPer], float (&S)[kPer]) {
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int pc = g + kGather * j, r = pc / kPcs, w = pc - r * kPcs;
+                if (w == 0 && i < nt && (tile0 + i) * kTileRows + r < n_sel && P[j] < 0)
+                    report_error(status, IDX_ERR_DEVICE_ARG, t);
+                R[j] = P[j] >= 0 ? ld_nc_v4(cache8 + (k0 + P[j]) * kRow8 + w * 16) : make_uint4(0u, 0u, 0u, 0u);
+                S[j] = w == 0 && P[j] >= 0 ? __ldg(row_scale + k0 + P[j]) : 0.f;
             }
-            if (i < nt) issued = i + 1;
-            if (i == 0) continue;
-            const int k = i - 1, f = k & 1, st = k % NST;
-            bool ok = mbar_wait(g_full + f, (k >> 1) & 1, abort_flag, wait_ns);
-            if (ok) waited = k + 1;
-            if (ok && k >= NST) ok = mbar_wait(c_empty + st, (k / NST - 1) & 1, abort_flag, wait_ns);
-            // every thread of the group agrees on the outcome before the barriers below
-            if (bar_red_or(kGatherBar, kGather, !ok)) {
-                give_up(27);
-                break;
-            }
-            const uint32_t vm = vmask8[f];
-            const uint8_t* src = st8 + f * kStage8;
+            fetch_positions(i + 2, P);
+        };
+        // tile i from R into stage i % NST (false: a wait gave up)
+        auto store_tile = [&](int i, const uint4 (&R)[kPer], const float (&S)[kPer]) -> bool {
+            const int st = i % NST;
+            if (i >= NST && !mbar_wait(c_empty + st, (i / NST - 1) & 1, abort_flag, wait_ns)) return false;
             uint8_t* dst = c_s + st * kStageBytes;
-            // 32 rows x 72 pieces (8 codes -> 16 bytes of bf16); thread g takes
-            // pieces g, g + 128, ...
-#pragma unroll 2
-            for (int pc = g; pc < kTileRows * 72; pc += kGather) {
-                const int r = pc / 72, w = pc - r * 72, c = w >> 3, q8 = w & 7;
-                uint4 o = make_uint4(0u, 0u, 0u, 0u);
-                if ((vm >> r) & 1u) {
-                    const uint2 in = *reinterpret_cast<const uint2*>(src + r * kRow8 + w * 8);
-                    o = make_uint4(e4m3x2_to_bf16x2(in.x & 0xFFFFu), e4m3x2_to_bf16x2(in.x >> 16),
-                                   e4m3x2_to_bf16x2(in.y & 0xFFFFu), e4m3x2_to_bf16x2(in.y >> 16));
-                }
-                *reinterpret_cast<uint4*>(dst + c * kChunkBytes + r * 128 + ((q8 ^ (r & 7)) << 4)) = o;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int pc = g + kGather * j, r = pc / kPcs, w = pc - r * kPcs;
+                if (w == 0) sc_s[st * kTileRows + r] = S[j];
+                const int c = w >> 2, q0 = (w & 3) * 2;   // chunk; first 16-byte piece in its 128-byte row
+                const uint4 lo = make_uint4(e4m3x2_to_bf16x2(R[j].x & 0xFFFFu), e4m3x2_to_bf16x2(R[j].x >> 16),
+                                            e4m3x2_to_bf16x2(R[j].y & 0xFFFFu), e4m3x2_to_bf16x2(R[j].y >> 16));
+                const uint4 hi = make_uint4(e4m3x2_to_bf16x2(R[j].z & 0xFFFFu), e4m3x2_to_bf16x2(R[j].z >> 16),
+                                            e4m3x2_to_bf16x2(R[j].w & 0xFFFFu), e4m3x2_to_bf16x2(R[j].w >> 16));
+                uint8_t* row = dst + c * kChunkBytes + r * 128;
+                *reinterpret_cast<uint4*>(row + ((q0 ^ (r & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(row + (((q0 + 1) ^ (r & 7)) << 4)) = hi;
             }
             fence_proxy_async_smem();   // the MMAs read the tile through the async proxy
             mbar_arrive(c_full + st);
-            named_bar_sync(kGatherBar, kGather);   // staging buffer f is free again
+            return true;
+        };
+        uint4 ra[kPer], rb[kPer];
+        float sa[kPer], sb[kPer];
+        fetch_positions(0, pe);
+        fetch_positions(1, po);
+        if (nt > 0) load_tile(0, pe, ra, sa);
+        for (int i = 0; i < nt; i += 2) {
+            if (i + 1 < nt) load_tile(i + 1, po, rb, sb);
+            if (!store_tile(i, ra, sa)) {
+                give_up(27);
+                break;
+            }
+            if (i + 1 >= nt) break;
+            if (i + 2 < nt) load_tile(i + 2, pe, ra, sa);
+            if (!store_tile(i + 1, rb, sb)) {
+                give_up(27);
+                break;
+            }
         }
-        // copies issued but not seen landing (after an abort) land before exit
-        if (warp == 1 && lane == 0)
-            for (int k = waited; k < issued; ++k) mbar_wait(g_full + (k & 1), (k >> 1) & 1, nullptr, kMlaDrainNs);
         if (g == 0 && nt > 0) mbar_wait(q_full, 0, nullptr, kMlaDrainNs);   // Q landed before exit
     } else if (warp <= 4) {
         // ------------------------------------------------------------ gather
@@ -486,29 +503,16 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         float m_used = -INFINITY, l = 0.f;
         int done = 0;
-        // FP8: the row scale of row `lane` of the current tile, loaded a tile
-        // ahead (its position two tiles ahead)
-        auto scale_of = [&](int32_t pos) -> float { return pos >= 0 ? __ldg(row_scale + k0 + pos) : 0.f; };
-        int32_t pos_cur = 0, pos_next = 0;
-        float sc_cur = 0.f;
-        if (kFp8 && nt > 0) {
-            pos_cur = position(tile0 * kTileRows + lane);
-            sc_cur = scale_of(pos_cur);
-            pos_next = position((tile0 + 1) * kTileRows + lane);
-        }
         for (int i = 0; i < nt; ++i) {
             const int s = i & 1;
-            float sc_next = 0.f;
-            int32_t pos_after = -1;
-            if (kFp8) {
-                sc_next = i + 1 < nt ? scale_of(pos_next) : 0.f;
-                pos_after = i + 2 < nt ? position((tile0 + i + 2) * kTileRows + lane) : -1;
-            }
-            const bool vc = kFp8 ? pos_cur >= 0 : position((tile0 + i) * kTileRows + lane) >= 0;
+            const bool vc = position((tile0 + i) * kTileRows + lane) >= 0;
             const uint32_t vmask = __ballot_sync(0xffffffffu, vc);
             // every wait's outcome is agreed by the whole group (bar.red.or),
-            // so the group's barriers always see all of its threads
-            const bool s_ok = mbar_wait(s_full + s, (i >> 1) & 1, abort_flag, wait_ns);
+            // so the group's barriers always see all of its threads. FP8: the
+            // tile's barrier (complete before its S) also orders the gather
+            // threads' row scales before the reads below.
+            const bool s_ok = mbar_wait(s_full + s, (i >> 1) & 1, abort_flag, wait_ns) &&
+                              (!kFp8 || mbar_wait(c_full + i % NST, (i / NST) & 1, abort_flag, wait_ns));
             if (bar_red_or(kSoftBar, kSoft, !s_ok)) {
                 give_up(24);
                 break;
@@ -520,6 +524,7 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
             tc_fence_before_sync();
             mbar_arrive(s_free + s);   // MMA1 of tile i+2 may overwrite this buffer
             // logits in the log2 domain (FP8: times the row's scale)
+            const float sc_cur = kFp8 ? sc_s[(i % NST) * kTileRows + lane] : 1.f;
             float sc[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -530,10 +535,10 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
 #pragma unroll
             for (int c = 0; c < 32; ++c)
                 if ((vmask >> c) & 1u) tmax = fmaxf(tmax, __uint_as_float(v[c]));
-            // new reference maximum: the first finite one, or one that grew past 2^8
+            // new reference maximum: the first finite one, or one that grew past 2^kRescaleLog2
             bool need = false;
             float f = 1.f;
-            if (tmax > -INFINITY && (m_used == -INFINITY || tmax > m_used + 8.f)) {
+            if (tmax > -INFINITY && (m_used == -INFINITY || tmax > m_used + kRescaleLog2)) {
                 f = m_used == -INFINITY ? 0.f : exp2f(m_used - tmax);
                 need = i > 0;   // before the first MMA2, O holds nothing to rescale
                 m_used = tmax;
@@ -550,11 +555,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __
                 if (kFp8) p[c] *= sc[c];   // O gathers p x row scale x code; l sums p
             }
             l += psum;
-            if (kFp8) {
-                pos_cur = pos_next;
-                sc_cur = sc_next;
-                pos_next = pos_after;
-            }
             // factors of tile i in buffer i & 1: the barrier of tile i+1 lies
             // between this tile's reads and the next writes of the same buffer
             float* fac_i = fac + 128 * (i & 1);
