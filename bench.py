@@ -675,7 +675,7 @@ def run_project(args):
     slot = torch.randperm(2 * T, generator=gen)[:T].to(dev)
     q = torch.empty((T, 32, 128), dtype=torch.bfloat16, device=dev)
     w = torch.empty((T, 32), dtype=torch.float32, device=dev)
-    ws = B.workspace(64 << 20, dev)
+    ws = B.workspace(B.indexer_project_workspace_size(T), dev)
     flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
     flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
     call = lambda: B.indexer_project(x, ql, wq, wk, ww, g, b, 1e-6, cache, slot, q=q, w=w, ws=ws)

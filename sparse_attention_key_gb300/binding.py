@@ -177,6 +177,14 @@ def key_layernorm_append(k_raw: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Te
     return k_cache
 
 
+def indexer_project_workspace_size(T: int) -> int:
+    """Bytes of workspace idx_indexer_project needs for T tokens on this device."""
+    L = lib()
+    L.idx_indexer_project_workspace_size.argtypes = [ctypes.c_int32]
+    L.idx_indexer_project_workspace_size.restype = ctypes.c_size_t
+    return int(L.idx_indexer_project_workspace_size(T))
+
+
 def indexer_project(x: torch.Tensor, q_lora: torch.Tensor, w_q: torch.Tensor, w_k: torch.Tensor,
                     w_w: torch.Tensor, ln_w: torch.Tensor, ln_b: torch.Tensor, eps: float,
                     k_cache: torch.Tensor, slot: torch.Tensor, q: torch.Tensor | None = None,
@@ -203,9 +211,7 @@ def indexer_project(x: torch.Tensor, q_lora: torch.Tensor, w_q: torch.Tensor, w_
     _dev(q, "q", _BF16, (T, HEADS, DIM))
     _dev(w, "w", _F32, (T, HEADS))
     L = lib()
-    L.idx_indexer_project_workspace_size.argtypes = [ctypes.c_int32]
-    L.idx_indexer_project_workspace_size.restype = ctypes.c_size_t
-    need = int(L.idx_indexer_project_workspace_size(T))
+    need = indexer_project_workspace_size(T)
     if ws is None:
         ws = workspace(need, x.device)
     P = ctypes.c_void_p

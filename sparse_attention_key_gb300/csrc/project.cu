@@ -57,6 +57,11 @@ namespace lidx {
 
 namespace {
 
+// Splits the finishing kernel loads per round (each round is a dependent
+// memory round trip): 8, or 4 when no product has more splits (fewer
+// registers, so all of a large T's tokens are resident at once).
+constexpr int kFinishRound = 8;
+
 constexpr int kGemmBM = 128;   // rows of A per tile (TMEM lanes)
 constexpr int kGemmBK = 64;    // K per stage: one 128-byte swizzled row
 constexpr int kGemmThreads = 6 * 32;
@@ -381,10 +386,10 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmGroup G, DeviceS
 //     (fp32), and the key LayerNorm of k_pre into row slot[t] of the cache
 //     (ln_row_half_warp, as idx_key_layernorm_append: the same bits; slots
 //     outside [0, cache_rows) write nothing).
-// Loads of up to 4 splits are in flight at a time; the additions keep the
+// Loads of up to kB splits are in flight at a time; the additions keep the
 // split order.
-template <bool kF32Params>
-__global__ void __launch_bounds__(256)
+template <bool kF32Params, int kB>
+__global__ void __launch_bounds__(256, kB <= 4 ? 3 : 2)
 project_finish_kernel(const float* __restrict__ q_partial, int q_splits, uint16_t* __restrict__ q,
                       int q_blocks, const float* __restrict__ kw_partial, int kw_splits, int T,
                       const void* __restrict__ ln_w, const void* __restrict__ ln_b, float eps,
@@ -392,7 +397,6 @@ project_finish_kernel(const float* __restrict__ q_partial, int q_splits, uint16_
                       const int64_t* __restrict__ slot, float* __restrict__ w_out) {
     pdl_wait();
     pdl_launch_dependents();
-    constexpr int kB = 4;   // splits loaded per round
     if ((int)blockIdx.x < q_blocks) {
         constexpr int kNq4 = IDX_HEADS * IDX_DIM / 4;
         const int64_t vecs = (int64_t)T * kNq4;
@@ -418,8 +422,6 @@ project_finish_kernel(const float* __restrict__ q_partial, int q_splits, uint16_
         return;
     }
     const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
-    float2 g[4], b[4];
-    ln_params_half_warp(ln_w, ln_b, kF32Params, hl, g, b);
     const int64_t warp_id = ((int64_t)(blockIdx.x - q_blocks) * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)(gridDim.x - q_blocks) * blockDim.x) >> 5;
     constexpr int kN = IDX_DIM + IDX_HEADS;
@@ -428,6 +430,7 @@ project_finish_kernel(const float* __restrict__ q_partial, int q_splits, uint16_
         const bool ok = t < T;
         float4 ka = make_float4(0.f, 0.f, 0.f, 0.f), kb = ka;
         float2 wv = make_float2(0.f, 0.f);
+        const int64_t sr = ok ? __ldg(slot + t) : -1;   // (issued early: used at the end)
         if (ok) {
             for (int s0 = 0; s0 < kw_splits; s0 += kB) {
                 float4 a[kB], c[kB];
@@ -452,11 +455,12 @@ project_finish_kernel(const float* __restrict__ q_partial, int q_splits, uint16_
         }
         const uint4 kpre = make_uint4(f32x2_to_bf16x2_rn(ka.x, ka.y), f32x2_to_bf16x2_rn(ka.z, ka.w),
                                       f32x2_to_bf16x2_rn(kb.x, kb.y), f32x2_to_bf16x2_rn(kb.z, kb.w));
+        float2 g[4], b[4];   // (loaded here: not live across the split loads)
+        ln_params_half_warp(ln_w, ln_b, kF32Params, hl, g, b);
         uint32_t o16[4];
         ln_row_half_warp(kpre, g, b, eps, o16);   // both half warps take part
         if (ok) {
             *reinterpret_cast<float2*>(w_out + t * IDX_HEADS + 2 * hl) = wv;
-            const int64_t sr = __ldg(slot + t);
             if (sr >= 0 && sr < cache_rows) k_cache[sr * 16 + hl] = make_uint4(o16[0], o16[1], o16[2], o16[3]);
         }
     }
@@ -511,10 +515,13 @@ int max_splits(int64_t pairs) {
 
 // K splits for `pairs` row-tile pairs x column tiles of a product with KB K
 // blocks: the smallest split with the least estimated time, counting waves of
-// items over the clusters (K blocks per item) and the partial sums' extra
+// items over the clusters (K blocks per item), the partial sums' extra
 // traffic (rows x cols x 8 bytes per split, at about 4 K blocks' worth per
-// 512 KB per cluster). Each split keeps at least 2 K blocks when K allows, and
-// there are at most max_splits(pairs) (the workspace holds that many).
+// 512 KB per cluster) and the finishing kernel's dependent rounds of loads
+// (about 3 K blocks' worth each; measured: 56 splits of a few tokens took
+// 19.5 us to sum in rounds of 4, against 17.9 us for the whole GEMM). Each
+// split keeps at least 2 K blocks when K allows, and there are at most
+// max_splits(pairs) (the workspace holds that many).
 int choose_splits(int64_t pairs, int KB, int64_t rows, int cols) {
     const int64_t clusters = cluster_count();
     int cap = KB >= 4 ? KB / 2 : (KB > 0 ? KB : 1);
@@ -525,7 +532,9 @@ int choose_splits(int64_t pairs, int KB, int64_t rows, int cols) {
         const int64_t items = pairs * s;
         const double waves = (double)((items + clusters - 1) / clusters);
         const double kb = (double)((KB + s - 1) / s);
-        const double extra = s > 1 ? (double)s * rows * cols * 8.0 / (512.0 * 1024.0) * 4.0 / clusters : 0.0;
+        const double extra = s > 1 ? (double)s * rows * cols * 8.0 / (512.0 * 1024.0) * 4.0 / clusters +
+                                         3.0 * ((s + kFinishRound - 1) / kFinishRound)
+                                   : 0.0;
         const double cost = waves * kb + extra;
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
@@ -674,10 +683,11 @@ idx_status idx_indexer_project(const uint16_t* x, const uint16_t* q_lora, const 
     pq.items = pq.m_pairs * pq.n_tiles * pq.splits;
     if (pq.items >= cluster_count()) {
         // q alone fills the clusters: cut the key/weight product (bound by
-        // reading x) into items of at most 16 K blocks, interleaved with the
-        // q items, so that every cluster gets a similar share of both
+        // reading x) into at most 4 items per row-tile pair, of at least 16 K
+        // blocks, interleaved with the q items, so that every cluster gets a
+        // similar share of both
         const int fine = (kw.KB + 15) / 16;
-        const int cap = max_splits(kw.m_pairs);
+        const int cap = max_splits(kw.m_pairs) < 4 ? max_splits(kw.m_pairs) : 4;
         kw.splits = fine < 1 ? 1 : (fine > cap ? cap : fine);
     }
     kw.items = kw.m_pairs * kw.n_tiles * kw.splits;
@@ -716,7 +726,9 @@ idx_status idx_indexer_project(const uint16_t* x, const uint16_t* q_lora, const 
     const int q_blocks = pq.out_bf16 ? 0 : (int)((q_vecs + 255) / 256 < 2 * sms ? (q_vecs + 255) / 256 : 2 * sms);
     const int64_t kw_blocks_need = (((int64_t)T + 1) / 2 + 7) / 8;   // a half warp per token
     const int kw_blocks = (int)(kw_blocks_need < 4 * sms ? kw_blocks_need : 4 * sms);
-    auto fin = ln_dtype == IDX_PARAM_F32 ? project_finish_kernel<true> : project_finish_kernel<false>;
+    const bool round4 = kw.splits <= 4 && (pq.out_bf16 || pq.splits <= 4);
+    auto fin = ln_dtype == IDX_PARAM_F32 ? (round4 ? project_finish_kernel<true, 4> : project_finish_kernel<true, kFinishRound>)
+                                         : (round4 ? project_finish_kernel<false, 4> : project_finish_kernel<false, kFinishRound>);
     e = launch_kernel(fin, dim3(q_blocks + kw_blocks), dim3(256), 0, s, 1, (const float*)q_partial,
                       pq.splits, q, q_blocks, (const float*)kw_partial, kw.splits, T, ln_w, ln_b, eps,
                       reinterpret_cast<uint4*>(k_cache), cache_rows, slot, w);
