@@ -187,7 +187,7 @@ def test_scores_real_inputs_within_tolerance(B):
 
 @pytest.mark.parametrize("kind", ["ties", "normal", "mixed", "const", "tiny"])
 @pytest.mark.parametrize("K", [1, 7, 2048])
-@pytest.mark.parametrize("lens", ["short", "mid", "long", "cap", "over_cap"])
+@pytest.mark.parametrize("lens", ["short", "mid", "wide", "long", "cap", "over_cap"])
 def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
     rng = np.random.default_rng(zlib.crc32(f"{kind}/{K}/{lens}".encode()))
     if lens == "short":
@@ -198,6 +198,9 @@ def test_topk_bit_exact_on_synthetic_rows(B, kind, K, lens):
         # around the candidate list's capacity (8192): const rows are all candidates
         n_valid[:10] = [30_000, 16_385, K + 1, 2047, 2048, 2051, 8191, 8192, 8195, 12_289]
         n_valid[:10] = np.maximum(n_valid[:10], K + 1)
+    elif lens == "wide":  # many rows of 40K..53K positions (the agentic chunk's row lengths)
+        n_valid = rng.integers(40_000, 53_001, size=200).astype(np.int32)
+        n_valid[:8] = [53_000, 52_999, 12_289, K + 1, 2048, 2047, 49_999, 1]
     elif lens == "long":   # few long rows
         n_valid = np.array([70_000, 131_072, 65_537, K + 3, 100_001], np.int32)
         if kind in ("normal", "ties"):
