@@ -52,11 +52,19 @@ struct TcPlanHeader {
 };
 
 constexpr int kMaxScorerCtas = 1024;   // per-CTA start descriptors in the plan
+// Steps per claim of the work-stealing scorers (score_tc_dyn_kernel). The plan
+// hands each CTA its first chunk: its counter starts at kDynChunk.
+constexpr int kDynChunk = 4;
+// Key tiles of the cache per CTA from which the decode and verification
+// scorers steal work (measured: a 250K-key decode batch, 13 tiles per CTA, is
+// faster with static ranges; 64 histories of 64K-128K keys gain 11%).
+constexpr int kDynMinTilesPerCta = 32;
 
 size_t tc_plan_bytes(int32_t B, int32_t T) {
     const size_t g = (size_t)T + (size_t)B + 1;  // >= number of groups for any GQ >= 1
     return align_up(sizeof(TcPlanHeader), 256) + align_up(g * sizeof(int4), 256) +
-           align_up((g + 1) * sizeof(int32_t), 256) + 2 * kMaxScorerCtas * sizeof(int4);
+           align_up((g + 1) * sizeof(int32_t), 256) + 2 * kMaxScorerCtas * sizeof(int4) +
+           kMaxScorerCtas * sizeof(int32_t);
 }
 
 struct TcPlan {
@@ -67,6 +75,9 @@ struct TcPlan {
     // step within the group, first step of the next group, end of the CTA's
     // range}, [2c+1] = that group's entry of `groups`.
     int4* cta_desc;
+    // Per scorer CTA c: steps of its range already handed out (chunks are
+    // claimed by atomicAdd; see score_tc_dyn_kernel). Set by the plan.
+    int32_t* claim;
     int32_t capacity;    // entries of groups
 };
 
@@ -81,6 +92,7 @@ static TcPlan plan_layout(void* base, int32_t B, int32_t T) {
     pl.cta_desc = reinterpret_cast<int4*>(p + align_up(sizeof(TcPlanHeader), 256) +
                                           align_up(g * sizeof(int4), 256) +
                                           align_up((g + 1) * sizeof(int32_t), 256));
+    pl.claim = reinterpret_cast<int32_t*>(pl.cta_desc + 2 * kMaxScorerCtas);
     pl.capacity = (int32_t)g;
     return pl;
 }
@@ -131,6 +143,7 @@ __device__ __forceinline__ void write_cta_desc(const TcPlan& plan, const int32_t
     }
     plan.cta_desc[2 * c] = make_int4(lo, (int)(beg - sb[lo]), sb[lo + 1], (int)end);
     plan.cta_desc[2 * c + 1] = plan.groups[lo];
+    plan.claim[c] = kDynChunk;
 }
 
 // Descriptors of a plan with no steps: every CTA has an empty range.
@@ -138,6 +151,7 @@ __device__ __forceinline__ void write_empty_descs(const TcPlan& plan, int grid) 
     for (int c = threadIdx.x; c < grid; c += blockDim.x) {
         plan.cta_desc[2 * c] = make_int4(0, 0, 0, 0);
         plan.cta_desc[2 * c + 1] = make_int4(0, 0, 0, 0);
+        plan.claim[c] = 0;
     }
 }
 
@@ -864,6 +878,494 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
+// scorer with work stealing (a few queries per group: decode, verification)
+// ---------------------------------------------------------------------------
+// The SMs of a GB300 do not stream keys at one rate: some are 10-20% slower
+// than the median, always the same ones, so equal static ranges end at
+// different times. Here a CTA takes its (cost-balanced) range in chunks of
+// kDynChunk steps from its own counter, and once the range is used up takes
+// chunks from the CTA with the most steps left. Warp 0 schedules: it claims a
+// chunk, cuts it at group boundaries into segments, hands each segment to the
+// MMA issuer and the epilogue through a ring of descriptors in shared memory,
+// and issues the segment's TMA loads. A group's queries are loaded when the
+// group changes, into the other of two buffers, so that they land while the
+// previous group still computes. The plan gives every CTA its first chunk,
+// and the claim of the next own chunk is issued before the current chunk's
+// loads, so the counters' latency stays off the stream of key tiles.
+constexpr int kDynSegs = 8;      // segment descriptors in flight
+
+struct DynSeg {
+    int32_t s0, n;      // n steps from step s0; n == 0: no more work
+    int32_t j;          // key tile of s0 within its group
+    int32_t qb;         // bit 0: query buffer; bit 1: the queries are new here
+    int4 desc;          // the group's entry of plan.groups
+};
+
+template <class C>
+struct DynLayout {
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = 2 * C::Q_BYTES;
+    static constexpr int EPI_OFF = K_OFF + C::STAGES * C::K_STAGE;
+    static constexpr int BAR_OFF = EPI_OFF + C::EPI_BYTES;
+    static constexpr int NBARS = 2 * C::STAGES + 2 * C::NACC + 4 + 2 * kDynSegs + 2;
+    static constexpr int SEG_OFF = (BAR_OFF + NBARS * 8 + 16 + 15) / 16 * 16;
+    static constexpr int HIST_OFF = SEG_OFF + kDynSegs * (int)sizeof(DynSeg);
+    static constexpr int SMEM = HIST_OFF + C::HIST_BINS * 4;
+    static_assert(C::Q_BYTES % 1024 == 0 && K_OFF % 1024 == 0, "swizzled tiles are 1024-byte aligned");
+    static_assert(BAR_OFF % 16 == 0, "barrier alignment");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+score_tc_dyn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                    const float* __restrict__ w, const int32_t* __restrict__ q_pos,
+                    const int32_t* __restrict__ cu_k, int64_t max_len, float* __restrict__ scores,
+                    int64_t ld, TcPlan plan, DeviceStatus* status, uint32_t* __restrict__ row_hist,
+                    uint64_t wait_ns) {
+    using namespace ptx;
+    using Ly = DynLayout<C>;
+    static_assert(C::GQ <= 4, "work stealing is for a few queries per group");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if ((smem_addr(smem_raw) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
+        pdl_wait();
+        if (threadIdx.x == 0) report_error(status, IDX_ERR_UNSUPPORTED, 1024);
+        return;
+    }
+    uint8_t* smem = smem_raw;
+    uint8_t* q_smem = smem + Ly::Q_OFF;
+    uint8_t* k_smem = smem + Ly::K_OFF;
+    float* epi_w = reinterpret_cast<float*>(smem + Ly::EPI_OFF);
+    float** epi_row = reinterpret_cast<float**>(epi_w + C::GQ * 32);
+    int32_t* epi_n = reinterpret_cast<int32_t*>(epi_row + C::GQ);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::BAR_OFF);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = bars + C::STAGES;
+    uint64_t* acc_full = bars + 2 * C::STAGES;
+    uint64_t* acc_empty = acc_full + C::NACC;
+    uint64_t* q_full = acc_empty + C::NACC;     // [2]
+    uint64_t* q_empty = q_full + 2;             // [2]
+    uint64_t* seg_full = q_empty + 2;           // [kDynSegs]
+    uint64_t* seg_empty = seg_full + kDynSegs;  // [kDynSegs]
+    uint64_t* done_bar = seg_empty + kDynSegs;
+    uint64_t* epi_bar = done_bar + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    DynSeg* segs = reinterpret_cast<DynSeg*>(smem + Ly::SEG_OFF);
+    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + Ly::HIST_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(k_full + s, 1);
+            mbar_init(k_empty + s, 1);
+        }
+        for (int a = 0; a < C::NACC; ++a) {
+            mbar_init(acc_full + a, 1);
+            mbar_init(acc_empty + a, C::EPI_WARPS);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(q_full + b, 1);
+            mbar_init(q_empty + b, 1);
+        }
+        for (int i = 0; i < kDynSegs; ++i) {
+            mbar_init(seg_full + i, 1);
+            mbar_init(seg_empty + i, 1 + C::EPI_WARPS);
+        }
+        mbar_init(done_bar, 1);
+        mbar_init(epi_bar, C::EPI_WARPS);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    bool aborted = false;
+    auto give_up = [&](int site) {
+        if (!*abort_flag) report_error(status, IDX_ERR_TIMEOUT, site);
+        *abort_flag = 1;
+        aborted = true;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------- scheduler + TMA
+        const int me = blockIdx.x;
+        const int4 st = plan.cta_desc[2 * me], sg = plan.cta_desc[2 * me + 1];
+        const int32_t my_beg = st.z - sg.w + st.y, my_end = st.w;
+        int own_g = st.x;            // cursor over the own range (claims only move forward)
+        int32_t own_next = st.z;
+        int4 own_desc = sg;
+        bool own = true;
+        int32_t own_off = 0;         // the first own chunk needs no claim
+        int32_t own_claim = 0;       // lane 0: the claim issued for the next own chunk
+        int seg_slot = 0, stage = 0, qb = 1, last_g = -1;
+        uint32_t seg_phase = 0, phase = 0;
+        int q_uses[2] = {0, 0};
+        int issued[C::STAGES];
+#pragma unroll
+        for (int s = 0; s < C::STAGES; ++s) issued[s] = 0;
+        const uint64_t key_policy = l2_policy_evict_first();
+        while (!aborted) {
+            // ---- claim a chunk [c0, c1) and the cursor at the group holding c0
+            int32_t c0 = 0, c1 = 0, nxt = 0;
+            int g = 0;
+            int4 d = make_int4(0, 0, 0, 0);
+            if (own) {
+                if (own_off < my_end - my_beg) {
+                    c0 = my_beg + own_off;
+                    c1 = min(c0 + kDynChunk, my_end);
+                    g = own_g;
+                    nxt = own_next;
+                    d = own_desc;
+                    // claim the next own chunk now; its offset is read after this
+                    // chunk's loads are issued, so the atomic's latency is hidden
+                    if (lane == 0) own_claim = atomicAdd(plan.claim + me, kDynChunk);
+                } else {
+                    own = false;
+                }
+            }
+            if (!own) {   // the CTA with the most steps left
+                bool got = false;
+                for (int attempt = 0; attempt < 4 && !got; ++attempt) {
+                    int best_v = -1;
+                    int32_t best_rem = 0;
+                    for (int v = lane; v < (int)gridDim.x; v += 32) {
+                        const int4 vs = plan.cta_desc[2 * v];
+                        const int32_t len = vs.w - (vs.z - plan.cta_desc[2 * v + 1].w + vs.y);
+                        const int32_t rem = len - *reinterpret_cast<volatile const int32_t*>(plan.claim + v);
+                        if (rem > best_rem) {
+                            best_rem = rem;
+                            best_v = v;
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const int32_t r2 = __shfl_xor_sync(0xffffffffu, best_rem, o);
+                        const int v2 = __shfl_xor_sync(0xffffffffu, best_v, o);
+                        if (r2 > best_rem || (r2 == best_rem && v2 < best_v)) {
+                            best_rem = r2;
+                            best_v = v2;
+                        }
+                    }
+                    if (best_rem <= 0 || best_v < 0) break;   // nothing left anywhere
+                    int32_t off = 0;
+                    if (lane == 0) off = atomicAdd(plan.claim + best_v, kDynChunk);
+                    off = __shfl_sync(0xffffffffu, off, 0);
+                    const int4 vs = plan.cta_desc[2 * best_v], vg = plan.cta_desc[2 * best_v + 1];
+                    const int32_t vbeg = vs.z - vg.w + vs.y;
+                    if (off < vs.w - vbeg) {
+                        got = true;
+                        c0 = vbeg + off;
+                        c1 = min(c0 + kDynChunk, vs.w);
+                        g = vs.x;
+                        nxt = vs.z;
+                        d = vg;
+                    }
+                }
+                if (!got) break;
+            }
+            // ---- cut the chunk at group boundaries; publish and load each segment
+            int32_t s = c0;
+            while (s < c1 && !aborted) {
+                while (s >= nxt) {   // the group holding step s
+                    ++g;
+                    d = plan.groups[g];
+                    nxt = __ldg(plan.step_begin + g + 1);
+                }
+                const int32_t e = min(c1, nxt);
+                const int32_t j0 = s - (nxt - d.w);
+                const bool new_q = g != last_g;
+                if (new_q) {
+                    qb ^= 1;
+                    last_g = g;
+                }
+                if (lane == 0) {
+                    if (!mbar_wait(seg_empty + seg_slot, seg_phase ^ 1, abort_flag, wait_ns)) give_up(11);
+                    if (!aborted) {
+                        DynSeg sd;
+                        sd.s0 = s;
+                        sd.n = e - s;
+                        sd.j = j0;
+                        sd.qb = qb | (new_q ? 2 : 0);
+                        sd.desc = d;
+                        segs[seg_slot] = sd;
+                        mbar_arrive(seg_full + seg_slot);
+                    }
+                    if (!aborted && new_q) {
+                        if (q_uses[qb] > 0 && !mbar_wait(q_empty + qb, (q_uses[qb] - 1) & 1, abort_flag, wait_ns))
+                            give_up(12);
+                        if (!aborted) {
+                            mbar_arrive_expect_tx(q_full + qb, C::Q_BYTES);
+                            const int32_t qrow0 = d.y * 32;
+                            uint8_t* qdst = q_smem + qb * C::Q_BYTES;
+#pragma unroll
+                            for (int half = 0; half < 2; ++half)
+#pragma unroll
+                                for (int r = 0; r < C::QROWS; r += C::Q_BOX_ROWS)
+                                    tma_load_2d(smem_addr(qdst + half * C::Q_HALF + r * 128), &tmap_q,
+                                                q_full + qb, half * 64, qrow0 + r);
+                            ++q_uses[qb];
+                        }
+                    }
+                    const int32_t key0 = __ldg(cu_k + d.x);
+                    for (int32_t i = 0; i < e - s && !aborted; ++i) {
+                        if (!mbar_wait(k_empty + stage, phase ^ 1, abort_flag, wait_ns)) {
+                            give_up(13);
+                            break;
+                        }
+                        mbar_arrive_expect_tx(k_full + stage, C::K_STAGE);
+                        const int32_t key_row = key0 + (j0 + i) * 128;
+                        uint8_t* dst = k_smem + stage * C::K_STAGE;
+                        tma_load_2d_hint(smem_addr(dst), &tmap_k, k_full + stage, 0, key_row, key_policy);
+                        tma_load_2d_hint(smem_addr(dst + C::K_HALF), &tmap_k, k_full + stage, 64, key_row,
+                                         key_policy);
+                        ++issued[stage];
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                }
+                if (++seg_slot == kDynSegs) {
+                    seg_slot = 0;
+                    seg_phase ^= 1;
+                }
+                aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
+                s = e;
+            }
+            if (own) {
+                own_g = g;
+                own_next = nxt;
+                own_desc = d;
+                own_off = __shfl_sync(0xffffffffu, own_claim, 0);
+            }
+        }
+        if (lane == 0) {
+            if (!aborted) {   // the end marker
+                if (mbar_wait(seg_empty + seg_slot, seg_phase ^ 1, abort_flag, wait_ns)) {
+                    segs[seg_slot].n = 0;
+                    mbar_arrive(seg_full + seg_slot);
+                } else {
+                    give_up(14);
+                }
+            }
+            // let every copy this lane issued land before the CTA may exit
+            for (int s = 0; s < C::STAGES; ++s)
+                if (issued[s] > 0) mbar_wait(k_full + s, (issued[s] - 1) & 1, nullptr, kDrainLimitNs);
+            for (int b = 0; b < 2; ++b)
+                if (q_uses[b] > 0) mbar_wait(q_full + b, (q_uses[b] - 1) & 1, nullptr, kDrainLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdesc = idesc_bf16_f32(128, C::N);
+            const uint32_t q_base = smem_addr(q_smem), k_base = smem_addr(k_smem);
+            int seg_slot = 0, stage = 0, acc = 0, cur_qb = -1;
+            uint32_t seg_phase = 0, phase = 0, aphase = 0;
+            int q_uses[2] = {0, 0};
+            while (!aborted) {
+                if (!mbar_wait(seg_full + seg_slot, seg_phase, abort_flag, wait_ns)) {
+                    give_up(15);
+                    break;
+                }
+                const DynSeg sd = segs[seg_slot];
+                mbar_arrive(seg_empty + seg_slot);
+                if (++seg_slot == kDynSegs) {
+                    seg_slot = 0;
+                    seg_phase ^= 1;
+                }
+                if (sd.n == 0) break;
+                const int qb = sd.qb & 1;
+                if (sd.qb & 2) {   // new queries: the previous buffer is free once its MMAs are done
+                    if (cur_qb >= 0) tc_commit(q_empty + cur_qb);
+                    if (!mbar_wait(q_full + qb, q_uses[qb] & 1, abort_flag, wait_ns)) {
+                        give_up(16);
+                        break;
+                    }
+                    ++q_uses[qb];
+                    cur_qb = qb;
+                }
+                for (int32_t i = 0; i < sd.n && !aborted; ++i) {
+                    if (!mbar_wait(k_full + stage, phase, abort_flag, wait_ns)) {
+                        give_up(17);
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t k_addr = k_base + stage * C::K_STAGE;
+#pragma unroll 1
+                    for (int sub = 0; sub < C::NSUB; ++sub) {
+                        if (!mbar_wait(acc_empty + acc, aphase ^ 1, abort_flag, wait_ns)) {
+                            give_up(18);
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t d_tmem = tmem_base + acc * C::N;
+                        const uint32_t b_addr = q_base + qb * C::Q_BYTES + sub * C::N * 128;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t koff = (kk & 3) * 32;
+                            const uint64_t a_desc = smem_desc_sw128(k_addr + (kk >> 2) * C::K_HALF + koff);
+                            const uint64_t b_desc = smem_desc_sw128(b_addr + (kk >> 2) * C::Q_HALF + koff);
+                            tc_mma_bf16(d_tmem, a_desc, b_desc, kIdesc, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(acc_full + acc);
+                        if (++acc == C::NACC) {
+                            acc = 0;
+                            aphase ^= 1;
+                        }
+                    }
+                    if (aborted) break;
+                    tc_commit(k_empty + stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // every MMA issued so far (and the arrivals of the commits before) completes
+            tc_commit(done_bar);
+            mbar_wait(done_bar, 0, nullptr, kDrainLimitNs);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        constexpr int kSplit = C::EPI_WARPS / 4;
+        constexpr int kQpw = C::NQ / kSplit;
+        const int quarter = warp & 3;
+        const int et = threadIdx.x - 64;
+        const int qoff = ((warp - 2) / 4) * kQpw;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+        int acc = 0, seg_slot = 0;
+        uint32_t aphase = 0, ephase = 0, seg_phase = 0;
+        const bool hist_on = C::HIST_BINS > 0 && row_hist != nullptr;
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_bar);
+            const bool ok = mbar_wait(epi_bar, ephase, abort_flag, wait_ns);
+            ephase ^= 1;
+            if (!ok) give_up(19);
+            return ok;
+        };
+        auto flush_hist = [&](int t) {
+            uint32_t* gh = row_hist + (int64_t)t * C::HIST_BINS;
+            for (int b = et; b < C::HIST_BINS; b += C::EPI_THREADS) {
+                const uint32_t v = hist_s[b];
+                if (v) {
+                    atomicAdd(gh + b, v);
+                    hist_s[b] = 0;
+                }
+            }
+        };
+        if (hist_on)
+            for (int b = et; b < C::HIST_BINS; b += C::EPI_THREADS) hist_s[b] = 0;
+        int hist_row = -1, cur_q0 = -1;
+        while (!aborted) {
+            if (!mbar_wait(seg_full + seg_slot, seg_phase, abort_flag, wait_ns)) {
+                give_up(20);
+                break;
+            }
+            const DynSeg sd = segs[seg_slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(seg_empty + seg_slot);
+            if (++seg_slot == kDynSegs) {
+                seg_slot = 0;
+                seg_phase ^= 1;
+            }
+            if (sd.n == 0) break;
+            if (sd.desc.y != cur_q0) {   // a new group: its weights, causal lengths, row pointers
+                if (!epi_sync()) break;
+                if (hist_on && hist_row >= 0) flush_hist(hist_row);
+                const int q0 = sd.desc.y, nq = sd.desc.z;
+                hist_row = q0;
+                cur_q0 = q0;
+                for (int i = et; i < C::GQ * 32; i += C::EPI_THREADS) {
+                    const int qi = i >> 5;
+                    epi_w[i] = qi < nq ? __ldg(w + (int64_t)(q0 + qi) * 32 + (i & 31)) : 0.f;
+                }
+                if (et < C::GQ) {
+                    const int64_t k0 = __ldg(cu_k + sd.desc.x);
+                    const int64_t len_k = (int64_t)__ldg(cu_k + sd.desc.x + 1) - k0;
+                    int32_t ne = 0;
+                    if (et < nq) {
+                        const int64_t n = (int64_t)__ldg(q_pos + q0 + et) + 1;
+                        if (n >= 1 && n <= len_k && n <= max_len) ne = (int32_t)n;
+                    }
+                    epi_n[et] = ne;
+                    epi_row[et] = scores + (int64_t)(q0 + et) * ld;
+                }
+                if (!epi_sync()) break;
+            }
+            for (int32_t i = 0; i < sd.n && !aborted; ++i) {
+                const int32_t key = (sd.j + i) * 128 + quarter * 32 + lane;
+#pragma unroll 1
+                for (int sub = 0; sub < C::NSUB; ++sub) {
+                    if (!mbar_wait(acc_full + acc, aphase, abort_flag, wait_ns)) {
+                        give_up(21);
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    uint32_t v[kQpw][32];
+#pragma unroll
+                    for (int qi = 0; qi < kQpw; ++qi)
+                        tmem_ld_x32(lane_base + acc * C::N + (qoff + qi) * 32, v[qi]);
+                    tmem_ld_wait(v[0]);
+#pragma unroll
+                    for (int qi = 1; qi < kQpw; ++qi) reg_fence(v[qi]);
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty + acc);
+                    if (++acc == C::NACC) {
+                        acc = 0;
+                        aphase ^= 1;
+                    }
+#pragma unroll
+                    for (int qi = 0; qi < kQpw; ++qi) {
+                        const int q = sub * C::NQ + qoff + qi;
+                        if (key >= epi_n[q]) continue;
+                        const float4* w4 = reinterpret_cast<const float4*>(epi_w + q * 32);
+                        float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int h4 = 0; h4 < 8; ++h4) {
+                            const float4 ww = w4[h4];
+                            const float2 r0 = make_float2(fmaxf(__uint_as_float(v[qi][4 * h4 + 0]), 0.f),
+                                                          fmaxf(__uint_as_float(v[qi][4 * h4 + 1]), 0.f));
+                            const float2 r1 = make_float2(fmaxf(__uint_as_float(v[qi][4 * h4 + 2]), 0.f),
+                                                          fmaxf(__uint_as_float(v[qi][4 * h4 + 3]), 0.f));
+                            acc2 = __ffma2_rn(make_float2(ww.x, ww.y), r0, acc2);
+                            acc2 = __ffma2_rn(make_float2(ww.z, ww.w), r1, acc2);
+                        }
+                        const float S = acc2.x + acc2.y;
+                        epi_row[q][key] = S;
+                        if (hist_on) atomicAdd(&hist_s[score_key(S) >> 20], 1u);
+                    }
+                }
+            }
+        }
+        if (hist_on && !aborted && hist_row >= 0 && epi_sync()) flush_hist(hist_row);
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
@@ -926,6 +1428,19 @@ static cudaError_t launch_cfg(const ScoreArgs& a, const TcPlan& plan, cudaStream
                                   a.zero_status, reinterpret_cast<uint4*>(a.zero_ptr), zero_vec,
                                   dev.sm_count);
     if (e != cudaSuccess) return e;
+    // A few queries per group and enough key tiles per CTA (the keys of the
+    // cache bound the steps): work stealing between the CTAs. With less work
+    // per CTA the claims and the final search for work would cost more than
+    // the imbalance they remove.
+    const bool steal = C::GQ <= 4 && (a.n_keys + 127) / 128 >= (int64_t)kDynMinTilesPerCta * dev.sm_count;
+    if constexpr (C::GQ <= 4) if (steal) {
+        constexpr int kSmem = DynLayout<C>::SMEM;
+        e = ensure_smem_optin((const void*)score_tc_dyn_kernel<C>, kSmem);
+        if (e != cudaSuccess) return e;
+        return launch_kernel(score_tc_dyn_kernel<C>, dim3(dev.sm_count), dim3(C::THREADS), (size_t)kSmem,
+                             stream, 1, tk, tq, a.w, a.q_pos, a.cu_k, a.max_len, a.scores, a.ld, plan,
+                             a.status, row_hist, g_wait_limit_ns.load());
+    }
     e = ensure_smem_optin((const void*)score_tc_kernel<C>, C::SMEM);
     if (e != cudaSuccess) return e;
     return launch_kernel(score_tc_kernel<C>, dim3(dev.sm_count), dim3(C::THREADS), (size_t)C::SMEM,

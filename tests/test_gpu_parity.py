@@ -511,6 +511,29 @@ def test_indexer_many_rows_long_histories_real_values(B):
     _check_tolerance(B, w, list(range(w.T)))
 
 
+def _stealing_batch(seed, per_seq, kind, positions):
+    # 30 sequences of 1..60K keys: more than 32 key tiles of cache per SM, so
+    # the decode (1 query per sequence) and verification (4) scorers share
+    # their work between CTAs
+    rng = np.random.default_rng(seed)
+    k_lens = rng.integers(per_seq, 60_001, size=30).tolist()
+    k_lens[:3] = [60_000, per_seq, 2049]
+    w = wl.custom(seed, q_counts=[per_seq] * 30, k_lens=k_lens, kind=kind, positions=positions)
+    assert int(w.cu_k[-1]) // 128 >= 32 * 152
+    return w
+
+
+@pytest.mark.parametrize("per_seq", [1, 4])
+def test_indexer_work_stealing_scorers_integer_ties_exact(B, per_seq):
+    _check_exact(B, _stealing_batch(411 + per_seq, per_seq, "int2", "random"))
+
+
+@pytest.mark.parametrize("per_seq", [1, 4])
+def test_indexer_work_stealing_scorers_real_values_all_rows(B, per_seq):
+    w = _stealing_batch(421 + per_seq, per_seq, "normal", "chunk")
+    _check_tolerance(B, w, list(range(w.T)))
+
+
 def test_indexer_decode_integer_ties_long_histories(B):
     # one query per sequence (the scorer histograms the first digit itself) on
     # integer inputs: tie groups far larger than the selection's candidate list
