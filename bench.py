@@ -142,7 +142,7 @@ KERNEL_SOURCES = {"key_layernorm": "layernorm.cu", "score": "score_tc.cu", "topk
 def _kernel_class(name: str):
     if "key_layernorm" in name:
         return "key_layernorm"
-    if "score_tc_kernel" in name:
+    if "score_tc_kernel" in name or "score_tc_dyn_kernel" in name:
         return "score"
     if "topk" in name:
         return "topk"
