@@ -30,12 +30,19 @@ def B():
     return binding
 
 
-@pytest.mark.parametrize("shape", ["decode", "prefill"])
+@pytest.mark.parametrize("shape", ["decode", "prefill", "decode_steal", "verify_steal"])
 def test_zero_wait_bound_reports_timeout_and_context_survives(B, shape):
+    # "_steal": a cache of more than 32 key tiles per SM, so the decode (one
+    # query per sequence) and verification (four) scorers share work between
+    # their CTAs, and their scheduling warp's waits are bounded too
     if shape == "decode":
         w = wl.custom(701, q_counts=[1, 1, 1], k_lens=[30000, 9000, 20000], kind="int2")
-    else:
+    elif shape == "prefill":
         w = wl.custom(702, q_counts=[300], k_lens=[3000], kind="int2")
+    else:
+        per = 1 if shape == "decode_steal" else 4
+        w = wl.custom(703, q_counts=[per] * 3, k_lens=[300000, 200000, 150000], kind="int2")
+        assert int(w.cu_k[-1]) // 128 >= 32 * 152
     d = to_device(w)
     ws = B.workspace(B.score_topk_workspace_size(w.B, w.T, w.max_len), "cuda")
     old = B.set_wait_limit_ns(0)
