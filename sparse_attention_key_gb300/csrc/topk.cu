@@ -336,6 +336,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
     constexpr int kD1Shift = 32 - D1;
     using S = TopkSmem<THREADS, D1>;
     __shared__ S sh;
+    __shared__ uint32_t s_d3_and[THREADS / 32], s_d3_or[THREADS / 32];
     // dynamic: keys[stage_cap] | above[nw_cap] | tie[nw_cap]
     extern __shared__ __align__(16) uint32_t dyn[];
     uint32_t* keys = dyn;
@@ -387,7 +388,12 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         uint32_t prefix = sh.sel_bin << kD1Shift;
         uint32_t rank = sh.sel_rank;
 
-        // ---- digits 2 and 3 among the keys that match the digits so far
+        // ---- digits 2 and 3 among the keys that match the digits so far.
+        // The second digit's pass also ANDs and ORs the third digit of the
+        // keys it counts; when those agree, every key sharing the first two
+        // digits is the same key (integer scores, for instance, leave the
+        // low key bits equal), and the third round is skipped.
+        constexpr uint32_t kD3Mask = (1u << kD3Bits) - 1u;
 #pragma unroll 1
         for (int d = 0; d < 2; ++d) {
             const int shift = d == 0 ? kD3Bits : 0;
@@ -397,18 +403,43 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
             __syncthreads();
             zero<THREADS>(sh.hist, 1 << bits);
             __syncthreads();
+            uint32_t d3_and = kD3Mask, d3_or = 0u;
             auto add = [&](uint32_t kk) {
-                if ((kk & mask_hi) == prefix) atomicAdd(&sh.hist[swz((kk >> shift) & bin_mask)], 1u);
+                if ((kk & mask_hi) == prefix) {
+                    atomicAdd(&sh.hist[swz((kk >> shift) & bin_mask)], 1u);
+                    d3_and &= kk;
+                    d3_or |= kk;
+                }
             };
             for (int32_t v = threadIdx.x; v < nvec; v += THREADS) {
                 const uint4 k = reinterpret_cast<const uint4*>(keys)[v];
                 add(k.x); add(k.y); add(k.z); add(k.w);
             }
             if (threadIdx.x < n - tail0) add(keys[tail0 + threadIdx.x]);
+            if (d == 0) {
+                d3_and = __reduce_and_sync(0xffffffffu, d3_and);
+                d3_or = __reduce_or_sync(0xffffffffu, d3_or);
+                if ((threadIdx.x & 31) == 0) {
+                    s_d3_and[threadIdx.x >> 5] = d3_and;
+                    s_d3_or[threadIdx.x >> 5] = d3_or;
+                }
+            }
             __syncthreads();
             select_bin_swz<THREADS>(sh, 1 << bits, rank);
             prefix |= sh.sel_bin << shift;
             rank = sh.sel_rank;
+            if (d == 0) {   // (the barriers above ordered the per-warp values; the same outcome everywhere)
+                uint32_t a = kD3Mask, o = 0u;
+#pragma unroll
+                for (int i = 0; i < THREADS / 32; ++i) {
+                    a &= s_d3_and[i];
+                    o |= s_d3_or[i];
+                }
+                if ((a & kD3Mask) == (o & kD3Mask) && rank > 0) {
+                    prefix |= o & kD3Mask;
+                    break;
+                }
+            }
         }
         const uint32_t tau = prefix;
         const uint32_t need = rank;   // tau-valued keys kept; every key above tau is kept
