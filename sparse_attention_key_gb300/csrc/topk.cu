@@ -444,18 +444,17 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         const uint32_t tau = prefix;
         const uint32_t need = rank;   // tau-valued keys kept; every key above tau is kept
 
-        // ---- mark: one thread per 32-position word, no atomics
-        for (int32_t w = threadIdx.x; w < nw; w += THREADS) {
-            uint32_t a = 0, e = 0;
-            const int32_t p0 = w << 5;
-            const int32_t m = n - p0 < 32 ? n - p0 : 32;
-            for (int32_t b = 0; b < m; ++b) {
-                const uint32_t kk = keys[p0 + b];
-                a |= (kk > tau ? 1u : 0u) << b;
-                e |= (kk == tau ? 1u : 0u) << b;
+        // ---- mark: a warp per 32-position word, one key per lane (consecutive
+        // keys, no bank conflicts); the two ballots are the word's bits
+        for (int32_t w = threadIdx.x >> 5; w < nw; w += THREADS / 32) {
+            const int32_t p = (w << 5) + (threadIdx.x & 31);
+            const uint32_t kk = p < n ? keys[p] : 0u;
+            const uint32_t a = __ballot_sync(0xffffffffu, p < n && kk > tau);
+            const uint32_t e = __ballot_sync(0xffffffffu, p < n && kk == tau);
+            if ((threadIdx.x & 31) == 0) {
+                above[w] = a;
+                tie[w] = e;
             }
-            above[w] = a;
-            tie[w] = e;
         }
         __syncthreads();
 
