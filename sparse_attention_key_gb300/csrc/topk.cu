@@ -270,7 +270,50 @@ __device__ __forceinline__ void emit_ordered(S& sh, const uint32_t* above, const
     }
 }
 
-// True when a bounded wait of the scorer that ran before this kernel in the
+// emit_ordered with warps instead of threads: warp w owns a contiguous range
+// of words; its lanes count their words' bits, one exchange of the warps'
+// totals through shared memory (cnt_a / cnt_t: THREADS / 32 words each) gives
+// every warp its offsets, and the warp then walks its words one at a time,
+// one bit per lane, so that consecutive lanes write consecutive outputs. One
+// block barrier instead of a block scan's three. Writes stay inside out[0..K).
+template <int THREADS>
+__device__ __forceinline__ void emit_ordered_warps(const uint32_t* above, const uint32_t* tie, int32_t nw,
+                                                   int32_t* out, uint32_t K, uint32_t need,
+                                                   uint32_t* cnt_a, uint32_t* cnt_t) {
+    constexpr int kWarps = THREADS / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    need = need < K ? need : K;
+    const uint32_t n_above = K - need;
+    const int32_t per = (nw + kWarps - 1) / kWarps;
+    const int32_t w0 = warp * per < nw ? warp * per : nw;
+    const int32_t w1 = w0 + per < nw ? w0 + per : nw;
+    uint32_t ca = 0, ct = 0;
+    for (int32_t w = w0 + lane; w < w1; w += 32) {
+        ca += __popc(above[w]);
+        ct += __popc(tie[w]);
+    }
+    ca = __reduce_add_sync(0xffffffffu, ca);
+    ct = __reduce_add_sync(0xffffffffu, ct);
+    if (lane == 0) {
+        cnt_a[warp] = ca;
+        cnt_t[warp] = ct;
+    }
+    __syncthreads();
+    uint32_t pa = __reduce_add_sync(0xffffffffu, lane < warp ? cnt_a[lane] : 0u);
+    uint32_t pt = __reduce_add_sync(0xffffffffu, lane < warp ? cnt_t[lane] : 0u);
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int32_t w = w0; w < w1; ++w) {   // warp-uniform
+        const uint32_t a = above[w], e = tie[w];
+        const int32_t p = (w << 5) + lane;
+        const uint32_t oa = pa + __popc(a & lt), ot = pt + __popc(e & lt);
+        if (((a >> lane) & 1u) && oa < n_above) out[oa] = p;
+        if (((e >> lane) & 1u) && ot < need) out[n_above + ot] = p;
+        pa += __popc(a);
+        pt += __popc(e);
+    }
+}
+
+// True when a bounded wait of the scorer that ran before this kernel in the// True when a bounded wait of the scorer that ran before this kernel in the
 // same call gave up: its staged scores are then incomplete, and every row of
 // the call is written as skipped (-1s, cnt 0) instead of being selected from
 // them. Read after pdl_wait(), when the scorer has completed.
@@ -337,6 +380,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
     using S = TopkSmem<THREADS, D1>;
     __shared__ S sh;
     __shared__ uint32_t s_d3_and[THREADS / 32], s_d3_or[THREADS / 32];
+    __shared__ uint32_t s_cnt_a[THREADS / 32], s_cnt_t[THREADS / 32];
     // dynamic: keys[stage_cap] | above[nw_cap] | tie[nw_cap]
     extern __shared__ __align__(16) uint32_t dyn[];
     uint32_t* keys = dyn;
@@ -459,7 +503,7 @@ topk_staged_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         __syncthreads();
 
         // ---- emit: above positions ascending, then the first `need` ties ascending
-        emit_ordered<THREADS>(sh, above, tie, nw, out, (uint32_t)K, need);
+        emit_ordered_warps<THREADS>(above, tie, nw, out, (uint32_t)K, need, s_cnt_a, s_cnt_t);
         if (cnt && threadIdx.x == 0) cnt[t] = K;
     }
 }
