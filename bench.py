@@ -14,7 +14,10 @@ one JSON line. Per-kernel times come from the same fused call: the library
 records CUDA events between its launches (idx_set_kernel_events). The line
 also carries a by_workload block with the fused-call time, per-kernel times
 and rooflines of the decode batch, prefill ties, long decode and speculative
-verification workloads.
+verification workloads. The e2e figure runs the same public call with the
+inputs copied from pinned host memory and the indices and counts copied back
+inside the timed region, the batch cut into up to four groups of whole
+sequences whose copies overlap the earlier groups' calls.
 
 --impl reference times the CPU oracle (the plain fp64 definition) on the host's
 cores on a bounded row sample of the same workload, as the reference arm.
