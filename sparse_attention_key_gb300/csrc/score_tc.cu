@@ -326,6 +326,11 @@ tc_plan_fast_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict
     __shared__ int s_q0[kPlanSeqs], s_nq[kPlanSeqs], s_lk[kPlanSeqs], s_gofs[kPlanSeqs + 1];
     __shared__ int s_sb[kPlanSbShared + 1];   // groups' first steps, when they fit
     __shared__ int warp_sums[33];
+    // Up to kPlanThreads query rows: their positions are read in the same
+    // round of loads as the sequences' bounds (one dependent round trip less).
+    __shared__ int s_qp[kPlanThreads];
+    const bool qp_pre = T <= kPlanThreads;
+    if (qp_pre && (int)threadIdx.x < T) s_qp[threadIdx.x] = __ldg(q_pos + threadIdx.x);
     if (zero_status && threadIdx.x == 0) {
         status->code = 0;
         status->detail = 0;
@@ -392,7 +397,7 @@ tc_plan_fast_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict
         const int lk = s_lk[b];
         int qp[GQ];
 #pragma unroll
-        for (int i = 0; i < GQ; ++i) qp[i] = i < nq ? __ldg(q_pos + q0 + i) : 0;
+        for (int i = 0; i < GQ; ++i) qp[i] = i < nq ? (qp_pre ? s_qp[q0 + i] : __ldg(q_pos + q0 + i)) : 0;
         int64_t nmax = 0;
 #pragma unroll
         for (int i = 0; i < GQ; ++i) {
