@@ -200,6 +200,20 @@ __device__ __forceinline__ void zero(uint32_t* p, int64_t n) {
 
 __device__ __forceinline__ uint32_t fkey(float x) { return score_key(x); }
 
+// Smallest non-NaN float whose order key is >= z (keys are monotone in the
+// value, with -0 == +0): every float if z is at or below the key of -inf; no
+// float (NaN, so that every comparison is false) if z is above the key of
+// +inf. Otherwise the float whose key is exactly z: positive for
+// z >= 0x80000000, negative below (z is never 0x7FFFFFFF, the key -0 would
+// have before folding). For non-NaN x: fkey(x) >= z  <=>  x >= key_floor(z),
+// denormals included (no flush to zero in this library).
+__device__ __forceinline__ float key_floor(uint64_t z) {
+    if (z <= 0x007FFFFFull) return -__int_as_float(0x7f800000);
+    if (z > 0xFF800000ull) return __int_as_float(0x7fffffff);
+    const uint32_t zz = (uint32_t)z;
+    return __uint_as_float(zz >= 0x80000000u ? (zz ^ 0x80000000u) : ~zz);
+}
+
 // Keys of the 4 scores of vector v (elements 4v..4v+3) of a row, from global.
 __device__ __forceinline__ uint4 gkeys(const float* row, int32_t v) {
     const float4 x = __ldg(reinterpret_cast<const float4*>(row) + v);
@@ -577,24 +591,30 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         uint32_t prefix = b1 << kD1Shift;
         uint32_t rank = sh.sel_rank;
 
-        // ---- split: above b1 -> above bits, in b1 -> cand bits (4-bit masks)
+        // ---- split: above b1 -> above bits, in b1 -> cand bits (4-bit masks).
+        // Compared as floats against the smallest values of bins b1 and b1+1
+        // (finite scores: x >= key_floor(z) exactly when key(x) >= z), which
+        // spares the key conversion of every score.
+        const float f_lo = key_floor((uint64_t)b1 << kD1Shift);         // bin b1 or above
+        const float f_hi = key_floor((uint64_t)(b1 + 1) << kD1Shift);   // above bin b1
         for (int32_t vb = 0; vb < nvec; vb += kUnroll * THREADS) {
-            uint4 k[kUnroll];
+            float4 x[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int32_t v = vb + u * THREADS + threadIdx.x;
-                if (v < nvec) k[u] = gkeys(row, v);
+                if (v < nvec) x[u] = __ldg(reinterpret_cast<const float4*>(row) + v);
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int32_t v = vb + u * THREADS + threadIdx.x;
                 if (v >= nvec) break;
+                const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
                 uint32_t ma = 0, mc = 0;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t d = comp(k[u], j) >> kD1Shift;
-                    ma |= (d > b1 ? 1u : 0u) << j;
-                    mc |= (d == b1 ? 1u : 0u) << j;
+                    const bool a = xs[j] >= f_hi;
+                    ma |= (a ? 1u : 0u) << j;
+                    mc |= (!a && xs[j] >= f_lo ? 1u : 0u) << j;
                 }
                 const uint32_t sh4 = (uint32_t)(v & 7) * 4;   // 4 positions of word v/8
                 if (ma) atomicOr(above + (v >> 3), ma << sh4);
@@ -603,9 +623,9 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         }
         if (threadIdx.x < n - tail0) {
             const int32_t p = tail0 + threadIdx.x;
-            const uint32_t d = fkey(__ldg(row + p)) >> kD1Shift;
-            if (d > b1) set_bit(above, p);
-            else if (d == b1) set_bit(cand, p);
+            const float xf = __ldg(row + p);
+            if (xf >= f_hi) set_bit(above, p);
+            else if (xf >= f_lo) set_bit(cand, p);
         }
         __syncthreads();
 
@@ -1067,20 +1087,6 @@ struct ClusterTopkSmem : TopkSmem<kClThreads, 12> {
     uint32_t seg[kClusterMax + 1];     // leader: first gathered key of each CTA
     uint32_t tau, need, a_off, t_off;  // written by the leader
 };
-
-// Smallest non-NaN float whose order key is >= z (keys are monotone in the
-// value, with -0 == +0): every float if z is at or below the key of -inf; no
-// float (NaN, so that every comparison is false) if z is above the key of
-// +inf. Otherwise the float whose key is exactly z: positive for
-// z >= 0x80000000, negative below (z is never 0x7FFFFFFF, the key -0 would
-// have before folding). For non-NaN x: fkey(x) >= z  <=>  x >= key_floor(z),
-// denormals included (no flush to zero in this library).
-__device__ __forceinline__ float key_floor(uint64_t z) {
-    if (z <= 0x007FFFFFull) return -__int_as_float(0x7f800000);
-    if (z > 0xFF800000ull) return __int_as_float(0x7fffffff);
-    const uint32_t zz = (uint32_t)z;
-    return __uint_as_float(zz >= 0x80000000u ? (zz ^ 0x80000000u) : ~zz);
-}
 
 __global__ void __launch_bounds__(kClThreads)
 topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
