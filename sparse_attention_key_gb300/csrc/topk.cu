@@ -327,7 +327,7 @@ __device__ __forceinline__ void emit_ordered_warps(const uint32_t* above, const 
     }
 }
 
-// True when a bounded wait of the scorer that ran before this kernel in the// True when a bounded wait of the scorer that ran before this kernel in the
+// True when a bounded wait of the scorer that ran before this kernel in the
 // same call gave up: its staged scores are then incomplete, and every row of
 // the call is written as skipped (-1s, cnt 0) instead of being selected from
 // them. Read after pdl_wait(), when the scorer has completed.
@@ -567,24 +567,43 @@ topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
         zero<THREADS>(tie, nw);
         zero<THREADS>(cand, nw);
         __syncthreads();
+        // Counted by the top 12 bits of the score itself (after -0 -> +0),
+        // which spares the key conversion of every score; the counts are then
+        // moved to key order: a non-negative score's key digit is its bits'
+        // digit + 2048, a negative one's 4095 - its bits' digit.
+        static_assert(D1 == 12 && (1 << D1) % THREADS == 0, "raw-digit histogram");
         for (int32_t vb = 0; vb < nvec; vb += kUnroll * THREADS) {
-            uint4 k[kUnroll];
+            float4 x[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int32_t v = vb + u * THREADS + threadIdx.x;
-                if (v < nvec) k[u] = gkeys(row, v);
+                if (v < nvec) x[u] = __ldg(reinterpret_cast<const float4*>(row) + v);
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 if (vb + u * THREADS + threadIdx.x >= nvec) break;
-                atomicAdd(&sh.hist[k[u].x >> kD1Shift], 1u);
-                atomicAdd(&sh.hist[k[u].y >> kD1Shift], 1u);
-                atomicAdd(&sh.hist[k[u].z >> kD1Shift], 1u);
-                atomicAdd(&sh.hist[k[u].w >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[__float_as_uint(__fadd_rn(x[u].x, 0.0f)) >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[__float_as_uint(__fadd_rn(x[u].y, 0.0f)) >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[__float_as_uint(__fadd_rn(x[u].z, 0.0f)) >> kD1Shift], 1u);
+                atomicAdd(&sh.hist[__float_as_uint(__fadd_rn(x[u].w, 0.0f)) >> kD1Shift], 1u);
             }
         }
         if (threadIdx.x < n - tail0)
-            atomicAdd(&sh.hist[fkey(__ldg(row + tail0 + threadIdx.x)) >> kD1Shift], 1u);
+            atomicAdd(&sh.hist[__float_as_uint(__fadd_rn(__ldg(row + tail0 + threadIdx.x), 0.0f)) >> kD1Shift],
+                      1u);
+        __syncthreads();
+        {
+            constexpr int kPer = (1 << D1) / THREADS;
+            uint32_t c[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) c[i] = sh.hist[threadIdx.x + i * THREADS];
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const uint32_t rb = threadIdx.x + i * THREADS;
+                sh.hist[rb < 2048u ? rb + 2048u : 4095u - rb] = c[i];
+            }
+        }
         __syncthreads();
         select_bin<THREADS>(sh, 1 << D1, (uint32_t)K);
         const uint32_t b1 = sh.sel_bin;
