@@ -220,10 +220,6 @@ __device__ __forceinline__ uint4 gkeys(const float* row, int32_t v) {
     return make_uint4(fkey(x.x), fkey(x.y), fkey(x.z), fkey(x.w));
 }
 
-__device__ __forceinline__ uint32_t comp(const uint4& k, int j) {
-    return j == 0 ? k.x : j == 1 ? k.y : j == 2 ? k.z : k.w;
-}
-
 // Ask L2 to fetch [p, p + bytes) ahead of the reads (p 16-byte aligned, bytes
 // a multiple of 16).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
