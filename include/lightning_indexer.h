@@ -40,7 +40,9 @@
  *   Workspace  ws / ws_bytes: caller-owned device scratch, at least the size the
  *              matching *_workspace_size function returns, 256-byte aligned. It
  *              holds the status word, the tile plan and staged scores. Calls that
- *              may overlap on the GPU need separate workspaces.
+ *              may overlap on the GPU need separate workspaces. For arguments
+ *              that the call itself rejects (B < 1, T < 0, max_len < 1) the size
+ *              functions return the 256-byte header size.
  */
 #ifndef LIGHTNING_INDEXER_H
 #define LIGHTNING_INDEXER_H

@@ -229,6 +229,7 @@ idx_status idx_key_layernorm_append(const uint16_t* k_raw, const void* ln_w, con
 }
 
 size_t idx_score_workspace_size(int32_t B, int32_t T, int64_t /*max_len*/) {
+    if (B < 1 || T < 0) return kWsHeader;   // arguments the call rejects
     return kWsHeader + align_up(score_plan_bytes(B, T), 256);
 }
 
@@ -284,7 +285,7 @@ idx_status idx_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
 }
 
 size_t idx_score_topk_workspace_size(int32_t B, int32_t T, int64_t max_len, int32_t /*topk*/) {
-    if (T < 0 || max_len < 1) return kWsHeader;
+    if (B < 1 || T < 0 || max_len < 1) return kWsHeader;   // arguments the call rejects
     return kWsHeader + align_up(score_plan_bytes(B, T), 256) +
            align_up((size_t)T * (size_t)staged_ld(max_len) * sizeof(float), 256) +
            align_up(topk_scratch_bytes(T, max_len), 256);

@@ -59,6 +59,16 @@ def test_workspace_sizes_are_host_only(L):
     s = binding.score_topk_workspace_size(4, 3200, 50800, 2048)
     assert s >= 3200 * 50800 * 4
     assert s % 256 == 0
+    # arguments the calls reject: the header size, not a wrapped-around count
+    assert binding.score_topk_workspace_size(0, 3200, 50800, 2048) == 256
+    assert binding.score_topk_workspace_size(4, -1, 50800, 2048) == 256
+    assert binding.score_topk_workspace_size(4, 3200, 0, 2048) == 256
+    assert binding.topk_workspace_size(-1, 50800, 2048) == 256
+    L.idx_score_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]
+    L.idx_score_workspace_size.restype = ctypes.c_size_t
+    assert L.idx_score_workspace_size(0, 10, 100) == 256
+    assert L.idx_score_workspace_size(2, -3, 100) == 256
+    assert L.idx_score_workspace_size(2, 10, 100) > 256
 
 
 # Host argument errors: each returns its code with no CUDA call (no GPU here).
