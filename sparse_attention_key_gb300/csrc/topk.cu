@@ -10,8 +10,10 @@
 //
 // Scores become order-preserving uint32 keys (-0 folded onto +0). The K-th
 // largest key tau is found by most-significant-digit radix select over three
-// digits: bits 31..(32-D1), (31-D1)..10 and 9..0. One block per row, with the
-// row's positions tracked in bitmaps (one bit per position):
+// digits: bits 31..(32-D1), (31-D1)..10 and 9..0. One block per row (for a
+// few long rows, a thread-block cluster per row; beyond 2^21 positions,
+// slice-parallel kernels), with the row's positions tracked in bitmaps (one
+// bit per position):
 //
 //   pass A   histogram of the first digit; the bin b1 holding rank K (counted
 //            from the top) follows.
@@ -29,10 +31,14 @@
 //            in increasing order.
 // Short rows (staged kernel) are copied into shared memory as keys during pass
 // A; every later step reads that copy. Long rows (streamed kernel) are first
-// requested into L2 as a whole (bulk prefetch), then read twice (pass A and the
-// split); the candidates' keys are gathered once into a shared-memory list
-// that digits 2-3 and the mark read (or, when the list would overflow, gathered
-// again at each step). No block waits on another.
+// requested into L2 as a whole (bulk prefetch), then read twice: pass A counts
+// the first digit of the scores' own bits (moved into key order afterwards)
+// and the split compares the scores as floats with the bounds of bin b1, so
+// neither converts every score to its key; the candidates' keys are gathered
+// once into a shared-memory list that digits 2-3 and the mark read (or, when
+// the list would overflow, gathered again at each step). No block waits on
+// another except through the cluster barriers, which every CTA of a cluster
+// reaches.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
