@@ -15,9 +15,13 @@
 // Work decomposition. Queries of a sequence form groups of GQ = NQ * NSUB
 // consecutive rows; a group needs ceil(max n(t) / 128) key tiles ("steps"). A
 // plan kernel lists the groups and prefix-sums their steps; the scorer runs
-// one CTA per SM and gives each CTA an equal contiguous range of steps, so a
-// CTA streams key tiles of one group while the group's queries stay resident
-// in shared memory.
+// one CTA per SM and gives each CTA a contiguous range of steps of equal cost
+// (a step costs 1, the start of a group kGroupStartCost more), so a CTA streams
+// key tiles of one group while the group's queries stay resident in shared
+// memory. With one or four queries per group and a large cache,
+// score_tc_dyn_kernel starts from the same ranges but claims them in chunks
+// and takes chunks from the CTA with the most steps left: some SMs pull keys
+// from HBM more slowly than others, and static ranges leave them last.
 //
 // Roles inside a CTA (warp specialisation):
 //   warp 0        TMA producer: the group's Q tile once per group, then key
