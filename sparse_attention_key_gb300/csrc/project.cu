@@ -104,11 +104,12 @@ struct GemmGroup {
     int items;         // all problems' items
 };
 
-struct alignas(64) GemmMaps {
+struct GemmMaps {   // CUtensorMap's own alignment keeps every map 64-byte aligned
     CUtensorMap a[2];      // A of each problem
     CUtensorMap b[2][3];   // B maps of each problem (BSeg::map)
     CUtensorMap out[2];    // output (bf16 2-D, or fp32 partials 3-D)
 };
+static_assert(alignof(GemmMaps) >= 64 && sizeof(CUtensorMap) % 64 == 0, "tensor maps 64-byte aligned");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -643,7 +644,6 @@ idx_status idx_indexer_project(const uint16_t* x, const uint16_t* q_lora, const 
         return proj_fail(IDX_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300) only");
     cudaStream_t s = (cudaStream_t)stream;
     DeviceStatus* status = static_cast<DeviceStatus*>(ws);
-    float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s);
     if (e != cudaSuccess) return proj_fail(IDX_ERR_CUDA, cudaGetErrorString(e));
 

@@ -293,13 +293,13 @@ tc_plan_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict__ cu
         return;
     }
     __syncthreads();   // step_begin and groups are complete
-    if (GQ > 4) {   // several queries per group: CTA c's first step, steps shared uniformly
+    if constexpr (GQ > 4) {   // several queries per group: CTA c's first step, steps shared uniformly
         for (int c = threadIdx.x; c < grid; c += kPlanThreads)
             plan.cta_desc[2 * c].x = (int32_t)((int64_t)carry * c / grid);
-        return;
+    } else {
+        for (int c = threadIdx.x; c < grid; c += kPlanThreads)
+            write_cta_desc(plan, plan.step_begin, n_groups, carry, grid, c, false);
     }
-    for (int c = threadIdx.x; c < grid; c += kPlanThreads)
-        write_cta_desc(plan, plan.step_begin, n_groups, carry, grid, c, false);
 }
 
 // Fast plan for up to kPlanSeqs sequences: one thread per sequence reads its
@@ -438,17 +438,18 @@ tc_plan_fast_kernel(const int32_t* __restrict__ q_pos, const int32_t* __restrict
         return;
     }
     __syncthreads();   // step offsets and groups are complete
-    if (GQ > 4) {
+    if constexpr (GQ > 4) {
         // several queries per group: [2c].x = the first step of CTA c, the
         // steps shared by cost (uniform when the group starts are not in
         // shared memory)
         for (int c = threadIdx.x; c < grid; c += kPlanThreads)
             plan.cta_desc[2 * c].x = sb_shared ? cost_boundary(s_sb, n_groups, total, grid, c)
                                                : (int32_t)((int64_t)total * c / grid);
-        return;
+    } else {
+        for (int c = threadIdx.x; c < grid; c += kPlanThreads)
+            write_cta_desc(plan, sb_shared ? s_sb : plan.step_begin, n_groups, total, grid, c,
+                           sb_shared);
     }
-    for (int c = threadIdx.x; c < grid; c += kPlanThreads)
-        write_cta_desc(plan, sb_shared ? s_sb : plan.step_begin, n_groups, total, grid, c, sb_shared);
 }
 
 // ---------------------------------------------------------------------------
